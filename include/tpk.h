@@ -1,0 +1,236 @@
+/*
+ * tpk.h -- C ABI of the prefix-tree-packed DFS attention library (GB300, sm_103a).
+ *
+ * The library computes attention over training rows packed as a prefix tree:
+ * sequences that share a token prefix are laid out once, depth first, in
+ * fixed-capacity rows; every token attends only to itself and its
+ * root-to-leaf ancestors; position ids are tree depths; a token_index maps
+ * every raw token back to its forwarded position.  The pages that define the
+ * method:
+ *   [ART]  "Prefix Tree Packing in ART" -- sections "The tree" (recursive
+ *          longest-run walk, minimum shared-segment length, duplicated join
+ *          token), "One tree, not one per group", "Bin packing, with a twist"
+ *          (best-fit decreasing over marginal cost), "Token-mixing layers"
+ *          (tree mask = full ancestor blocks + causal own block; [enter, exit]
+ *          interval ancestor test), "Metadata space first".
+ *   [DAG]  "DAG packing" -- sections "The walk" (depth-first layout, last
+ *          common node copied per child), "The mask", "Positions" (depth).
+ *   [TRL]  "TRL Tree Packing for AsyncGRPO" -- section "How tree packing
+ *          works" (planner -> collator -> attention; token_index).
+ *
+ * Conventions for every call
+ *  - Return value: TPK_OK (0) or a negative TPK_E_* code; tpk_status_string()
+ *    names it.  No call aborts the process.
+ *  - Memory: the library never allocates device memory.  The caller owns
+ *    every device buffer (PyTorch in the bundled binding) and the stream.
+ *    Plan handles live in host memory owned by the library until
+ *    tpk_plan_destroy().
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *    default stream).  GPU calls only enqueue work; they never synchronise.
+ *  - Layouts (row-major, contiguous):
+ *      Q, O      [F, Hq, d]  bf16, forwarded order (rows concatenated)
+ *      K, V      [F, Hkv, d] bf16
+ *      LSE       [Hq, F]     fp32, natural log
+ *      raw-order outputs: [R, Hq, d] bf16 and [Hq, R] fp32, raw order = the
+ *      concatenation of the input sequences by seq_offsets.
+ *    Grouped-query attention: query head h reads key/value head h / (Hq/Hkv).
+ *  - Device errors: attention kernels bound every wait; a wait that gives up
+ *    writes TPK_E_TIMEOUT to *dev_err (device int32, caller-initialised to 0)
+ *    and the kernel exits cleanly.  Read it after synchronising.
+ *  - There is no CPU fallback: GPU entry points return TPK_E_CUDA or
+ *    TPK_E_UNSUPPORTED when no sm_103 device is usable.
+ */
+#ifndef TPK_H_
+#define TPK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define TPK_OK               0
+#define TPK_E_ARG           -1  /* bad argument (NULL pointer, size, offsets) */
+#define TPK_E_SEQ_TOO_LONG  -2  /* a sequence is longer than row_capacity */
+#define TPK_E_OVERFLOW      -3  /* F, R or a table size does not fit int32 */
+#define TPK_E_UNSUPPORTED   -4  /* head_dim not in {64,128}, Hq % Hkv != 0, no sm_103 device */
+#define TPK_E_CUDA          -5  /* a CUDA runtime/driver call failed */
+#define TPK_E_TIMEOUT       -6  /* a device wait gave up (read from dev_err) */
+#define TPK_E_WORKSPACE     -7  /* workspace missing or smaller than required */
+
+/* ---- placement rules ---------------------------------------------------- */
+#define TPK_PLACE_BFD       0   /* [ART] "Bin packing, with a twist": best-fit decreasing
+                                   over marginal cost (the default) */
+#define TPK_PLACE_NEXT_FIT  1   /* [ART] "One tree, not one per group": fill rows in
+                                   order, open a new row when the next leaf does not fit */
+
+typedef struct tpk_plan tpk_plan;   /* opaque, host memory */
+
+typedef struct {
+    int64_t row_capacity;  /* forwarded tokens per row ([ART] intro: row length set by
+                              memory; [TRL] token_budget counts forwarded tokens) */
+    int32_t min_shared;    /* minimum shared-segment length ([ART] "The tree": shorter
+                              shared runs are copied into each branch); <=1 disables */
+    int32_t placement;     /* TPK_PLACE_BFD or TPK_PLACE_NEXT_FIT */
+} tpk_plan_opts;
+
+typedef struct {
+    int64_t n_seqs;        /* input sequences */
+    int64_t n_rows;        /* packed rows */
+    int64_t n_fwd;         /* F: forwarded positions over all rows */
+    int64_t n_raw;         /* R: raw tokens */
+    int64_t n_segments;    /* segments of the global prefix tree */
+    int64_t n_leaves;      /* distinct sequences */
+    int64_t n_qtiles;      /* 128-query tiles (forward work list) */
+    int64_t n_kblocks;     /* key blocks over all query tiles */
+    int64_t n_ktiles;      /* 128-key tiles (backward work list) */
+    int64_t n_qblocks;     /* query blocks over all key tiles */
+    int64_t useful_pairs;  /* sum over forwarded f of depth[f]+1: visible (query, key) pairs */
+    int64_t visited_pairs; /* query rows x key columns the forward kernel visits */
+    int64_t max_depth;
+    double packing_ratio;  /* R / F ([TRL] "How tree packing works") */
+    double row_fill_frac;  /* F / (n_rows * row_capacity) */
+    double fork_frac;      /* segments with >= 2 children / segments */
+} tpk_plan_info;
+
+/* ---- planner (host only, no GPU needed) --------------------------------- */
+
+/* Build the packing plan ([ART] "The tree", "Bin packing, with a twist";
+ * [DAG] "The walk", "Positions"; [TRL] "How tree packing works").
+ *   tokens      [R] int32 token ids >= 0, sequences concatenated
+ *   seq_offsets [n_seqs+1] int64, seq_offsets[0] = 0, strictly increasing
+ *               (every sequence has >= 1 token), seq_offsets[n_seqs] = R
+ *   trained     [R] uint8 or NULL (= all 1): 1 if the position's next-token
+ *               prediction carries a loss.  A position is shared only when
+ *               the token prefix, the flags and -- for a trained position --
+ *               its target agree, so the last common token before a fork is
+ *               kept once per branch ([ART] "The tree", off-by-one note).
+ *   group_ids   [n_seqs] int32 or NULL: placement groups (best-fit decreasing
+ *               orders groups by their most expensive leaf).  NULL = the tree
+ *               family (root segment) of each sequence.
+ *   opts        see tpk_plan_opts (NULL = capacity 65536, min_shared 64, BFD)
+ *   out         receives the new plan; free with tpk_plan_destroy.
+ * Errors: TPK_E_ARG (bad offsets / negative token / NULL), TPK_E_SEQ_TOO_LONG,
+ *         TPK_E_OVERFLOW (F or R >= 2^31).  Inputs are copied; the caller
+ *         keeps ownership of its buffers. */
+int tpk_plan_build(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs,
+                   const uint8_t* trained, const int32_t* group_ids,
+                   const tpk_plan_opts* opts, tpk_plan** out);
+
+int tpk_plan_info_get(const tpk_plan* plan, tpk_plan_info* out);
+
+/* Copy the layout into caller-allocated host buffers (any pointer may be NULL):
+ *   row_offsets [n_rows+1] forwarded offset of each row
+ *   row_loads   [n_rows]   forwarded tokens of each row
+ *   row_of_seq  [n_seqs]
+ *   fwd_token   [F]  token id at each forwarded position
+ *   fwd_src     [F]  lowest raw index that maps to the position (its owner)
+ *   parent      [F]  forwarded index of the position one level up, -1 at a root
+ *   depth       [F]  tree depth = position id ([DAG] "Positions")
+ *   token_index [R]  forwarded index of every raw token ([TRL])
+ *   subtree_end [F]  one past the last position of the subtree: key j is visible
+ *                    to query i iff j <= i < subtree_end[j] ([ART] "Token-mixing
+ *                    layers", [enter, exit] interval test) */
+int tpk_plan_export(const tpk_plan* plan, int64_t* row_offsets, int64_t* row_loads,
+                    int32_t* row_of_seq, int32_t* fwd_token, int32_t* fwd_src,
+                    int32_t* parent, int32_t* depth, int32_t* token_index,
+                    int32_t* subtree_end);
+
+/* Kernel work lists (int32, host copies; any pointer may be NULL).
+ * Forward: query tile t covers forwarded [qt_q0[t], qt_q0[t]+qt_nq[t]) inside one
+ * row; its key blocks are kb[2*b], kb[2*b+1] for b in [qt_kb_begin[t],
+ * qt_kb_begin[t+1]): kb[2b] = first key, kb[2b+1] = count | (full << 16), where
+ * full = every key of the block is visible to every query of the tile.  The
+ * key set of a tile is the ancestors of its first query plus the tile itself
+ * (a contiguous ancestor chain of segment intervals, [ART] "Token-mixing layers").
+ * Backward: key tile u covers [kt_k0[u], +kt_nk[u]); its query blocks qb[2c],
+ * qb[2c+1] for c in [kt_qb_begin[u], kt_qb_begin[u+1]) cover [k0, max subtree_end).
+ * qt_order / kt_order list the tiles by decreasing work (longest first). */
+int tpk_plan_worklists(const tpk_plan* plan, int32_t* qt_q0, int32_t* qt_nq,
+                       int32_t* qt_kb_begin, int32_t* kb, int32_t* qt_order,
+                       int32_t* kt_k0, int32_t* kt_nk, int32_t* kt_qb_begin,
+                       int32_t* qb, int32_t* kt_order);
+
+/* Device image of the plan.  The caller allocates tpk_plan_device_bytes()
+ * bytes of device memory (256-byte aligned) and uploads the image with
+ * tpk_plan_upload (async on `stream`; the plan keeps the host image alive until
+ * destroyed).  tpk_plan_field_offset gives the byte offset of a field inside
+ * the image so callers can pass e.g. depth or token_index to the kernels. */
+#define TPK_FIELD_DEPTH        0   /* int32 [F] */
+#define TPK_FIELD_TOKEN_INDEX  1   /* int32 [R] */
+#define TPK_FIELD_SUBTREE_END  2   /* int32 [F] */
+#define TPK_FIELD_PARENT       3   /* int32 [F] */
+size_t tpk_plan_device_bytes(const tpk_plan* plan);
+int tpk_plan_field_offset(const tpk_plan* plan, int32_t field, size_t* offset);
+int tpk_plan_upload(const tpk_plan* plan, void* dev_image, void* stream);
+void tpk_plan_destroy(tpk_plan* plan);
+
+/* ---- GPU kernels (sm_103a) ---------------------------------------------- */
+
+/* RoPE at depth positions ([DAG] "Positions": position id = graph depth, so
+ * every parent->child edge has relative distance 1).  In place on q [F,Hq,d]
+ * and k [F,Hkv,d] (bf16; either may be NULL).  Pair i < d/2 is (x_i, x_{i+d/2})
+ * rotated by angle depth[f] * base^(-2i/d) (by minus that angle when
+ * `inverse` != 0, which maps gradients w.r.t. rotated inputs back to the
+ * un-rotated ones).  Math in fp32 with the angle reduced in fp64; output
+ * rounded to nearest even.  depth: device int32 [F].  d in {64, 128}. */
+int tpk_rope_by_depth(void* q, void* k, const int32_t* depth, int64_t F,
+                      int32_t Hq, int32_t Hkv, int32_t d, double base,
+                      int32_t inverse, void* stream);
+
+/* Workspace bytes for the attention calls (0 for the forward). */
+size_t tpk_attn_workspace_bytes(const tpk_plan* plan, int32_t Hq, int32_t Hkv,
+                                int32_t d, int32_t backward);
+
+/* Tree attention forward ([ART] "Token-mixing layers"; [DAG] "The mask"):
+ * O[f,h] = sum over keys j visible to f of softmax_j(scale * q_f . k_j) v_j,
+ * visible = f itself and its ancestors (j <= f < subtree_end[j]);
+ * LSE[h,f] = ln sum_j exp(scale * q_f . k_j).  q, k are the RoPE-rotated
+ * inputs.  Only key blocks on the query tile's ancestor chain are visited,
+ * so work scales with forwarded tokens, not raw ones.
+ *   plan/dev_image  the plan and its uploaded image
+ *   q [F,Hq,d], k/v [F,Hkv,d], o [F,Hq,d] bf16 (device, 16-byte aligned)
+ *   lse [Hq,F] fp32 (device)
+ *   d in {64,128}; Hq % Hkv == 0; scale > 0 (usually 1/sqrt(d))
+ *   workspace/ws_bytes: may be NULL/0 (none needed)
+ *   dev_err: device int32 set to TPK_E_TIMEOUT if a wait gave up (may be NULL) */
+int tpk_tree_attn_fwd(const tpk_plan* plan, const void* dev_image,
+                      const void* q, const void* k, const void* v,
+                      void* o, float* lse, int32_t Hq, int32_t Hkv, int32_t d,
+                      float scale, void* workspace, size_t ws_bytes,
+                      int32_t* dev_err, void* stream);
+
+/* Tree attention backward: gradients of sum_{f,h} <dout[f,h], O[f,h]> w.r.t.
+ * the rotated q and k and w.r.t. v (apply tpk_rope_by_depth(inverse=1) to dq
+ * and dk for the un-rotated inputs).  o and lse are the forward's outputs.
+ * dk, dv are summed over the query heads of each key/value head.
+ *   workspace: >= tpk_attn_workspace_bytes(plan, Hq, Hkv, d, 1) bytes, 256-byte
+ *   aligned (fp32 dQ accumulator and row terms); contents need not be cleared. */
+int tpk_tree_attn_bwd(const tpk_plan* plan, const void* dev_image,
+                      const void* q, const void* k, const void* v,
+                      const void* o, const float* lse, const void* dout,
+                      void* dq, void* dk, void* dv, int32_t Hq, int32_t Hkv,
+                      int32_t d, float scale, void* workspace, size_t ws_bytes,
+                      int32_t* dev_err, void* stream);
+
+/* Scatter forwarded outputs back to raw-token order ([TRL] "How tree packing
+ * works": token_index maps each raw token to its forwarded position):
+ *   dst[r] = src[token_index[r]]            src [F,H,d] -> dst [R,H,d] bf16
+ *   lse_dst[h,r] = lse_src[h,token_index[r]]  [H,F] -> [H,R] fp32
+ * lse_src/lse_dst may both be NULL; src/dst may both be NULL. */
+int tpk_scatter_token_index(const int32_t* token_index, int64_t R, int64_t F,
+                            const void* src, void* dst, const float* lse_src,
+                            float* lse_dst, int32_t H, int32_t d, void* stream);
+
+const char* tpk_status_string(int status);
+
+/* Library version string. */
+const char* tpk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPK_H_ */

@@ -207,3 +207,86 @@ def backward(plan, Q, K, V, dO, base, scale=None, round_rotated=True):
         np.add.at(dK, path, rope(dk, pos, base, inverse=True))
         np.add.at(dV, path, dv)
     return dQ, dK, dV
+
+
+def _path_rows(plan, r):
+    off = plan["seq_offsets"]
+    s = int(np.searchsorted(off, r, side="right") - 1)
+    p = int(r - off[s])
+    return s, p, plan["token_index"][off[s]:off[s] + p + 1]
+
+
+def backward_rows_q(plan, Q_rows, K_rows, V_rows, dO_rows, raw, base, scale=None):
+    """dQ (w.r.t. un-rotated Q) at the forwarded positions of the raw tokens
+    ``raw``.  A query's own row is the only place its Q enters the loss, so
+    dQ[f] needs only f's own softmax row: P_j, dP_j = dO_f.v_j, D = dO_f.O_f,
+    dS_j = P_j (dP_j - D), dQ_rot = scale sum_j dS_j k_j, then the inverse
+    rotation at f's position.  Returns [n, Hq, d]."""
+    out = []
+    for r in raw:
+        _, p, path = _path_rows(plan, r)
+        q = round_to_bf16(rope(Q_rows(path[-1:]), [p], base))
+        k = round_to_bf16(rope(K_rows(path), np.arange(p + 1), base))
+        v = np.asarray(V_rows(path), dtype=np.float64)
+        do = np.asarray(dO_rows(path[-1:]), dtype=np.float64)[0]
+        hq, d = q.shape[1], q.shape[2]
+        hkv = k.shape[1]
+        sc = 1.0 / np.sqrt(d) if scale is None else scale
+        dq = np.zeros((1, hq, d))
+        for h in range(hq):
+            g = _kv_head(h, hq, hkv)
+            s = (k[:, g, :] @ q[0, h, :]) * sc
+            w = np.exp(s - s.max())
+            pr = w / w.sum()
+            o = pr @ v[:, g, :]
+            dp = v[:, g, :] @ do[h]
+            ds = pr * (dp - do[h] @ o)
+            dq[0, h] = sc * (ds @ k[:, g, :])
+        out.append(rope(dq, [p], base, inverse=True)[0])
+    return np.stack(out)
+
+
+def backward_rows_kv(plan, Q_rows, K_rows, V_rows, dO_rows, fwd, base, scale=None):
+    """dK (w.r.t. un-rotated K) and dV at forwarded key positions ``fwd``.
+
+    Key j receives gradient from every forwarded query that sees it (the
+    positions of its subtree).  Each such query i is taken once, through the
+    sequence owning it (its lowest raw index), with its full softmax row over
+    that sequence's prefix.  Returns ([n, Hkv, d], [n, Hkv, d])."""
+    off = plan["seq_offsets"]
+    ti = plan["token_index"]
+    src = plan["fwd_src"]
+    se = plan["subtree_end"]
+    dks, dvs = [], []
+    for j in fwd:
+        pj = int(plan["depth"][j])
+        dk_acc = None
+        dv_acc = None
+        for i in range(int(j), int(se[j])):
+            r = int(src[i])
+            s, p, path = _path_rows(plan, r)
+            if pj > p or path[pj] != j:
+                continue   # j is not on i's path (a later subtree of the row)
+            q = round_to_bf16(rope(Q_rows(path[-1:]), [p], base))
+            k = round_to_bf16(rope(K_rows(path), np.arange(p + 1), base))
+            v = np.asarray(V_rows(path), dtype=np.float64)
+            do = np.asarray(dO_rows(path[-1:]), dtype=np.float64)[0]
+            hq, d = q.shape[1], q.shape[2]
+            hkv = k.shape[1]
+            sc = 1.0 / np.sqrt(d) if scale is None else scale
+            if dk_acc is None:
+                dk_acc = np.zeros((hkv, d))
+                dv_acc = np.zeros((hkv, d))
+            for h in range(hq):
+                g = _kv_head(h, hq, hkv)
+                sv = (k[:, g, :] @ q[0, h, :]) * sc
+                w = np.exp(sv - sv.max())
+                pr = w / w.sum()
+                o = pr @ v[:, g, :]
+                dp = v[:, g, :] @ do[h]
+                ds = pr * (dp - do[h] @ o)
+                dv_acc[g] += pr[pj] * do[h]
+                dk_acc[g] += sc * ds[pj] * q[0, h]
+        dks.append(rope(dk_acc[None], [pj], base, inverse=True)[0])
+        dvs.append(dv_acc)
+    return np.stack(dks), np.stack(dvs)

@@ -1,0 +1,147 @@
+// C ABI: planner entry points, device image upload, status strings.
+#include <cuda_runtime_api.h>
+
+#include <cstring>
+#include <new>
+
+#include "plan_handle.h"
+#include "tpk.h"
+
+namespace {
+template <typename T, typename U>
+void copy_out(T* dst, const std::vector<U>& v) {
+  if (dst)
+    for (size_t i = 0; i < v.size(); ++i) dst[i] = static_cast<T>(v[i]);
+}
+}  // namespace
+
+extern "C" {
+
+int tpk_plan_build(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs,
+                   const uint8_t* trained, const int32_t* group_ids,
+                   const tpk_plan_opts* opts, tpk_plan** out) {
+  if (!out) return TPK_E_ARG;
+  *out = nullptr;
+  tpk::PlanOptions o;
+  if (opts) {
+    o.row_capacity = opts->row_capacity;
+    o.min_shared = opts->min_shared;
+    o.placement = opts->placement;
+  }
+  tpk_plan* h = new (std::nothrow) tpk_plan();
+  if (!h) return TPK_E_ARG;
+  int st;
+  try {
+    st = tpk::build_plan(tokens, seq_offsets, n_seqs, trained, group_ids, o, &h->p);
+  } catch (const std::bad_alloc&) {
+    st = TPK_E_OVERFLOW;
+  }
+  if (st != TPK_OK) {
+    delete h;
+    return st;
+  }
+  *out = h;
+  return TPK_OK;
+}
+
+int tpk_plan_info_get(const tpk_plan* plan, tpk_plan_info* out) {
+  if (!plan || !out) return TPK_E_ARG;
+  const tpk::Plan& P = plan->p;
+  out->n_seqs = P.n_seqs;
+  out->n_rows = P.n_rows;
+  out->n_fwd = P.F;
+  out->n_raw = P.R;
+  out->n_segments = P.n_segments;
+  out->n_leaves = P.n_leaves;
+  out->n_qtiles = static_cast<int64_t>(P.qt_q0.size());
+  out->n_kblocks = static_cast<int64_t>(P.kb.size() / 2);
+  out->n_ktiles = static_cast<int64_t>(P.kt_k0.size());
+  out->n_qblocks = static_cast<int64_t>(P.qb.size() / 2);
+  out->useful_pairs = P.useful_pairs;
+  out->visited_pairs = P.visited_pairs;
+  out->max_depth = P.max_depth;
+  out->packing_ratio = P.packing_ratio;
+  out->row_fill_frac = P.row_fill_frac;
+  out->fork_frac = P.fork_frac;
+  return TPK_OK;
+}
+
+int tpk_plan_export(const tpk_plan* plan, int64_t* row_offsets, int64_t* row_loads,
+                    int32_t* row_of_seq, int32_t* fwd_token, int32_t* fwd_src,
+                    int32_t* parent, int32_t* depth, int32_t* token_index,
+                    int32_t* subtree_end) {
+  if (!plan) return TPK_E_ARG;
+  const tpk::Plan& P = plan->p;
+  copy_out(row_offsets, P.row_offsets);
+  copy_out(row_loads, P.row_loads);
+  copy_out(row_of_seq, P.row_of_seq);
+  copy_out(fwd_token, P.fwd_token);
+  copy_out(fwd_src, P.fwd_src);
+  copy_out(parent, P.parent);
+  copy_out(depth, P.depth);
+  copy_out(token_index, P.token_index);
+  copy_out(subtree_end, P.subtree_end);
+  return TPK_OK;
+}
+
+int tpk_plan_worklists(const tpk_plan* plan, int32_t* qt_q0, int32_t* qt_nq,
+                       int32_t* qt_kb_begin, int32_t* kb, int32_t* qt_order,
+                       int32_t* kt_k0, int32_t* kt_nk, int32_t* kt_qb_begin,
+                       int32_t* qb, int32_t* kt_order) {
+  if (!plan) return TPK_E_ARG;
+  const tpk::Plan& P = plan->p;
+  copy_out(qt_q0, P.qt_q0);
+  copy_out(qt_nq, P.qt_nq);
+  copy_out(qt_kb_begin, P.qt_kb_begin);
+  copy_out(kb, P.kb);
+  copy_out(qt_order, P.qt_order);
+  copy_out(kt_k0, P.kt_k0);
+  copy_out(kt_nk, P.kt_nk);
+  copy_out(kt_qb_begin, P.kt_qb_begin);
+  copy_out(qb, P.qb);
+  copy_out(kt_order, P.kt_order);
+  return TPK_OK;
+}
+
+size_t tpk_plan_device_bytes(const tpk_plan* plan) { return plan ? plan->p.image.size() : 0; }
+
+int tpk_plan_field_offset(const tpk_plan* plan, int32_t field, size_t* offset) {
+  if (!plan || !offset) return TPK_E_ARG;
+  switch (field) {
+    case TPK_FIELD_DEPTH: *offset = plan->p.off_depth; return TPK_OK;
+    case TPK_FIELD_TOKEN_INDEX: *offset = plan->p.off_token_index; return TPK_OK;
+    case TPK_FIELD_SUBTREE_END: *offset = plan->p.off_subtree_end; return TPK_OK;
+    case TPK_FIELD_PARENT: *offset = plan->p.off_parent; return TPK_OK;
+    default: return TPK_E_ARG;
+  }
+}
+
+int tpk_plan_upload(const tpk_plan* plan, void* dev_image, void* stream) {
+  if (!plan || !dev_image) return TPK_E_ARG;
+  if (reinterpret_cast<uintptr_t>(dev_image) % 256) return TPK_E_ARG;
+  const auto& img = plan->p.image;
+  if (img.empty()) return TPK_OK;
+  cudaError_t e = cudaMemcpyAsync(dev_image, img.data(), img.size(), cudaMemcpyHostToDevice,
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TPK_OK : TPK_E_CUDA;
+}
+
+void tpk_plan_destroy(tpk_plan* plan) { delete plan; }
+
+const char* tpk_status_string(int status) {
+  switch (status) {
+    case TPK_OK: return "ok";
+    case TPK_E_ARG: return "invalid argument";
+    case TPK_E_SEQ_TOO_LONG: return "a sequence is longer than the row capacity";
+    case TPK_E_OVERFLOW: return "size does not fit the int32 layout";
+    case TPK_E_UNSUPPORTED: return "unsupported shape or device (needs sm_103, head_dim 64/128, Hq % Hkv == 0)";
+    case TPK_E_CUDA: return "CUDA call failed";
+    case TPK_E_TIMEOUT: return "a device wait gave up";
+    case TPK_E_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+const char* tpk_version(void) { return "tpk 0.1 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,594 @@
+// Tree attention backward on tcgen05 (sm_103a).
+//
+// Gradients of L = sum_{f,h} <dO[f,h], O[f,h]> for the forward of attn_fwd.cu
+// (every query attends to itself and its ancestors, j <= i < subtree_end[j];
+// "Prefix Tree Packing in ART", section "Token-mixing layers").  With
+// P_ij = exp(scale q_i.k_j - LSE_i) on visible pairs (0 elsewhere),
+// dP_ij = dO_i.v_j, D_i = dO_i.O_i and dS_ij = P_ij (dP_ij - D_i):
+//   dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j.
+//
+// Three launches, all deterministic (no atomics):
+//  1. prep:      D[h,i] = dO_i . O_i (fp32, into the workspace).
+//  2. key-major: one CTA per (128-key tile, KV head).  It walks the tile's
+//     query blocks -- [k0, max subtree_end) of its keys, the only queries that
+//     can see them -- for every query head of the group, and keeps dK, dV of
+//     the tile in TMEM.  Per (query block, head):
+//        S^T = K Q^T, dP^T = V dO^T            (tcgen05, operands from smem)
+//        softmax warps: P^T, dS^T -> bf16, written back into TMEM over S^T, dP^T
+//        dV += P^T dO, dK += dS^T Q            (A operand straight from TMEM)
+//  3. query-major: one CTA per (128-query tile, query head), the forward's key
+//     blocks:  S = Q K^T, dP = dO V^T, dS -> TMEM, dQ += dS K.
+// Pass 3 recomputes S and dP (7 matrix products instead of 5) in exchange for
+// a dQ that needs neither an fp32 accumulator nor atomics.
+//
+// Warp roles in passes 2 and 3: warp 0 TMA producer, warp 1 MMA issuer and
+// TMEM owner, warps 4-7 the 128 row threads (one TMEM lane each).  Waits are
+// bounded as in the forward; a timeout sets *dev_err = TPK_E_TIMEOUT.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "plan_handle.h"
+#include "ptx.cuh"
+
+namespace tpk {
+namespace {
+
+constexpr int BT = 128;          // tile height (keys in pass 2, queries in pass 3)
+constexpr int kBox = BT * 128;   // one 128-row x 64-element swizzled box
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct BwdParams {
+  // forward work list (pass 3)
+  const int32_t* qt_q0;
+  const int32_t* qt_nq;
+  const int32_t* qt_kb_begin;
+  const int2* kb;
+  const int32_t* qt_order;
+  // backward work list (pass 2)
+  const int32_t* kt_k0;
+  const int32_t* kt_nk;
+  const int32_t* kt_qb_begin;
+  const int2* qb;
+  const int32_t* kt_order;
+  const int32_t* subtree_end;
+  const float* lse;     // [Hq, F]
+  const float* dsum;    // [Hq, F]
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int32_t F, Hq, Hkv, group_size;
+  float scale, scale_log2;
+  int32_t* err;
+};
+
+// ----------------------------------------------------------------- pass 1
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                                       const __nv_bfloat16* __restrict__ dout,
+                                                       float* __restrict__ dsum, int64_t F, int Hq, int D) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n = F * Hq;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < n; w += nwarps) {
+    const int64_t f = w / Hq, h = w % Hq;
+    const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(o + w * D);
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(dout + w * D);
+    float acc = 0.f;
+    for (int c = lane; c < D / 2; c += 32) {
+      const float2 x = __bfloat1622float2(a[c]), y = __bfloat1622float2(b[c]);
+      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) dsum[h * F + f] = acc;
+  }
+}
+
+// Row epilogue helper: 32 fp32 TMEM columns * mul -> 32 bf16 stored to dst.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&u)[32], float mul) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) pk[j] = ptx::pack_bf16x2(__uint_as_float(u[2 * j]) * mul, __uint_as_float(u[2 * j + 1]) * mul);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+}
+
+// ----------------------------------------------------------------- pass 2
+template <int D, int NS>
+struct KVSmem {
+  uint8_t k[D / 64][kBox];
+  uint8_t v[D / 64][kBox];
+  uint8_t q[NS][D / 64][kBox];
+  uint8_t dO[NS][D / 64][kBox];
+  uint64_t kv_full, q_full[NS], q_empty[NS], s_full, p_full, acc_done, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D, int NS>
+__global__ void __launch_bounds__(256, 1)
+    bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdParams p) {
+  using Smem = KVSmem<D, NS>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  volatile int* abort_flag = &S.abort_flag;
+
+  const int item = blockIdx.x;
+  const int tile = __ldg(p.kt_order + item / p.Hkv);
+  const int g = item % p.Hkv;                 // KV head
+  const int G = p.group_size;                 // query heads per KV head
+  const int k0 = __ldg(p.kt_k0 + tile);
+  const int nk = __ldg(p.kt_nk + tile);
+  const int qb_begin = __ldg(p.kt_qb_begin + tile);
+  const int n_steps = (__ldg(p.kt_qb_begin + tile + 1) - qb_begin) * G;
+
+  // TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D)
+  constexpr uint32_t cS = 0, cdP = 128, cdV = 256, cdK = 256 + D;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&S.kv_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(&S.q_full[s], 1);
+      ptx::mbar_init(&S.q_empty[s], 1);
+    }
+    ptx::mbar_init(&S.s_full, 1);
+    ptx::mbar_init(&S.p_full, 128);
+    ptx::mbar_init(&S.acc_done, 1);
+    ptx::mbar_init(&S.drain, 1);
+    S.abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&S.tmem_base, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == 0) {
+    if (ptx::elect_one()) {
+      ptx::mbar_arrive_expect_tx(&S.kv_full, 2 * D * 256);
+      for (int c = 0; c < D / 64; ++c) {
+        ptx::tma_load_3d(S.k[c], &tm_k, &S.kv_full, c * 64, g, k0);
+        ptx::tma_load_3d(S.v[c], &tm_v, &S.kv_full, c * 64, g, k0);
+      }
+      int issued = 0;
+      for (int n = 0; n < n_steps; ++n) {
+        const int st = n % NS;
+        const uint32_t use = n / NS;
+        const int qs = __ldg(&p.qb[qb_begin + n / G].x);
+        const int h = g * G + n % G;
+        if (n >= NS && !ptx::mbar_wait(&S.q_empty[st], (use - 1) & 1, abort_flag, kWaitLimitNs)) break;
+        ptx::mbar_arrive_expect_tx(&S.q_full[st], 2 * D * 256);
+        for (int c = 0; c < D / 64; ++c) {
+          ptx::tma_load_3d(S.q[st][c], &tm_q, &S.q_full[st], c * 64, h, qs);
+          ptx::tma_load_3d(S.dO[st][c], &tm_do, &S.q_full[st], c * 64, h, qs);
+        }
+        issued = n + 1;
+      }
+      if (*abort_flag) {
+        for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n) ptx::mbar_drain(&S.q_full[n % NS], (n / NS) & 1);
+        ptx::mbar_drain(&S.kv_full, 0);
+      }
+    }
+  } else if (warp == 1) {
+    if (ptx::elect_one()) {
+      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(BT, BT, false, false);
+      constexpr uint32_t idesc_acc = ptx::idesc_bf16_f32(BT, D, false, true);
+      bool ok = ptx::mbar_wait(&S.kv_full, 0, abort_flag, kWaitLimitNs);
+      ptx::tc_fence_after();
+      const uint32_t k_base = ptx::smem_addr(S.k[0]);
+      const uint32_t v_base = ptx::smem_addr(S.v[0]);
+      for (int n = 0; ok && n < n_steps; ++n) {
+        const int st = n % NS;
+        if (!ptx::mbar_wait(&S.q_full[st], (n / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t q_base = ptx::smem_addr(S.q[st][0]);
+        const uint32_t do_base = ptx::smem_addr(S.dO[st][0]);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
+          ptx::mma_ss(tmem + cS, ptx::sw128_desc(k_base + koff, 16, 1024), ptx::sw128_desc(q_base + koff, 16, 1024),
+                      idesc_s, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
+          ptx::mma_ss(tmem + cdP, ptx::sw128_desc(v_base + koff, 16, 1024),
+                      ptx::sw128_desc(do_base + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(&S.s_full);
+        if (!ptx::mbar_wait(&S.p_full, n & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk) {
+          // B operands dO / Q blocks are MN-major: N = head dim, K = 16 queries per step
+          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
+          ptx::mma_ts(tmem + cdV, tmem + cS + kk * 8, ptx::sw128_desc(do_base + kk * 2048, kBox, 1024), idesc_acc, acc);
+          ptx::mma_ts(tmem + cdK, tmem + cdP + kk * 8, ptx::sw128_desc(q_base + kk * 2048, kBox, 1024), idesc_acc, acc);
+        }
+        ptx::mma_commit(&S.q_empty[st]);
+      }
+      if (ok) ptx::mma_commit(&S.acc_done);
+      ptx::mma_commit(&S.drain);
+      ptx::mbar_drain(&S.drain, 0);
+    }
+  } else if (warp >= 4) {
+    const int wq = warp & 3;
+    const int t = wq * 32 + (threadIdx.x & 31);
+    const int j = k0 + t;                        // this thread's key
+    const int se_j = t < nk ? __ldg(p.subtree_end + j) : -1;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int n = 0; n < n_steps; ++n) {
+      ok = ptx::mbar_wait(&S.s_full, n & 1, abort_flag, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int2 blk = __ldg(&p.qb[qb_begin + n / G]);
+      const int qs = blk.x, nq = blk.y & 0xFFFF;
+      const bool full = (blk.y >> 16) & 1;
+      const int h = g * G + n % G;
+      const float* lse_h = p.lse + static_cast<int64_t>(h) * p.F;
+      const float* dsum_h = p.dsum + static_cast<int64_t>(h) * p.F;
+#pragma unroll
+      for (int c = 0; c < BT / 32; ++c) {
+        uint32_t us[32], ud[32];
+        ptx::tmem_ld32(tmem + lane_off + cS + c * 32, us);
+        ptx::tmem_ld32(tmem + lane_off + cdP + c * 32, ud);
+        ptx::tmem_wait_ld();
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            const int col = c * 32 + e + x;
+            const int i = qs + col;
+            const bool in = col < nq;
+            const bool vis = in && (full || (j <= i && i < se_j));
+            const float l2 = in ? __ldg(lse_h + i) * kLog2e : 0.f;
+            const float dd = in ? __ldg(dsum_h + i) : 0.f;
+            const float pr = vis ? ptx::ex2(fmaf(__uint_as_float(us[e + x]), sl2, -l2)) : 0.f;
+            pv[x] = pr;
+            dv[x] = pr * (__uint_as_float(ud[e + x]) - dd);
+          }
+          pp[e / 2] = ptx::pack_bf16x2(pv[0], pv[1]);
+          pd[e / 2] = ptx::pack_bf16x2(dv[0], dv[1]);
+        }
+        ptx::tmem_st16(tmem + lane_off + cS + c * 16, pp);
+        ptx::tmem_st16(tmem + lane_off + cdP + c * 16, pd);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&S.p_full);
+    }
+    if (ok) {
+      ok = ptx::mbar_wait(&S.acc_done, 0, abort_flag, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      ptx::tc_fence_after();
+      __nv_bfloat16* dv_row = p.dv + (static_cast<int64_t>(j) * p.Hkv + g) * D;
+      __nv_bfloat16* dk_row = p.dk + (static_cast<int64_t>(j) * p.Hkv + g) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        ptx::tmem_ld32(tmem + lane_off + cdV + c * 32, u);
+        ptx::tmem_wait_ld();
+        if (t < nk) store_row32(dv_row + c * 32, u, 1.f);
+        ptx::tmem_ld32(tmem + lane_off + cdK + c * 32, u);
+        ptx::tmem_wait_ld();
+        if (t < nk) store_row32(dk_row + c * 32, u, p.scale);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && S.abort_flag && p.err) atomicExch(p.err, TPK_E_TIMEOUT);
+}
+
+// ----------------------------------------------------------------- pass 3
+template <int D, int NS>
+struct QSmem {
+  uint8_t q[D / 64][kBox];
+  uint8_t dO[D / 64][kBox];
+  uint8_t k[NS][D / 64][kBox];
+  uint8_t v[NS][D / 64][kBox];
+  uint64_t q_full, kv_full[NS], kv_empty[NS], s_full, p_full, acc_done, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D, int NS>
+__global__ void __launch_bounds__(256, 1)
+    bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                 const BwdParams p) {
+  using Smem = QSmem<D, NS>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  volatile int* abort_flag = &S.abort_flag;
+
+  const int item = blockIdx.x;
+  const int tile = __ldg(p.qt_order + item / p.Hq);
+  const int h = item % p.Hq;
+  const int kvh = h / p.group_size;
+  const int q0 = __ldg(p.qt_q0 + tile);
+  const int nq = __ldg(p.qt_nq + tile);
+  const int kb_begin = __ldg(p.qt_kb_begin + tile);
+  const int n_blocks = __ldg(p.qt_kb_begin + tile + 1) - kb_begin;
+
+  // TMEM columns: S [0,128), dP [128,256), dQ [256, 256+D)
+  constexpr uint32_t cS = 0, cdP = 128, cdQ = 256;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&S.q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(&S.kv_full[s], 1);
+      ptx::mbar_init(&S.kv_empty[s], 1);
+    }
+    ptx::mbar_init(&S.s_full, 1);
+    ptx::mbar_init(&S.p_full, 128);
+    ptx::mbar_init(&S.acc_done, 1);
+    ptx::mbar_init(&S.drain, 1);
+    S.abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&S.tmem_base, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == 0) {
+    if (ptx::elect_one()) {
+      ptx::mbar_arrive_expect_tx(&S.q_full, 2 * D * 256);
+      for (int c = 0; c < D / 64; ++c) {
+        ptx::tma_load_3d(S.q[c], &tm_q, &S.q_full, c * 64, h, q0);
+        ptx::tma_load_3d(S.dO[c], &tm_do, &S.q_full, c * 64, h, q0);
+      }
+      int issued = 0;
+      for (int i = 0; i < n_blocks; ++i) {
+        const int st = i % NS;
+        const uint32_t use = i / NS;
+        const int kb0 = __ldg(&p.kb[kb_begin + i].x);
+        if (i >= NS && !ptx::mbar_wait(&S.kv_empty[st], (use - 1) & 1, abort_flag, kWaitLimitNs)) break;
+        ptx::mbar_arrive_expect_tx(&S.kv_full[st], 2 * D * 256);
+        for (int c = 0; c < D / 64; ++c) {
+          ptx::tma_load_3d(S.k[st][c], &tm_k, &S.kv_full[st], c * 64, kvh, kb0);
+          ptx::tma_load_3d(S.v[st][c], &tm_v, &S.kv_full[st], c * 64, kvh, kb0);
+        }
+        issued = i + 1;
+      }
+      if (*abort_flag) {
+        for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i) ptx::mbar_drain(&S.kv_full[i % NS], (i / NS) & 1);
+        ptx::mbar_drain(&S.q_full, 0);
+      }
+    }
+  } else if (warp == 1) {
+    if (ptx::elect_one()) {
+      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(BT, BT, false, false);
+      constexpr uint32_t idesc_dq = ptx::idesc_bf16_f32(BT, D, false, true);
+      bool ok = ptx::mbar_wait(&S.q_full, 0, abort_flag, kWaitLimitNs);
+      ptx::tc_fence_after();
+      const uint32_t q_base = ptx::smem_addr(S.q[0]);
+      const uint32_t do_base = ptx::smem_addr(S.dO[0]);
+      for (int i = 0; ok && i < n_blocks; ++i) {
+        const int st = i % NS;
+        if (!ptx::mbar_wait(&S.kv_full[st], (i / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t k_base = ptx::smem_addr(S.k[st][0]);
+        const uint32_t v_base = ptx::smem_addr(S.v[st][0]);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
+          ptx::mma_ss(tmem + cS, ptx::sw128_desc(q_base + koff, 16, 1024), ptx::sw128_desc(k_base + koff, 16, 1024),
+                      idesc_s, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
+          ptx::mma_ss(tmem + cdP, ptx::sw128_desc(do_base + koff, 16, 1024),
+                      ptx::sw128_desc(v_base + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(&S.s_full);
+        if (!ptx::mbar_wait(&S.p_full, i & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BT / 16; ++kk)
+          ptx::mma_ts(tmem + cdQ, tmem + cS + kk * 8, ptx::sw128_desc(k_base + kk * 2048, kBox, 1024), idesc_dq,
+                      (i > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(&S.kv_empty[st]);
+      }
+      if (ok) ptx::mma_commit(&S.acc_done);
+      ptx::mma_commit(&S.drain);
+      ptx::mbar_drain(&S.drain, 0);
+    }
+  } else if (warp >= 4) {
+    const int wq = warp & 3;
+    const int t = wq * 32 + (threadIdx.x & 31);
+    const int i = q0 + t;                         // this thread's query
+    const bool row_ok = t < nq;
+    const float l2 = row_ok ? __ldg(p.lse + static_cast<int64_t>(h) * p.F + i) * kLog2e : 0.f;
+    const float dd = row_ok ? __ldg(p.dsum + static_cast<int64_t>(h) * p.F + i) : 0.f;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int b = 0; b < n_blocks; ++b) {
+      ok = ptx::mbar_wait(&S.s_full, b & 1, abort_flag, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int2 blk = __ldg(&p.kb[kb_begin + b]);
+      const int kb0 = blk.x, nkb = blk.y & 0xFFFF;
+      const bool full = (blk.y >> 16) & 1;
+#pragma unroll
+      for (int c = 0; c < BT / 32; ++c) {
+        uint32_t us[32], ud[32];
+        ptx::tmem_ld32(tmem + lane_off + cS + c * 32, us);
+        ptx::tmem_ld32(tmem + lane_off + cdP + c * 32, ud);
+        ptx::tmem_wait_ld();
+        uint32_t pd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float dv[2];
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            const int col = c * 32 + e + x;
+            const int jj = kb0 + col;
+            bool vis = row_ok;
+            if (!full) vis = vis && col < nkb && jj <= i && i < __ldg(p.subtree_end + jj);
+            const float pr = vis ? ptx::ex2(fmaf(__uint_as_float(us[e + x]), sl2, -l2)) : 0.f;
+            dv[x] = pr * (__uint_as_float(ud[e + x]) - dd);
+          }
+          pd[e / 2] = ptx::pack_bf16x2(dv[0], dv[1]);
+        }
+        ptx::tmem_st16(tmem + lane_off + cS + c * 16, pd);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&S.p_full);
+    }
+    if (ok) {
+      ok = ptx::mbar_wait(&S.acc_done, 0, abort_flag, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      ptx::tc_fence_after();
+      __nv_bfloat16* row = p.dq + (static_cast<int64_t>(i) * p.Hq + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        ptx::tmem_ld32(tmem + lane_off + cdQ + c * 32, u);
+        ptx::tmem_wait_ld();
+        if (row_ok) store_row32(row + c * 32, u, p.scale);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && S.abort_flag && p.err) atomicExch(p.err, TPK_E_TIMEOUT);
+}
+
+template <typename Kern>
+int set_smem(Kern kern, size_t bytes, bool& done) {
+  if (!done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) != cudaSuccess)
+      return TPK_E_CUDA;
+    done = true;
+  }
+  return TPK_OK;
+}
+
+template <int D, int NS_KV, int NS_Q>
+int launch_bwd(const BwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const CUtensorMap& tdo, int64_t n_ktiles, int64_t n_qtiles, cudaStream_t stream) {
+  constexpr size_t smem_kv = sizeof(KVSmem<D, NS_KV>) + 1024;
+  constexpr size_t smem_q = sizeof(QSmem<D, NS_Q>) + 1024;
+  static_assert(smem_kv <= 227 * 1024 && smem_q <= 227 * 1024, "shared memory");
+  static bool cfg_kv = false, cfg_q = false;
+  int st = set_smem(bwd_kv_kernel<D, NS_KV>, smem_kv, cfg_kv);
+  if (st != TPK_OK) return st;
+  if ((st = set_smem(bwd_q_kernel<D, NS_Q>, smem_q, cfg_q)) != TPK_OK) return st;
+  const int64_t kv_items = n_ktiles * prm.Hkv, q_items = n_qtiles * prm.Hq;
+  if (kv_items > 0x7fffffff || q_items > 0x7fffffff) return TPK_E_OVERFLOW;
+  if (kv_items > 0) bwd_kv_kernel<D, NS_KV><<<static_cast<unsigned>(kv_items), 256, smem_kv, stream>>>(tq, tk, tv, tdo, prm);
+  if ((st = cuda_status(cudaGetLastError())) != TPK_OK) return st;
+  if (q_items > 0) bwd_q_kernel<D, NS_Q><<<static_cast<unsigned>(q_items), 256, smem_q, stream>>>(tq, tk, tv, tdo, prm);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+}  // namespace tpk
+
+extern "C" size_t tpk_attn_workspace_bytes(const tpk_plan* plan, int32_t Hq, int32_t Hkv, int32_t d, int32_t backward) {
+  (void)Hkv;
+  (void)d;
+  if (!plan || !backward || Hq <= 0) return 0;
+  // D[h, f] = dO . O, fp32 [Hq, F]
+  return (static_cast<size_t>(Hq) * static_cast<size_t>(plan->p.F) * 4 + 255) & ~size_t(255);
+}
+
+extern "C" int tpk_tree_attn_bwd(const tpk_plan* plan, const void* dev_image, const void* q, const void* k,
+                                 const void* v, const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                                 void* dv, int32_t Hq, int32_t Hkv, int32_t d, float scale, void* workspace,
+                                 size_t ws_bytes, int32_t* dev_err, void* stream) {
+  using namespace tpk;
+  if (!plan || !dev_image || !q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return TPK_E_ARG;
+  if (Hq <= 0 || Hkv <= 0 || !(scale > 0.f)) return TPK_E_ARG;
+  if ((d != 64 && d != 128) || Hq % Hkv != 0) return TPK_E_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv) |
+       reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dout)) % 16)
+    return TPK_E_ARG;
+  const Plan& P = plan->p;
+  if (P.F == 0) return TPK_OK;
+  const size_t need = tpk_attn_workspace_bytes(plan, Hq, Hkv, d, 1);
+  if (!workspace || ws_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256) return TPK_E_WORKSPACE;
+  int st = check_device();
+  if (st != TPK_OK) return st;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((st = make_map_bf16(&tq, q, P.F, Hq, d, 128)) != TPK_OK) return st;
+  if ((st = make_map_bf16(&tk, k, P.F, Hkv, d, 128)) != TPK_OK) return st;
+  if ((st = make_map_bf16(&tv, v, P.F, Hkv, d, 128)) != TPK_OK) return st;
+  if ((st = make_map_bf16(&tdo, dout, P.F, Hq, d, 128)) != TPK_OK) return st;
+  const uint8_t* img = static_cast<const uint8_t*>(dev_image);
+  BwdParams prm;
+  prm.qt_q0 = reinterpret_cast<const int32_t*>(img + P.off_qt_q0);
+  prm.qt_nq = reinterpret_cast<const int32_t*>(img + P.off_qt_nq);
+  prm.qt_kb_begin = reinterpret_cast<const int32_t*>(img + P.off_qt_kb_begin);
+  prm.kb = reinterpret_cast<const int2*>(img + P.off_kb);
+  prm.qt_order = reinterpret_cast<const int32_t*>(img + P.off_qt_order);
+  prm.kt_k0 = reinterpret_cast<const int32_t*>(img + P.off_kt_k0);
+  prm.kt_nk = reinterpret_cast<const int32_t*>(img + P.off_kt_nk);
+  prm.kt_qb_begin = reinterpret_cast<const int32_t*>(img + P.off_kt_qb_begin);
+  prm.qb = reinterpret_cast<const int2*>(img + P.off_qb);
+  prm.kt_order = reinterpret_cast<const int32_t*>(img + P.off_kt_order);
+  prm.subtree_end = reinterpret_cast<const int32_t*>(img + P.off_subtree_end);
+  prm.lse = lse;
+  prm.dsum = static_cast<float*>(workspace);
+  prm.dq = static_cast<__nv_bfloat16*>(dq);
+  prm.dk = static_cast<__nv_bfloat16*>(dk);
+  prm.dv = static_cast<__nv_bfloat16*>(dv);
+  prm.F = static_cast<int32_t>(P.F);
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.group_size = Hq / Hkv;
+  prm.scale = scale;
+  prm.scale_log2 = scale * kLog2e;
+  prm.err = dev_err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    const int64_t warps = P.F * Hq;
+    int64_t blocks = (warps + 7) / 8;
+    const int64_t cap = int64_t{num_sms()} * 32;
+    if (blocks > cap) blocks = cap;
+    bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                                                  static_cast<const __nv_bfloat16*>(dout),
+                                                                  static_cast<float*>(workspace), P.F, Hq, d);
+    if ((st = cuda_status(cudaGetLastError())) != TPK_OK) return st;
+  }
+  const int64_t nkt = static_cast<int64_t>(P.kt_k0.size()), nqt = static_cast<int64_t>(P.qt_q0.size());
+  if (d == 128) return launch_bwd<128, 2, 2>(prm, tq, tk, tv, tdo, nkt, nqt, s);
+  return launch_bwd<64, 4, 4>(prm, tq, tk, tv, tdo, nkt, nqt, s);
+}

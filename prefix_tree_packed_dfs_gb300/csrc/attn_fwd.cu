@@ -1,0 +1,408 @@
+// Tree attention forward on tcgen05 (sm_103a).
+//
+// What it computes ("Prefix Tree Packing in ART", section "Token-mixing
+// layers"; "DAG packing", section "The mask"): for every forwarded query f and
+// query head h, softmax attention over the keys visible to f -- f itself and
+// its ancestors, i.e. keys j with j <= f < subtree_end[j] (the [enter, exit]
+// interval test) -- and the natural-log LSE.
+//
+// Work decomposition.  Queries are cut into 128-row tiles on a per-row grid.
+// The keys any query of tile [q0, q1) can see are the ancestors of q0 plus the
+// tile itself (an ancestor of a later query that precedes q0 contains q0 in
+// its subtree).  The planner lists them as key blocks of <= 128 keys taken
+// from the merged ancestor intervals, flagging blocks visible to the whole
+// tile ("full", no mask) -- the "one fully visible block per ancestor segment
+// plus a causal triangle" of the pages.  Blocks off the ancestor chain are
+// never visited, so work follows forwarded tokens, not raw ones.
+//
+// One CTA = one (query tile, pair of query heads sharing a KV head).  Both
+// heads use the same K/V blocks, loaded once.  Warp roles:
+//   warp 0      TMA producer: Q tiles once, then K and V blocks through an
+//               NS-stage ring (K and V have separate full/empty barriers)
+//   warp 1      MMA issuer (one thread) and TMEM owner
+//   warps 4..   one softmax warpgroup per head slot; thread t owns query row t
+// TMEM (512 columns): S_h at [128h, 128h+128) fp32, O_h at [128*HPC + D*h, +D).
+// P_h (bf16) is written over the first 64 columns of S_h and fed to the PV MMA
+// straight from TMEM.  The MMA thread interleaves the two head slots
+// (PV_0(i-1), S_0(i), PV_1(i-1), S_1(i)) so one slot's softmax overlaps the
+// other slot's matrix products.
+// Online softmax with a lazily raised running maximum: O and the row sum are
+// rescaled only when the block maximum exceeds the one in use by more than
+// 2^8, which keeps exponentials <= 256 and skips almost every rescale.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "plan_handle.h"
+#include "ptx.cuh"
+
+namespace tpk {
+namespace {
+
+constexpr int BM = 128;          // query rows per tile
+constexpr int BN = 128;          // keys per block
+constexpr int kBox = BM * 128;   // bytes of one 128-row x 64-element swizzled box
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+struct FwdParams {
+  const int32_t* qt_q0;
+  const int32_t* qt_nq;
+  const int32_t* qt_kb_begin;
+  const int2* kb;
+  const int32_t* qt_order;
+  const int32_t* subtree_end;
+  __nv_bfloat16* o;
+  float* lse;
+  int32_t F, Hq, n_hgroups, group_size;
+  float scale_log2;
+  int32_t* err;
+};
+
+template <int D, int HPC, int NS>
+struct FwdSmem {
+  uint8_t q[HPC][D / 64][kBox];
+  uint8_t k[NS][D / 64][kBox];
+  uint8_t v[NS][D / 64][kBox];
+  uint64_t q_full;
+  uint64_t k_full[NS], v_full[NS], k_empty[NS], v_empty[NS];
+  uint64_t s_full[HPC], p_full[HPC], o_done[HPC];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D, int HPC, int NS>
+constexpr size_t fwd_smem_bytes() {
+  return sizeof(FwdSmem<D, HPC, NS>) + 1024;
+}
+
+template <int D, int HPC, int NS>
+__global__ void __launch_bounds__(128 * (1 + HPC), 1)
+    tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using Smem = FwdSmem<D, HPC, NS>;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  volatile int* abort_flag = &S.abort_flag;
+
+  const int item = blockIdx.x;
+  const int tile = __ldg(p.qt_order + item / p.n_hgroups);
+  const int h0 = (item % p.n_hgroups) * HPC;
+  const int kvh = h0 / p.group_size;
+  const int q0 = __ldg(p.qt_q0 + tile);
+  const int nq = __ldg(p.qt_nq + tile);
+  const int kb_begin = __ldg(p.qt_kb_begin + tile);
+  const int n_blocks = __ldg(p.qt_kb_begin + tile + 1) - kb_begin;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&S.q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(&S.k_full[s], 1);
+      ptx::mbar_init(&S.v_full[s], 1);
+      ptx::mbar_init(&S.k_empty[s], 1);
+      ptx::mbar_init(&S.v_empty[s], 1);
+    }
+    for (int h = 0; h < HPC; ++h) {
+      ptx::mbar_init(&S.s_full[h], 1);
+      ptx::mbar_init(&S.p_full[h], 128);
+      ptx::mbar_init(&S.o_done[h], 1);
+    }
+    ptx::mbar_init(&S.drain, 1);
+    S.abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&S.tmem_base, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (ptx::elect_one()) {
+      ptx::prefetch_tensormap(&tm_q);
+      ptx::prefetch_tensormap(&tm_k);
+      ptx::prefetch_tensormap(&tm_v);
+      ptx::mbar_arrive_expect_tx(&S.q_full, HPC * D * 256);
+      for (int s = 0; s < HPC; ++s)
+        for (int c = 0; c < D / 64; ++c) ptx::tma_load_3d(S.q[s][c], &tm_q, &S.q_full, c * 64, h0 + s, q0);
+      int issued = 0;
+      for (int i = 0; i < n_blocks; ++i) {
+        const int st = i % NS;
+        const uint32_t use = i / NS;
+        const int k0 = __ldg(&p.kb[kb_begin + i].x);
+        if (i >= NS && !ptx::mbar_wait(&S.k_empty[st], (use - 1) & 1, abort_flag, kWaitLimitNs)) break;
+        ptx::mbar_arrive_expect_tx(&S.k_full[st], D * 256);
+        for (int c = 0; c < D / 64; ++c) ptx::tma_load_3d(S.k[st][c], &tm_k, &S.k_full[st], c * 64, kvh, k0);
+        if (i >= NS && !ptx::mbar_wait(&S.v_empty[st], (use - 1) & 1, abort_flag, kWaitLimitNs)) {
+          issued = -(i + 1);   // K of block i issued, V not
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(&S.v_full[st], D * 256);
+        for (int c = 0; c < D / 64; ++c) ptx::tma_load_3d(S.v[st][c], &tm_v, &S.v_full[st], c * 64, kvh, k0);
+        issued = i + 1;
+      }
+      if (*abort_flag) {
+        // never leave a copy in flight into shared memory: wait (bounded, not
+        // interruptible) for the last load of every stage and for Q
+        const int last_k = issued < 0 ? -issued : issued;
+        const int last_v = issued < 0 ? -issued - 1 : issued;
+        for (int i = (last_k > NS ? last_k - NS : 0); i < last_k; ++i) ptx::mbar_drain(&S.k_full[i % NS], (i / NS) & 1);
+        for (int i = (last_v > NS ? last_v - NS : 0); i < last_v; ++i) ptx::mbar_drain(&S.v_full[i % NS], (i / NS) & 1);
+        ptx::mbar_drain(&S.q_full, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (ptx::elect_one()) {
+      constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, false, false);
+      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, false, true);
+      bool ok = ptx::mbar_wait(&S.q_full, 0, abort_flag, kWaitLimitNs);
+      ptx::tc_fence_after();
+      const uint32_t q_base[2] = {ptx::smem_addr(S.q[0][0]), ptx::smem_addr(S.q[HPC - 1][0])};
+      auto issue_pv = [&](int s, int blk) {
+        const int st = blk % NS;
+        const uint32_t v_base = ptx::smem_addr(S.v[st][0]);
+        const uint32_t o_col = tmem + BM * HPC + D * s;
+        const uint32_t p_col = tmem + BM * s;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          // V block as the MN-major B operand: N = head dim (64-wide column
+          // groups one box apart), K = 16 keys = 2 KB further per step
+          const uint64_t bdesc = ptx::sw128_desc(v_base + kk * 2048, kBox, 1024);
+          ptx::mma_ts(o_col, p_col + kk * 8, bdesc, idesc_pv, (blk > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      for (int i = 0; ok && i < n_blocks; ++i) {
+        const int st = i % NS;
+        const uint32_t use = i / NS;
+        if (!ptx::mbar_wait(&S.k_full[st], use & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t k_base = ptx::smem_addr(S.k[st][0]);
+        for (int s = 0; s < HPC; ++s) {
+          if (i > 0) {
+            const int pst = (i - 1) % NS;
+            if (s == 0 && !ptx::mbar_wait(&S.v_full[pst], ((i - 1) / NS) & 1, abort_flag, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            if (!ptx::mbar_wait(&S.p_full[s], (i - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            ptx::tc_fence_after();
+            issue_pv(s, i - 1);
+          }
+          const uint32_t s_col = tmem + BM * s;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            // Q and K as K-major operands: 16 elements = 32 bytes per step
+            // inside a 64-element box, next box after 4 steps
+            const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
+            const uint64_t adesc = ptx::sw128_desc(q_base[s] + koff, 16, 1024);
+            const uint64_t bdesc = ptx::sw128_desc(k_base + koff, 16, 1024);
+            ptx::mma_ss(s_col, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&S.s_full[s]);
+        }
+        if (!ok) break;
+        ptx::mma_commit(&S.k_empty[st]);
+        if (i > 0) ptx::mma_commit(&S.v_empty[(i - 1) % NS]);
+      }
+      if (ok && n_blocks > 0) {
+        const int last = n_blocks - 1;
+        if (ptx::mbar_wait(&S.v_full[last % NS], (last / NS) & 1, abort_flag, kWaitLimitNs)) {
+          for (int s = 0; s < HPC; ++s) {
+            if (!ptx::mbar_wait(&S.p_full[s], last & 1, abort_flag, kWaitLimitNs)) break;
+            ptx::tc_fence_after();
+            issue_pv(s, last);
+            ptx::mma_commit(&S.o_done[s]);
+          }
+        }
+      }
+      // drain: every MMA issued above has completed before TMEM is released
+      ptx::mma_commit(&S.drain);
+      ptx::mbar_drain(&S.drain, 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int slot = (warp - 4) >> 2;
+    const int wq = warp & 3;                 // TMEM lane quarter of this warp
+    const int r = wq * 32 + (threadIdx.x & 31);
+    const int qi = q0 + r;                   // this thread's query (forwarded index)
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t s_tm = tmem + lane_off + BM * slot;
+    const uint32_t o_tm = tmem + lane_off + BM * HPC + D * slot;
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY;   // running maximum in use (log2 units)
+    float l = 0.f;              // running row sum (relative to m_used)
+    bool ok = true;
+    for (int i = 0; i < n_blocks; ++i) {
+      ok = ptx::mbar_wait(&S.s_full[slot], i & 1, abort_flag, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int2 blk = __ldg(&p.kb[kb_begin + i]);
+      const int k0 = blk.x, nk = blk.y & 0xFFFF;
+      const bool full = (blk.y >> 16) & 1;
+      float sv[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t u[32];
+        ptx::tmem_ld32(s_tm + c * 32, u);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[c * 32 + j] = __uint_as_float(u[j]);
+      }
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          const int j = k0 + c;
+          const bool vis = (c < nk) && (j <= qi) && (qi < __ldg(p.subtree_end + j));
+          if (!vis) sv[c] = -INFINITY;
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, sv[c]);
+      const float m_blk = mx * sl2;
+      float alpha = 1.f;
+      const bool raise = m_blk > m_used + kRescaleThreshold;
+      if (raise) {
+        alpha = ptx::ex2(m_used - m_blk);   // 0 when m_used = -inf
+        m_used = m_blk;
+      }
+      const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float p0 = ptx::ex2(fmaf(sv[c * 64 + 2 * j], sl2, -m_sub));
+          const float p1 = ptx::ex2(fmaf(sv[c * 64 + 2 * j + 1], sl2, -m_sub));
+          sum += p0 + p1;
+          pk[j] = ptx::pack_bf16x2(p0, p1);
+        }
+        ptx::tmem_st32(s_tm + c * 32, pk);
+      }
+      l = l * alpha + sum;
+      if (i > 0 && __any_sync(0xffffffffu, raise)) {
+        // O accumulated through block i-1 is complete: the S(i) commit this
+        // warp waited on tracks every earlier MMA, including PV(i-1)
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          ptx::tmem_ld32(o_tm + c * 32, u);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * alpha);
+          ptx::tmem_st32(o_tm + c * 32, u);
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&S.p_full[slot]);
+    }
+    if (ok) {
+      ok = ptx::mbar_wait(&S.o_done[slot], 0, abort_flag, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      ptx::tc_fence_after();
+      const int h = h0 + slot;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = p.o + (static_cast<int64_t>(qi) * p.Hq + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        ptx::tmem_ld32(o_tm + c * 32, u);
+        ptx::tmem_wait_ld();
+        if (r < nq) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = ptx::pack_bf16x2(__uint_as_float(u[2 * j]) * inv_l, __uint_as_float(u[2 * j + 1]) * inv_l);
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+      if (r < nq) {
+        const float lse = l > 0.f ? (m_used + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+        p.lse[static_cast<int64_t>(h) * p.F + qi] = lse;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && S.abort_flag && p.err) atomicExch(p.err, TPK_E_TIMEOUT);
+}
+
+template <int D, int HPC, int NS>
+int launch(const FwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int64_t items,
+           cudaStream_t stream) {
+  auto kern = tree_attn_fwd_kernel<D, HPC, NS>;
+  constexpr size_t smem = fwd_smem_bytes<D, HPC, NS>();
+  static_assert(smem <= 227 * 1024, "shared memory");
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+      return TPK_E_CUDA;
+    configured = true;
+  }
+  if (items <= 0) return TPK_OK;
+  if (items > 0x7fffffff) return TPK_E_OVERFLOW;
+  kern<<<static_cast<unsigned>(items), 128 * (1 + HPC), smem, stream>>>(tq, tk, tv, prm);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+}  // namespace tpk
+
+extern "C" int tpk_tree_attn_fwd(const tpk_plan* plan, const void* dev_image, const void* q, const void* k,
+                                 const void* v, void* o, float* lse, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                                 void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
+  using namespace tpk;
+  (void)workspace;
+  (void)ws_bytes;
+  if (!plan || !dev_image || !q || !k || !v || !o || !lse) return TPK_E_ARG;
+  if (Hq <= 0 || Hkv <= 0 || !(scale > 0.f)) return TPK_E_ARG;
+  if ((d != 64 && d != 128) || Hq % Hkv != 0) return TPK_E_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dev_image) % 256) % 16) return TPK_E_ARG;
+  const Plan& P = plan->p;
+  if (P.F == 0) return TPK_OK;
+  int st = check_device();
+  if (st != TPK_OK) return st;
+  CUtensorMap tq, tk, tv;
+  if ((st = make_map_bf16(&tq, q, P.F, Hq, d, 128)) != TPK_OK) return st;
+  if ((st = make_map_bf16(&tk, k, P.F, Hkv, d, 128)) != TPK_OK) return st;
+  if ((st = make_map_bf16(&tv, v, P.F, Hkv, d, 128)) != TPK_OK) return st;
+  const uint8_t* img = static_cast<const uint8_t*>(dev_image);
+  FwdParams prm;
+  prm.qt_q0 = reinterpret_cast<const int32_t*>(img + P.off_qt_q0);
+  prm.qt_nq = reinterpret_cast<const int32_t*>(img + P.off_qt_nq);
+  prm.qt_kb_begin = reinterpret_cast<const int32_t*>(img + P.off_qt_kb_begin);
+  prm.kb = reinterpret_cast<const int2*>(img + P.off_kb);
+  prm.qt_order = reinterpret_cast<const int32_t*>(img + P.off_qt_order);
+  prm.subtree_end = reinterpret_cast<const int32_t*>(img + P.off_subtree_end);
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.F = static_cast<int32_t>(P.F);
+  prm.Hq = Hq;
+  prm.group_size = Hq / Hkv;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.err = dev_err;
+  const int hpc = (prm.group_size % 2 == 0) ? 2 : 1;
+  prm.n_hgroups = Hq / hpc;
+  const int64_t items = static_cast<int64_t>(P.qt_q0.size()) * prm.n_hgroups;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d == 128) return hpc == 2 ? launch<128, 2, 2>(prm, tq, tk, tv, items, s) : launch<128, 1, 2>(prm, tq, tk, tv, items, s);
+  return hpc == 2 ? launch<64, 2, 3>(prm, tq, tk, tv, items, s) : launch<64, 1, 4>(prm, tq, tk, tv, items, s);
+}

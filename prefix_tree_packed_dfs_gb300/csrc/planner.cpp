@@ -1,0 +1,434 @@
+// Host packing planner.  Integer-only; no CUDA.
+//
+// Steps ("Prefix Tree Packing in ART" = [ART], "DAG packing" = [DAG],
+// "TRL Tree Packing for AsyncGRPO" = [TRL]):
+//  1. position symbols (token, trained flag, target-if-trained): two positions
+//     share one forwarded slot iff their symbol prefixes agree, which keeps the
+//     last common token once per branch ([ART] "The tree", off-by-one note;
+//     [DAG] "The walk": the last common node is copied for every child);
+//  2. the prefix tree.  [ART] "The tree" builds it by a recursive walk
+//     (longest run all active sequences agree on, emit once, split by the next
+//     symbol).  Here the same tree comes from sorting the sequences'
+//     symbol strings and taking adjacent longest-common-prefix lengths: the
+//     sequences under any tree node are a contiguous run of the sorted order,
+//     the node's shared run ends at the minimum adjacent LCP inside that run,
+//     and the children are the sub-runs separated where the LCP equals it.
+//     Shared runs shorter than min_shared are not emitted; their positions
+//     are carried into each child ([ART] "The tree", first refinement);
+//  3. placement of leaves into rows: best-fit decreasing over marginal cost
+//     ([ART] "Bin packing, with a twist") or next-fit ([ART] "One tree, not one
+//     per group"); a row's segment set is closed under ancestors, so a leaf's
+//     marginal cost is the length of its path below the deepest segment the
+//     row already holds;
+//  4. depth-first layout of each row (leaves in symbol order, each segment
+//     emitted once, parents first; [DAG] "The walk", [TRL] "How tree packing
+//     works"), depth positions ([DAG] "Positions"), token_index, subtree ends
+//     ([ART] "Token-mixing layers": [enter, exit] intervals);
+//  5. the kernels' work lists: per 128-query tile, the key blocks of the
+//     ancestor chain of its first query plus the tile itself; per 128-key tile,
+//     the query blocks of [k0, max subtree_end); both in longest-first order.
+#include "planner.h"
+
+#include <algorithm>
+#include <cstring>
+#include <limits>
+#include <numeric>
+#include <unordered_map>
+
+#include "tpk.h"
+
+namespace tpk {
+namespace {
+
+constexpr int64_t kNoTarget = -2;  // untrained position: target not part of the key
+constexpr int64_t kEos = -1;       // target of the last position
+
+inline uint64_t pack_symbol(int32_t token, int flag, int64_t target) {
+  // lexicographic (token, flag, target) as one unsigned integer: tokens are
+  // >= 0 (31 bits), flag 1 bit, target + 2 in [0, 2^31 + 1] (32 bits)
+  return (static_cast<uint64_t>(static_cast<uint32_t>(token)) << 33) |
+         (static_cast<uint64_t>(flag ? 1 : 0) << 32) |
+         static_cast<uint64_t>(target + 2);
+}
+
+struct Segment {
+  int32_t parent;
+  int32_t start;   // depth of the first position
+  int32_t end;     // one past the depth of the last position
+  int32_t n_children;
+};
+
+struct Leaf {
+  std::vector<int32_t> members;   // original sequence indices, ascending
+  std::vector<int32_t> path;      // segment ids, root first
+  int32_t rank;                   // position of the sequence in symbol order
+  int64_t cost;                   // standalone cost = sequence length
+  int32_t rep() const { return members.front(); }
+};
+
+struct Bin {
+  int64_t load = 0;
+  std::vector<int32_t> leaves;
+  std::vector<uint64_t> held;     // bitset over segments
+  bool has(int32_t s) const { return (held[s >> 6] >> (s & 63)) & 1; }
+  void set(int32_t s) { held[s >> 6] |= (uint64_t{1} << (s & 63)); }
+};
+
+int64_t marginal_cost(const Bin& b, const Leaf& leaf, const std::vector<Segment>& segs) {
+  int64_t c = 0;
+  for (size_t i = leaf.path.size(); i-- > 0;) {
+    int32_t s = leaf.path[i];
+    if (b.has(s)) break;   // everything above is held too
+    c += segs[s].end - segs[s].start;
+  }
+  return c;
+}
+
+void take(Bin& b, int32_t leaf_id, const Leaf& leaf, const std::vector<Segment>& segs) {
+  b.load += marginal_cost(b, leaf, segs);
+  for (int32_t s : leaf.path) b.set(s);
+  b.leaves.push_back(leaf_id);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs,
+               const uint8_t* trained, const int32_t* group_ids,
+               const PlanOptions& opts, Plan* out) {
+  if (!tokens || !seq_offsets || !out || n_seqs <= 0) return TPK_E_ARG;
+  if (opts.row_capacity <= 0) return TPK_E_ARG;
+  if (opts.placement != TPK_PLACE_BFD && opts.placement != TPK_PLACE_NEXT_FIT) return TPK_E_ARG;
+  if (seq_offsets[0] != 0) return TPK_E_ARG;
+  for (int32_t s = 0; s < n_seqs; ++s)
+    if (seq_offsets[s + 1] <= seq_offsets[s]) return TPK_E_ARG;
+  const int64_t R = seq_offsets[n_seqs];
+  if (R >= (int64_t{1} << 31)) return TPK_E_OVERFLOW;
+  for (int64_t r = 0; r < R; ++r)
+    if (tokens[r] < 0) return TPK_E_ARG;
+  for (int32_t s = 0; s < n_seqs; ++s)
+    if (seq_offsets[s + 1] - seq_offsets[s] > opts.row_capacity) return TPK_E_SEQ_TOO_LONG;
+
+  Plan& P = *out;
+  P = Plan();
+  P.n_seqs = n_seqs;
+  P.R = R;
+  P.row_capacity = opts.row_capacity;
+  auto len = [&](int32_t s) { return static_cast<int32_t>(seq_offsets[s + 1] - seq_offsets[s]); };
+
+  // ---- 1. symbols --------------------------------------------------------
+  std::vector<uint64_t> sym(R);
+  for (int32_t s = 0; s < n_seqs; ++s) {
+    const int64_t o = seq_offsets[s];
+    const int32_t L = len(s);
+    for (int32_t p = 0; p < L; ++p) {
+      const int flag = trained ? (trained[o + p] != 0) : 1;
+      int64_t target = kNoTarget;
+      if (flag || p == L - 1) target = (p + 1 < L) ? tokens[o + p + 1] : kEos;
+      sym[o + p] = pack_symbol(tokens[o + p], flag, target);
+    }
+  }
+
+  // ---- 2. tree -----------------------------------------------------------
+  std::vector<int32_t> order(n_seqs);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
+    return std::lexicographical_compare(sym.begin() + seq_offsets[a], sym.begin() + seq_offsets[a + 1],
+                                        sym.begin() + seq_offsets[b], sym.begin() + seq_offsets[b + 1]);
+  });
+  std::vector<int32_t> rank(n_seqs);
+  for (int32_t i = 0; i < n_seqs; ++i) rank[order[i]] = i;
+  std::vector<int32_t> lcp(n_seqs, 0);   // lcp[i]: common prefix of order[i-1], order[i]
+  for (int32_t i = 1; i < n_seqs; ++i) {
+    const int32_t a = order[i - 1], b = order[i];
+    const int32_t n = std::min(len(a), len(b));
+    auto pa = sym.begin() + seq_offsets[a];
+    auto pb = sym.begin() + seq_offsets[b];
+    lcp[i] = static_cast<int32_t>(std::mismatch(pa, pa + n, pb).first - pa);
+  }
+
+  std::vector<Segment> segs;
+  std::vector<Leaf> leaves;
+  const int32_t min_len = std::max<int32_t>(opts.min_shared, 1);
+  struct Frame { int32_t lo, hi, seg_start, parent; };
+  std::vector<Frame> stack{{0, n_seqs, 0, -1}};
+  auto emit = [&](int32_t parent, int32_t start, int32_t end) {
+    segs.push_back({parent, start, end, 0});
+    if (parent >= 0) segs[parent].n_children++;
+    return static_cast<int32_t>(segs.size() - 1);
+  };
+  while (!stack.empty()) {
+    Frame fr = stack.back();
+    stack.pop_back();
+    bool identical = true;
+    int32_t end = std::numeric_limits<int32_t>::max();
+    for (int32_t i = fr.lo + 1; i < fr.hi; ++i) {
+      end = std::min(end, lcp[i]);
+      if (!(lcp[i] == len(order[i]) && len(order[i]) == len(order[i - 1]))) identical = false;
+    }
+    if (identical) {   // one distinct sequence: a leaf
+      const int32_t L = len(order[fr.lo]);
+      Leaf leaf;
+      const int32_t sid = emit(fr.parent, fr.seg_start, L);
+      for (int32_t i = fr.lo; i < fr.hi; ++i) leaf.members.push_back(order[i]);
+      std::sort(leaf.members.begin(), leaf.members.end());
+      for (int32_t s = sid; s >= 0; s = segs[s].parent) leaf.path.push_back(s);
+      std::reverse(leaf.path.begin(), leaf.path.end());
+      leaf.rank = fr.lo;
+      leaf.cost = L;
+      leaves.push_back(std::move(leaf));
+      continue;
+    }
+    int32_t parent = fr.parent, seg_start = fr.seg_start;
+    if (end > seg_start && end - seg_start >= min_len) {
+      parent = emit(parent, seg_start, end);
+      seg_start = end;
+    }
+    // children: sub-runs split where the adjacent LCP equals `end`; pushed in
+    // reverse so the smallest symbol is walked first (depth first)
+    int32_t hi = fr.hi;
+    for (int32_t i = fr.hi - 1; i >= fr.lo; --i) {
+      if (i == fr.lo || lcp[i] == end) {
+        stack.push_back({i, hi, seg_start, parent});
+        hi = i;
+      }
+    }
+  }
+  P.n_segments = static_cast<int64_t>(segs.size());
+  P.n_leaves = static_cast<int64_t>(leaves.size());
+
+  // ---- 3. placement -------------------------------------------------------
+  std::vector<int32_t> by_input(leaves.size());
+  std::iota(by_input.begin(), by_input.end(), 0);
+  std::sort(by_input.begin(), by_input.end(),
+            [&](int32_t a, int32_t b) { return leaves[a].rep() < leaves[b].rep(); });
+  std::vector<std::vector<int32_t>> groups;   // in first-appearance order
+  {
+    std::unordered_map<int64_t, size_t> index;
+    for (int32_t li : by_input) {
+      const int64_t g = group_ids ? group_ids[leaves[li].rep()] : leaves[li].path.front();
+      auto it = index.find(g);
+      if (it == index.end()) { it = index.emplace(g, groups.size()).first; groups.emplace_back(); }
+      groups[it->second].push_back(li);
+    }
+  }
+  const int64_t C = opts.row_capacity;
+  const size_t words = (segs.size() + 63) / 64;
+  std::vector<Bin> bins;
+  auto new_bin = [&]() { bins.emplace_back(); bins.back().held.assign(words, 0); return bins.size() - 1; };
+  if (opts.placement == TPK_PLACE_BFD) {
+    std::vector<int64_t> gmax(groups.size(), 0);
+    for (size_t g = 0; g < groups.size(); ++g)
+      for (int32_t li : groups[g]) gmax[g] = std::max(gmax[g], leaves[li].cost);
+    std::vector<int32_t> gorder(groups.size());
+    std::iota(gorder.begin(), gorder.end(), 0);
+    std::stable_sort(gorder.begin(), gorder.end(), [&](int32_t a, int32_t b) { return gmax[a] > gmax[b]; });
+    for (int32_t g : gorder) {
+      for (int32_t li : groups[g]) {
+        int64_t best = -1, best_room = C + 1;
+        for (size_t b = 0; b < bins.size(); ++b) {
+          const int64_t load = bins[b].load + marginal_cost(bins[b], leaves[li], segs);
+          if (load <= C && C - load < best_room) { best = static_cast<int64_t>(b); best_room = C - load; }
+        }
+        if (best < 0) best = static_cast<int64_t>(new_bin());
+        take(bins[best], li, leaves[li], segs);
+      }
+    }
+  } else {
+    for (auto& g : groups)
+      for (int32_t li : g) {
+        if (bins.empty() || bins.back().load + marginal_cost(bins.back(), leaves[li], segs) > C) new_bin();
+        take(bins.back(), li, leaves[li], segs);
+      }
+  }
+  P.n_rows = static_cast<int64_t>(bins.size());
+
+  // ---- 4. layout ----------------------------------------------------------
+  int64_t F = 0;
+  for (auto& b : bins) F += b.load;
+  if (F >= (int64_t{1} << 31)) return TPK_E_OVERFLOW;
+  P.F = F;
+  P.depth.reserve(F);
+  P.fwd_token.reserve(F);
+  P.parent.reserve(F);
+  P.token_index.assign(R, -1);
+  P.row_of_seq.assign(n_seqs, -1);
+  P.row_offsets.push_back(0);
+  // segment instances (a segment placed in one row)
+  std::vector<int32_t> inst_start, inst_len, inst_parent;
+  std::vector<int32_t> inst_of(F);
+  std::vector<int32_t> placed(segs.size(), -1), placed_inst(segs.size(), -1);
+  for (size_t b = 0; b < bins.size(); ++b) {
+    std::vector<int32_t> row_leaves = bins[b].leaves;
+    std::sort(row_leaves.begin(), row_leaves.end(),
+              [&](int32_t x, int32_t y) { return leaves[x].rank < leaves[y].rank; });
+    std::vector<int32_t> touched;
+    for (int32_t li : row_leaves) {
+      const Leaf& leaf = leaves[li];
+      const int64_t rep_off = seq_offsets[leaf.rep()];
+      int32_t prev = -1;
+      for (int32_t s : leaf.path) {
+        if (placed[s] < 0) {
+          const int32_t f0 = static_cast<int32_t>(P.depth.size());
+          placed[s] = f0;
+          placed_inst[s] = static_cast<int32_t>(inst_start.size());
+          touched.push_back(s);
+          inst_start.push_back(f0);
+          inst_len.push_back(segs[s].end - segs[s].start);
+          inst_parent.push_back(prev >= 0 ? placed_inst[prev] : -1);
+          for (int32_t p = segs[s].start; p < segs[s].end; ++p) {
+            const int32_t f = static_cast<int32_t>(P.depth.size());
+            P.depth.push_back(p);
+            P.fwd_token.push_back(tokens[rep_off + p]);
+            if (p > segs[s].start) P.parent.push_back(f - 1);
+            else if (prev >= 0) P.parent.push_back(placed[prev] + (segs[prev].end - 1 - segs[prev].start));
+            else P.parent.push_back(-1);
+            inst_of[f] = placed_inst[s];
+          }
+        }
+        prev = s;
+      }
+      for (int32_t m : leaf.members) {
+        P.row_of_seq[m] = static_cast<int32_t>(b);
+        const int64_t o = seq_offsets[m];
+        for (int32_t s : leaf.path)
+          for (int32_t p = segs[s].start; p < segs[s].end; ++p)
+            P.token_index[o + p] = placed[s] + (p - segs[s].start);
+      }
+    }
+    for (int32_t s : touched) { placed[s] = -1; placed_inst[s] = -1; }
+    P.row_offsets.push_back(static_cast<int64_t>(P.depth.size()));
+    P.row_loads.push_back(bins[b].load);
+  }
+  P.fwd_src.assign(F, -1);
+  for (int64_t r = 0; r < R; ++r)
+    if (P.fwd_src[P.token_index[r]] < 0) P.fwd_src[P.token_index[r]] = static_cast<int32_t>(r);
+  P.subtree_end.resize(F);
+  for (int64_t f = 0; f < F; ++f) P.subtree_end[f] = static_cast<int32_t>(f + 1);
+  for (int64_t f = F - 1; f >= 0; --f) {
+    const int32_t p = P.parent[f];
+    if (p >= 0 && P.subtree_end[f] > P.subtree_end[p]) P.subtree_end[p] = P.subtree_end[f];
+  }
+  int64_t forks = 0;
+  for (auto& s : segs) forks += (s.n_children >= 2);
+  P.useful_pairs = 0;
+  P.max_depth = 0;
+  for (int64_t f = 0; f < F; ++f) {
+    P.useful_pairs += P.depth[f] + 1;
+    P.max_depth = std::max<int64_t>(P.max_depth, P.depth[f]);
+  }
+  P.packing_ratio = static_cast<double>(R) / static_cast<double>(F);
+  P.row_fill_frac = static_cast<double>(F) / (static_cast<double>(P.n_rows) * static_cast<double>(C));
+  P.fork_frac = static_cast<double>(forks) / static_cast<double>(segs.size());
+
+  // ---- 5. work lists ------------------------------------------------------
+  std::vector<int32_t> chain;
+  std::vector<std::pair<int32_t, int32_t>> ivals;
+  P.visited_pairs = 0;
+  for (int64_t row = 0; row < P.n_rows; ++row) {
+    const int32_t rs = static_cast<int32_t>(P.row_offsets[row]);
+    const int32_t re = static_cast<int32_t>(P.row_offsets[row + 1]);
+    for (int32_t q0 = rs; q0 < re; q0 += kTile) {
+      const int32_t q1 = std::min(q0 + kTile, re);
+      P.qt_q0.push_back(q0);
+      P.qt_nq.push_back(q1 - q0);
+      P.qt_kb_begin.push_back(static_cast<int32_t>(P.kb.size() / 2));
+      // ancestor chain of q0: proper ancestor instances, then q0's own prefix
+      chain.clear();
+      for (int32_t i = inst_parent[inst_of[q0]]; i >= 0; i = inst_parent[i]) chain.push_back(i);
+      ivals.clear();
+      for (size_t c = chain.size(); c-- > 0;) {
+        const int32_t a = inst_start[chain[c]], e = a + inst_len[chain[c]];
+        if (!ivals.empty() && ivals.back().second == a) ivals.back().second = e;
+        else ivals.push_back({a, e});
+      }
+      const int32_t own = inst_start[inst_of[q0]];
+      if (own < q0) {
+        if (!ivals.empty() && ivals.back().second == own) ivals.back().second = q0;
+        else ivals.push_back({own, q0});
+      }
+      ivals.push_back({q0, q1});   // the tile itself (causal + subtree mask)
+      for (auto& iv : ivals) {
+        for (int32_t k0 = iv.first; k0 < iv.second; k0 += kTile) {
+          const int32_t nk = std::min(kTile, iv.second - k0);
+          // along an ancestor chain subtree ends do not increase, so the last
+          // key of the block has the smallest one
+          const bool full = (k0 + nk - 1 <= q0) && (P.subtree_end[k0 + nk - 1] >= q1);
+          P.kb.push_back(k0);
+          P.kb.push_back(nk | (full ? (1 << 16) : 0));
+          P.visited_pairs += int64_t{kTile} * kTile;
+        }
+      }
+    }
+    for (int32_t k0 = rs; k0 < re; k0 += kTile) {
+      const int32_t k1 = std::min(k0 + kTile, re);
+      int32_t qend = 0, min_se = std::numeric_limits<int32_t>::max();
+      for (int32_t j = k0; j < k1; ++j) {
+        qend = std::max(qend, P.subtree_end[j]);
+        min_se = std::min(min_se, P.subtree_end[j]);
+      }
+      P.kt_k0.push_back(k0);
+      P.kt_nk.push_back(k1 - k0);
+      P.kt_qb_begin.push_back(static_cast<int32_t>(P.qb.size() / 2));
+      for (int32_t qs = k0; qs < qend; qs += kTile) {
+        const int32_t qe = std::min(qs + kTile, qend);
+        const bool full = (k1 - 1 <= qs) && (min_se >= qe);
+        P.qb.push_back(qs);
+        P.qb.push_back((qe - qs) | (full ? (1 << 16) : 0));
+      }
+    }
+  }
+  if (P.kb.size() / 2 >= (size_t{1} << 31) || P.qb.size() / 2 >= (size_t{1} << 31)) return TPK_E_OVERFLOW;
+  P.qt_kb_begin.push_back(static_cast<int32_t>(P.kb.size() / 2));
+  P.kt_qb_begin.push_back(static_cast<int32_t>(P.qb.size() / 2));
+  auto lpt = [](const std::vector<int32_t>& begin) {
+    std::vector<int32_t> o(begin.size() - 1);
+    std::iota(o.begin(), o.end(), 0);
+    std::stable_sort(o.begin(), o.end(), [&](int32_t a, int32_t b) {
+      return begin[a + 1] - begin[a] > begin[b + 1] - begin[b];
+    });
+    return o;
+  };
+  P.qt_order = lpt(P.qt_kb_begin);
+  P.kt_order = lpt(P.kt_qb_begin);
+
+  // ---- device image -------------------------------------------------------
+  size_t off = 0;
+  auto place = [&](size_t& field, size_t bytes) { field = off; off = align256(off + bytes); };
+  place(P.off_depth, 4 * P.depth.size());
+  place(P.off_token_index, 4 * P.token_index.size());
+  place(P.off_subtree_end, 4 * P.subtree_end.size());
+  place(P.off_parent, 4 * P.parent.size());
+  place(P.off_qt_q0, 4 * P.qt_q0.size());
+  place(P.off_qt_nq, 4 * P.qt_nq.size());
+  place(P.off_qt_kb_begin, 4 * P.qt_kb_begin.size());
+  place(P.off_kb, 4 * P.kb.size());
+  place(P.off_qt_order, 4 * P.qt_order.size());
+  place(P.off_kt_k0, 4 * P.kt_k0.size());
+  place(P.off_kt_nk, 4 * P.kt_nk.size());
+  place(P.off_kt_qb_begin, 4 * P.kt_qb_begin.size());
+  place(P.off_qb, 4 * P.qb.size());
+  place(P.off_kt_order, 4 * P.kt_order.size());
+  P.image.assign(off, 0);
+  auto put = [&](size_t field, const std::vector<int32_t>& v) {
+    if (!v.empty()) std::memcpy(P.image.data() + field, v.data(), 4 * v.size());
+  };
+  put(P.off_depth, P.depth);
+  put(P.off_token_index, P.token_index);
+  put(P.off_subtree_end, P.subtree_end);
+  put(P.off_parent, P.parent);
+  put(P.off_qt_q0, P.qt_q0);
+  put(P.off_qt_nq, P.qt_nq);
+  put(P.off_qt_kb_begin, P.qt_kb_begin);
+  put(P.off_kb, P.kb);
+  put(P.off_qt_order, P.qt_order);
+  put(P.off_kt_k0, P.kt_k0);
+  put(P.off_kt_nk, P.kt_nk);
+  put(P.off_kt_qb_begin, P.kt_qb_begin);
+  put(P.off_qb, P.qb);
+  put(P.off_kt_order, P.kt_order);
+  return TPK_OK;
+}
+
+}  // namespace tpk

@@ -1,0 +1,48 @@
+// Host-side packing planner: prefix tree, row placement, depth-first layout and
+// the attention kernels' work lists.  Integer-only ("Prefix Tree Packing in
+// ART", section "Metadata space first": the plan is computed over plain
+// integers before any tensor is touched).
+#pragma once
+#include <cstdint>
+#include <cstddef>
+#include <vector>
+
+namespace tpk {
+
+constexpr int kTile = 128;   // query / key tile height of the attention kernels
+
+struct PlanOptions {
+  int64_t row_capacity = 65536;
+  int32_t min_shared = 64;
+  int32_t placement = 0;     // 0 best-fit decreasing, 1 next-fit
+};
+
+struct Plan {
+  // sizes
+  int64_t n_seqs = 0, R = 0, F = 0, n_rows = 0, n_segments = 0, n_leaves = 0;
+  int64_t useful_pairs = 0, visited_pairs = 0, max_depth = 0;
+  double packing_ratio = 0, row_fill_frac = 0, fork_frac = 0;
+  int64_t row_capacity = 0;
+
+  // layout
+  std::vector<int64_t> row_offsets, row_loads;
+  std::vector<int32_t> row_of_seq, fwd_token, fwd_src, parent, depth, token_index, subtree_end;
+
+  // forward work list: query tiles and their key blocks
+  std::vector<int32_t> qt_q0, qt_nq, qt_kb_begin, kb, qt_order;
+  // backward work list: key tiles and their query blocks
+  std::vector<int32_t> kt_k0, kt_nk, kt_qb_begin, qb, kt_order;
+
+  // device image: every array above that a kernel reads, 256-byte aligned sections
+  std::vector<uint8_t> image;
+  size_t off_depth = 0, off_token_index = 0, off_subtree_end = 0, off_parent = 0;
+  size_t off_qt_q0 = 0, off_qt_nq = 0, off_qt_kb_begin = 0, off_kb = 0, off_qt_order = 0;
+  size_t off_kt_k0 = 0, off_kt_nk = 0, off_kt_qb_begin = 0, off_qb = 0, off_kt_order = 0;
+};
+
+// Returns a TPK_* status; on success fills *out.
+int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs,
+               const uint8_t* trained, const int32_t* group_ids,
+               const PlanOptions& opts, Plan* out);
+
+}  // namespace tpk

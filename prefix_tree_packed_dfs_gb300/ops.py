@@ -1,0 +1,253 @@
+"""Torch-facing wrappers over the C ABI (same names as ``include/tpk.h``).
+
+PyTorch only provides device memory and the current stream; the wrappers check
+dtypes/shapes/contiguity, allocate outputs with torch and pass raw pointers.
+"""
+import ctypes
+import math
+
+import numpy as np
+import torch
+
+from . import binding as B
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t, dtype, name, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (no CPU path exists)" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dims" % (name, ndim))
+
+
+class Plan:
+    """Host packing plan (``tpk_plan_build``)."""
+
+    def __init__(self, tokens, seq_offsets, trained=None, group_ids=None, row_capacity=65536,
+                 min_shared=64, placement="bfd"):
+        lib = B.load()
+        self._lib = lib
+        self._h = None
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+        offs = np.ascontiguousarray(seq_offsets, dtype=np.int64)
+        n = len(offs) - 1
+        tr = None if trained is None else np.ascontiguousarray(trained, dtype=np.uint8)
+        gr = None if group_ids is None else np.ascontiguousarray(group_ids, dtype=np.int32)
+        if tr is not None and len(tr) != len(tokens):
+            raise ValueError("trained must have one flag per token")
+        if gr is not None and len(gr) != n:
+            raise ValueError("group_ids must have one id per sequence")
+        opts = B.PlanOpts(int(row_capacity), int(min_shared),
+                          B.PLACE_BFD if placement == "bfd" else B.PLACE_NEXT_FIT)
+        h = ctypes.c_void_p()
+        st = lib.tpk_plan_build(tokens.ctypes.data, offs.ctypes.data, n,
+                                None if tr is None else tr.ctypes.data,
+                                None if gr is None else gr.ctypes.data,
+                                ctypes.byref(opts), ctypes.byref(h))
+        B.check(st, "tpk_plan_build")
+        self._h = h
+        info = B.PlanInfo()
+        B.check(lib.tpk_plan_info_get(h, ctypes.byref(info)), "tpk_plan_info_get")
+        self.info = info.as_dict()
+
+    @classmethod
+    def from_sequences(cls, sequences, trained=None, **kw):
+        seqs = [np.asarray(s) for s in sequences]
+        offs = np.zeros(len(seqs) + 1, dtype=np.int64)
+        offs[1:] = np.cumsum([len(s) for s in seqs])
+        tr = None if trained is None else np.concatenate([np.asarray(t) for t in trained])
+        return cls(np.concatenate(seqs), offs, trained=tr, **kw)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def __getattr__(self, name):
+        info = self.__dict__.get("info")
+        if info is not None and name in info:
+            return info[name]
+        raise AttributeError(name)
+
+    def export(self):
+        i = self.info
+        F, R, n, rows = i["n_fwd"], i["n_raw"], i["n_seqs"], i["n_rows"]
+        out = {
+            "row_offsets": np.zeros(rows + 1, np.int64), "row_loads": np.zeros(rows, np.int64),
+            "row_of_seq": np.zeros(n, np.int32), "fwd_token": np.zeros(F, np.int32),
+            "fwd_src": np.zeros(F, np.int32), "parent": np.zeros(F, np.int32), "depth": np.zeros(F, np.int32),
+            "token_index": np.zeros(R, np.int32), "subtree_end": np.zeros(F, np.int32),
+        }
+        order = ["row_offsets", "row_loads", "row_of_seq", "fwd_token", "fwd_src", "parent", "depth",
+                 "token_index", "subtree_end"]
+        B.check(self._lib.tpk_plan_export(self._h, *[out[k].ctypes.data for k in order]), "tpk_plan_export")
+        return out
+
+    def worklists(self):
+        i = self.info
+        T, NB, KT, NQB = i["n_qtiles"], i["n_kblocks"], i["n_ktiles"], i["n_qblocks"]
+        out = {
+            "qt_q0": np.zeros(T, np.int32), "qt_nq": np.zeros(T, np.int32), "qt_kb_begin": np.zeros(T + 1, np.int32),
+            "kb": np.zeros(2 * NB, np.int32), "qt_order": np.zeros(T, np.int32),
+            "kt_k0": np.zeros(KT, np.int32), "kt_nk": np.zeros(KT, np.int32),
+            "kt_qb_begin": np.zeros(KT + 1, np.int32), "qb": np.zeros(2 * NQB, np.int32),
+            "kt_order": np.zeros(KT, np.int32),
+        }
+        order = ["qt_q0", "qt_nq", "qt_kb_begin", "kb", "qt_order", "kt_k0", "kt_nk", "kt_qb_begin", "qb",
+                 "kt_order"]
+        B.check(self._lib.tpk_plan_worklists(self._h, *[out[k].ctypes.data for k in order]), "tpk_plan_worklists")
+        return out
+
+    def device_bytes(self):
+        return int(self._lib.tpk_plan_device_bytes(self._h))
+
+    def field_offset(self, field):
+        off = ctypes.c_size_t()
+        B.check(self._lib.tpk_plan_field_offset(self._h, field, ctypes.byref(off)), "tpk_plan_field_offset")
+        return off.value
+
+    def to_device(self, device="cuda"):
+        return DevicePlan(self, device)
+
+    def close(self):
+        if self._h is not None:
+            self._lib.tpk_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class DevicePlan:
+    """A plan plus its device image (one torch uint8 buffer)."""
+
+    def __init__(self, plan, device="cuda"):
+        self.plan = plan
+        nbytes = max(plan.device_bytes(), 256)
+        self.image = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        if self.image.data_ptr() % 256:
+            raise RuntimeError("device image not 256-byte aligned")
+        B.check(plan._lib.tpk_plan_upload(plan.handle, _ptr(self.image), _stream()), "tpk_plan_upload")
+        F, R = plan.info["n_fwd"], plan.info["n_raw"]
+        self.depth = self._field(B.FIELD_DEPTH, F)
+        self.token_index = self._field(B.FIELD_TOKEN_INDEX, R)
+        self.subtree_end = self._field(B.FIELD_SUBTREE_END, F)
+        self.parent = self._field(B.FIELD_PARENT, F)
+
+    def _field(self, field, n):
+        off = self.plan.field_offset(field)
+        return self.image[off:off + 4 * n].view(torch.int32)
+
+    @property
+    def n_fwd(self):
+        return self.plan.info["n_fwd"]
+
+    @property
+    def n_raw(self):
+        return self.plan.info["n_raw"]
+
+
+def rope_by_depth(q, k, depth, base, inverse=False):
+    """In-place RoPE of q [F,Hq,d] and/or k [F,Hkv,d] at ``depth`` (int32 [F])."""
+    lib = B.load()
+    ref = q if q is not None else k
+    F, _, d = ref.shape
+    if q is not None:
+        _need(q, torch.bfloat16, "q", 3)
+    if k is not None:
+        _need(k, torch.bfloat16, "k", 3)
+    _need(depth, torch.int32, "depth", 1)
+    if depth.numel() != F or (q is not None and k is not None and k.shape[0] != F):
+        raise ValueError("shape mismatch")
+    Hq = q.shape[1] if q is not None else 0
+    Hkv = k.shape[1] if k is not None else 0
+    B.check(lib.tpk_rope_by_depth(_ptr(q), _ptr(k), _ptr(depth), F, Hq, Hkv, d, float(base),
+                                  1 if inverse else 0, _stream()), "tpk_rope_by_depth")
+
+
+def tree_attn_fwd(dplan, q, k, v, scale=None, out=None, lse=None, dev_err=None):
+    """Forward tree attention; returns (O [F,Hq,d] bf16, LSE [Hq,F] fp32)."""
+    lib = B.load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n, 3)
+    F, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if F != dplan.n_fwd or k.shape != v.shape or k.shape[0] != F or k.shape[2] != d:
+        raise ValueError("shape mismatch")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, F), dtype=torch.float32, device=q.device)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(lse, torch.float32, "lse", 2)
+    st = lib.tpk_tree_attn_fwd(dplan.plan.handle, _ptr(dplan.image), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                               _ptr(lse), Hq, Hkv, d, scale, None, 0, _ptr(dev_err), _stream())
+    B.check(st, "tpk_tree_attn_fwd")
+    return out, lse
+
+
+def attn_workspace_bytes(dplan, Hq, Hkv, d, backward):
+    lib = B.load()
+    return int(lib.tpk_attn_workspace_bytes(dplan.plan.handle, Hq, Hkv, d, 1 if backward else 0))
+
+
+def tree_attn_bwd(dplan, q, k, v, o, lse, do, scale=None, dq=None, dk=None, dv=None, workspace=None,
+                  dev_err=None):
+    """Backward tree attention; returns (dQ, dK, dV) w.r.t. the rotated q, k and v."""
+    lib = B.load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _need(t, torch.bfloat16, n, 3)
+    _need(lse, torch.float32, "lse", 2)
+    F, Hq, d = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = attn_workspace_bytes(dplan, Hq, Hkv, d, True)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib.tpk_tree_attn_bwd(dplan.plan.handle, _ptr(dplan.image), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                               _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), Hq, Hkv, d, scale,
+                               _ptr(workspace), workspace.numel(), _ptr(dev_err), _stream())
+    B.check(st, "tpk_tree_attn_bwd")
+    return dq, dk, dv
+
+
+def scatter_token_index(token_index, src=None, lse_src=None, dst=None, lse_dst=None):
+    """Raw-order copies: dst[r] = src[token_index[r]], lse_dst[:, r] = lse_src[:, token_index[r]]."""
+    lib = B.load()
+    _need(token_index, torch.int32, "token_index", 1)
+    R = token_index.numel()
+    if src is not None:
+        _need(src, torch.bfloat16, "src", 3)
+        F, H, d = src.shape
+        if dst is None:
+            dst = torch.empty((R, H, d), dtype=src.dtype, device=src.device)
+    if lse_src is not None:
+        _need(lse_src, torch.float32, "lse_src", 2)
+        H, F = lse_src.shape
+        if lse_dst is None:
+            lse_dst = torch.empty((H, R), dtype=torch.float32, device=lse_src.device)
+    if src is None and lse_src is None:
+        return None, None
+    d = src.shape[2] if src is not None else 8
+    B.check(lib.tpk_scatter_token_index(_ptr(token_index), R, F, _ptr(src), _ptr(dst), _ptr(lse_src),
+                                        _ptr(lse_dst), H, d, _stream()), "tpk_scatter_token_index")
+    return dst, lse_dst

@@ -1,0 +1,285 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Acceptance (floating point): bf16 outputs O / dQ / dK / dV within max-abs
+1e-2 and relative L2 5e-3 of the oracle; fp32 LSE within 1e-3 absolute.
+Integer work (scatter) is bit-exact; RoPE output is compared to the oracle's
+fp64 rotation rounded once to bf16 (the kernel rounds an fp32 result, so a
+value can land one bf16 step away when the exact result sits next to a
+rounding boundary).
+
+Small workloads are compared element by element in full.  Full-size
+workloads run in the bench's launch configuration and are compared on sampled
+raw tokens, which the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import attention as oa
+from oracle import planner as op
+from oracle.bf16 import round_to_bf16
+from workloads import rng as wrng
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 1e-2
+REL_L2 = 5e-3
+LSE_ABS = 1e-3
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def assert_close(got, ref, what):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(got)), what + ": non-finite values"
+    err = float(np.max(np.abs(got - ref))) if got.size else 0.0
+    rl = rel_l2(got, ref)
+    assert err <= MAX_ABS and rl <= REL_L2, "%s: max-abs %.3g rel-l2 %.3g" % (what, err, rl)
+
+
+@pytest.fixture(scope="module")
+def ops():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from prefix_tree_packed_dfs_gb300 import ops as _ops
+    _ops.B.load()
+    return _ops
+
+
+class Case:
+    """A workload plus its plans (C++ through the ABI, oracle in Python)."""
+
+    def __init__(self, ops, w, with_oracle_plan=True):
+        self.w = w
+        self.plan = ops.Plan.from_sequences(w.sequences, group_ids=w.group_ids, row_capacity=w.row_capacity,
+                                            min_shared=w.min_shared)
+        self.dplan = self.plan.to_device()
+        self.F = self.plan.info["n_fwd"]
+        self.ref = op.plan(w.sequences, group_ids=w.group_ids, min_shared=w.min_shared,
+                           row_capacity=w.row_capacity) if with_oracle_plan else None
+
+    def inputs(self, device, backward=False):
+        w, F = self.w, self.F
+        s = w.seeds
+        Q = wrng.normal_bf16(s["q"], (F, w.n_heads_q, w.head_dim), device)
+        K = wrng.normal_bf16(s["k"], (F, w.n_heads_kv, w.head_dim), device)
+        V = wrng.normal_bf16(s["v"], (F, w.n_heads_kv, w.head_dim), device)
+        dO = wrng.normal_bf16(s["do"], (F, w.n_heads_q, w.head_dim), device) if backward else None
+        return Q, K, V, dO
+
+    def rows(self, key, heads):
+        w = self.w
+        seed = w.seeds[key]
+        elems = heads * w.head_dim
+
+        def get(idx):
+            x = wrng.rows_bf16(seed, np.asarray(idx, dtype=np.int64), elems)
+            return x.to(torch.float64).numpy().reshape(len(idx), heads, w.head_dim)
+        return get
+
+
+def gpu_forward(ops, case, Q, K, V):
+    w = case.w
+    q, k = Q.clone(), K.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.rope_by_depth(q, k, case.dplan.depth, w.rope_base)
+    o, lse = ops.tree_attn_fwd(case.dplan, q, k, V, dev_err=err)
+    o_raw, lse_raw = ops.scatter_token_index(case.dplan.token_index, o, lse)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, "device wait timed out"
+    return q, k, o, lse, o_raw, lse_raw
+
+
+def gpu_backward(ops, case, q, k, V, o, lse, dO):
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dq, dk, dv = ops.tree_attn_bwd(case.dplan, q, k, V, o, lse, dO, dev_err=err)
+    ops.rope_by_depth(dq, dk, case.dplan.depth, case.w.rope_base, inverse=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, "device wait timed out"
+    return dq, dk, dv
+
+
+def f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+# ------------------------------------------------------------ custom shapes
+def _ragged(seed, hq, hkv, d, n_leaves=9, cap=2048):
+    """Random tree whose segment lengths hit tile edges (1, 63..65, 127..129,
+    255..257), several roots per row, duplicate and one-token sequences."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lens = [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 257]
+    used = set()
+
+    def run(n):
+        t = rng.integers(0, 32000, size=n)
+        while int(t[0]) in used:
+            t[0] = rng.integers(0, 32000)
+        used.add(int(t[0]))
+        return t
+    seqs = []
+    roots = [run(int(rng.choice(lens))) for _ in range(2)]
+    for _ in range(n_leaves):
+        s = [roots[int(rng.integers(0, 2))]]
+        for _ in range(int(rng.integers(0, 3))):
+            s.append(run(int(rng.choice(lens))))
+        seqs.append(np.concatenate(s))
+    seqs.append(seqs[0].copy())          # exact duplicate
+    seqs.append(run(1))                   # one-token sequence, its own root
+    return workloads.Workload("ragged%d" % seed, seqs, None, None, 16, cap, hq, hkv, d, 1e4, 9000 + seed)
+
+
+SMALL = {
+    "tiny": lambda: workloads.get("tiny"),
+    "tiny_fit": lambda: workloads.get("tiny_fit"),
+    "deep_small": lambda: workloads.get("deep_small"),
+    "ragged_d128_h1": lambda: _ragged(1, 3, 3, 128),
+    "ragged_d64_gqa2": lambda: _ragged(2, 4, 2, 64),
+    "ragged_d128_gqa4": lambda: _ragged(3, 8, 2, 128, cap=1024),
+}
+
+
+# ------------------------------------------------------------------- RoPE
+@pytest.mark.parametrize("name", ["tiny", "deep_small"])
+def test_rope_by_depth(ops, name):
+    case = Case(ops, SMALL[name]())
+    Q, K, _, _ = case.inputs("cpu")
+    q, k = Q.cuda(), K.cuda()
+    ops.rope_by_depth(q, k, case.dplan.depth, case.w.rope_base)
+    torch.cuda.synchronize()
+    depth = case.ref["depth"]
+    for got, X in ((q, Q), (k, K)):
+        ref = round_to_bf16(oa.rope(X.double().numpy(), depth, case.w.rope_base))
+        g = f64(got)
+        exact = np.mean(g == ref)
+        assert exact > 0.999, exact
+        ulp = np.abs(ref) * 2.0 ** -7 + 1e-30
+        assert np.all(np.abs(g - ref) <= ulp * 1.01)
+    # inverse undoes the rotation up to the two roundings
+    ops.rope_by_depth(q, k, case.dplan.depth, case.w.rope_base, inverse=True)
+    torch.cuda.synchronize()
+    assert np.max(np.abs(f64(q) - Q.double().numpy())) < 0.05
+
+
+# ---------------------------------------------------------------- scatter
+def test_scatter_token_index_bit_exact(ops):
+    case = Case(ops, SMALL["deep_small"]())
+    F, R = case.F, case.plan.info["n_raw"]
+    src = wrng.normal_bf16(77, (F, 8, 128), "cuda")
+    lse = torch.randn(8, F, device="cuda")
+    dst, lse_dst = ops.scatter_token_index(case.dplan.token_index, src, lse)
+    torch.cuda.synchronize()
+    ti = case.ref["token_index"]
+    assert torch.equal(dst.cpu(), src.cpu()[torch.from_numpy(ti)])
+    assert torch.equal(lse_dst.cpu(), lse.cpu()[:, torch.from_numpy(ti)])
+    assert dst.shape == (R, 8, 128)
+
+
+# ---------------------------------------------------------------- forward
+@pytest.mark.parametrize("name", list(SMALL))
+def test_forward_full_parity(ops, name):
+    case = Case(ops, SMALL[name]())
+    Q, K, V, _ = case.inputs("cpu")
+    _, _, o, lse, o_raw, lse_raw = gpu_forward(ops, case, Q.cuda(), K.cuda(), V.cuda())
+    ro, rl, rro, rrl = oa.forward(case.ref, Q, K, V, case.w.rope_base)
+    assert_close(f64(o), ro, name + " O")
+    assert np.max(np.abs(f64(lse) - rl)) <= LSE_ABS, name + " LSE"
+    assert_close(f64(o_raw), rro, name + " O_raw")
+    assert np.max(np.abs(f64(lse_raw) - rrl)) <= LSE_ABS
+
+
+def _sample_raw(case, n, seed):
+    """Raw tokens to check: ends of sequences, fork points and random ones."""
+    ref = case.ref
+    rng = np.random.Generator(np.random.PCG64(seed))
+    off = ref["seq_offsets"]
+    R = int(off[-1])
+    picks = {0, R - 1}
+    for s in rng.choice(len(off) - 1, size=min(4, len(off) - 1), replace=False):
+        picks.add(int(off[s + 1] - 1))
+        picks.add(int(off[s]))
+    forks = np.flatnonzero((ref["parent"][1:] != np.arange(ref["n_fwd"] - 1)))
+    for f in rng.choice(forks, size=min(4, len(forks)), replace=False) if len(forks) else []:
+        picks.add(int(ref["fwd_src"][f + 1]))
+    while len(picks) < n:
+        picks.add(int(rng.integers(0, R)))
+    return sorted(picks)
+
+
+FULL = ["grpo", "agentic"] + ["sweep_%.2f" % r for r in workloads.SWEEP_RHOS] + ["deep"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_forward_full_size_sampled(ops, name):
+    case = Case(ops, workloads.get(name))
+    Q, K, V, _ = case.inputs("cuda")
+    _, _, o, lse, o_raw, lse_raw = gpu_forward(ops, case, Q, K, V)
+    del Q, K, V
+    raw = _sample_raw(case, 16, 5)
+    w = case.w
+    ro, rl = oa.forward_rows(case.ref, case.rows("q", w.n_heads_q), case.rows("k", w.n_heads_kv),
+                             case.rows("v", w.n_heads_kv), raw, w.rope_base)
+    idx = torch.tensor(raw, device="cuda")
+    assert_close(f64(o_raw[idx]), ro, name + " O_raw samples")
+    assert np.max(np.abs(f64(lse_raw[:, idx]) - rl)) <= LSE_ABS
+    # forwarded and raw views agree everywhere (scatter is exact)
+    ti = case.dplan.token_index.long()
+    assert torch.equal(o_raw, o[ti])
+    # every output is finite and every row's softmax weight is positive
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+# --------------------------------------------------------------- backward
+@pytest.mark.parametrize("name", ["tiny", "deep_small", "ragged_d128_h1", "ragged_d64_gqa2", "ragged_d128_gqa4"])
+def test_backward_full_parity(ops, name):
+    case = Case(ops, SMALL[name]())
+    Q, K, V, dO = case.inputs("cpu", backward=True)
+    q, k, o, lse, _, _ = gpu_forward(ops, case, Q.cuda(), K.cuda(), V.cuda())
+    dq, dk, dv = gpu_backward(ops, case, q, k, V.cuda(), o, lse, dO.cuda())
+    rq, rk, rv = oa.backward(case.ref, Q, K, V, dO, case.w.rope_base)
+    assert_close(f64(dq), rq, name + " dQ")
+    assert_close(f64(dk), rk, name + " dK")
+    assert_close(f64(dv), rv, name + " dV")
+
+
+def test_backward_full_size_sampled(ops):
+    case = Case(ops, workloads.get("deep"))
+    w = case.w
+    Q, K, V, dO = case.inputs("cuda", backward=True)
+    q, k, o, lse, _, _ = gpu_forward(ops, case, Q, K, V)
+    del Q, K
+    dq, dk, dv = gpu_backward(ops, case, q, k, V, o, lse, dO)
+    del q, k, V, dO, o
+    rows = (case.rows("q", w.n_heads_q), case.rows("k", w.n_heads_kv), case.rows("v", w.n_heads_kv),
+            case.rows("do", w.n_heads_q))
+    raw = _sample_raw(case, 8, 6)
+    rq = oa.backward_rows_q(case.ref, *rows, raw, w.rope_base)
+    f = case.ref["token_index"][raw]
+    assert_close(f64(dq[torch.tensor(f, device="cuda")]), rq, "deep dQ samples")
+    # keys whose subtrees are short (tails of leaves): the oracle visits every
+    # query below them
+    ref = case.ref
+    leaf_ends = np.flatnonzero(ref["subtree_end"] == np.arange(1, ref["n_fwd"] + 1))
+    rng = np.random.Generator(np.random.PCG64(7))
+    keys = sorted(int(x) - int(rng.integers(0, 40)) for x in rng.choice(leaf_ends, size=3, replace=False))
+    rk, rv = oa.backward_rows_kv(ref, *rows, keys, w.rope_base)
+    kk = torch.tensor(keys, device="cuda")
+    assert_close(f64(dk[kk]), rk, "deep dK samples")
+    assert_close(f64(dv[kk]), rv, "deep dV samples")
+
+
+# ------------------------------------------------------------ properties
+def test_runtime_state_survives_repeated_calls(ops):
+    # two calls in a row give identical results (no hidden state)
+    case = Case(ops, SMALL["ragged_d64_gqa2"]())
+    Q, K, V, dO = case.inputs("cuda", backward=True)
+    a = gpu_forward(ops, case, Q, K, V)
+    b = gpu_forward(ops, case, Q, K, V)
+    assert torch.equal(a[2], b[2]) and torch.equal(a[3], b[3])
+    g1 = gpu_backward(ops, case, a[0], a[1], V, a[2], a[3], dO)
+    g2 = gpu_backward(ops, case, a[0], a[1], V, a[2], a[3], dO)
+    for x, y in zip(g1, g2):
+        assert torch.equal(x, y)   # deterministic backward (no atomics)

@@ -446,3 +446,18 @@ def test_packed_backward_matches_finite_differences():
                     args_m = [Tm if X is T else X for X in (Q, K, V)]
                     fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
                     assert abs(fd - G[f, h, i]) < 1e-6 * max(1.0, abs(fd)), (f, h, i)
+
+
+def test_backward_rows_match_full_backward():
+    seqs, p, Q, K, V = _tiny_tree(3, hq=2, hkv=1, d=8)
+    rng = np.random.Generator(np.random.PCG64(12))
+    dO = rng.standard_normal(Q.shape)
+    dQ, dK, dV = oa.backward(p, Q, K, V, dO, 1e4)
+    rows = lambda X: (lambda i: X[i])
+    raw = [0, 3, p["n_raw"] // 2, p["n_raw"] - 1]
+    dq = oa.backward_rows_q(p, rows(Q), rows(K), rows(V), rows(dO), raw, 1e4)
+    assert np.allclose(dq, dQ[p["token_index"][raw]], atol=1e-12)
+    fw = [0, 1, p["n_fwd"] // 2, p["n_fwd"] - 1]
+    dk, dv = oa.backward_rows_kv(p, rows(Q), rows(K), rows(V), rows(dO), fw, 1e4)
+    assert np.allclose(dk, dK[fw], atol=1e-12)
+    assert np.allclose(dv, dV[fw], atol=1e-12)

@@ -1,0 +1,168 @@
+"""C++ planner (through the C ABI) against the oracle planner: bit-exact.
+
+Host-only: the planner needs no GPU.  Also checks the kernels' work lists
+against visibility computed independently by the oracle (parent walks).
+"""
+import numpy as np
+import pytest
+
+import workloads
+from oracle import planner as op
+
+LAYOUT_KEYS = ["row_offsets", "row_of_seq", "fwd_token", "fwd_src", "parent", "depth", "token_index",
+               "subtree_end"]
+
+
+def _cpp_plan(seqs, trained=None, groups=None, min_shared=64, cap=65536, placement="bfd"):
+    from prefix_tree_packed_dfs_gb300 import ops
+    return ops.Plan.from_sequences(seqs, trained=trained, group_ids=groups, row_capacity=cap,
+                                   min_shared=min_shared, placement=placement)
+
+
+def _compare(seqs, trained=None, groups=None, min_shared=64, cap=65536, placement="bfd"):
+    ref = op.plan(seqs, trained=trained, group_ids=groups, min_shared=min_shared, row_capacity=cap,
+                  placement=placement)
+    got = _cpp_plan(seqs, trained, groups, min_shared, cap, placement)
+    ex = got.export()
+    for k in LAYOUT_KEYS:
+        assert np.array_equal(np.asarray(ex[k], np.int64), np.asarray(ref[k], np.int64)), k
+    assert list(ex["row_loads"]) == ref["row_loads"]
+    info = got.info
+    assert info["n_rows"] == ref["n_rows"] and info["n_fwd"] == ref["n_fwd"] and info["n_raw"] == ref["n_raw"]
+    assert info["n_segments"] == ref["n_segments"]
+    assert info["useful_pairs"] == ref["useful_pairs"]
+    assert info["packing_ratio"] == ref["packing_ratio"]
+    assert info["row_fill_frac"] == ref["row_fill_frac"]
+    assert info["fork_frac"] == ref["fork_frac"]
+    return ref, got
+
+
+@pytest.mark.parametrize("name", [n for n in workloads.ALL if n != "deep"])
+def test_workloads_bit_exact(lib, name):
+    w = workloads.get(name)
+    _compare(w.sequences, None, w.group_ids, w.min_shared, w.row_capacity)
+
+
+@pytest.mark.slow
+def test_deep_workload_bit_exact(lib):
+    w = workloads.get("deep")
+    _compare(w.sequences, None, w.group_ids, w.min_shared, w.row_capacity)
+
+
+@pytest.mark.parametrize("placement", ["bfd", "next_fit"])
+def test_art_example_rows(lib, placement):
+    from tests.test_oracle_pins import _art_example, golden
+    g, seqs, flags, groups, labels = _art_example()
+    exp = golden("art_32_rollouts.json")["expected"]
+    _, got = _compare(seqs, flags, groups, g["min_shared"], g["row_capacity"], placement)
+    key = "best_fit_decreasing_row_loads" if placement == "bfd" else "in_order_row_loads"
+    assert list(got.export()["row_loads"]) == exp[key]
+
+
+def _random_case(rng, alphabet, n_max, len_max):
+    n = int(rng.integers(1, n_max + 1))
+    base = rng.integers(0, alphabet, size=len_max)
+    seqs = []
+    for _ in range(n):
+        cut = int(rng.integers(0, len_max))
+        tail = rng.integers(0, alphabet, size=int(rng.integers(1, max(2, len_max // 2))))
+        seqs.append(np.concatenate([base[:cut], tail]))
+    if rng.random() < 0.3 and n > 1:   # exact duplicates
+        seqs[-1] = seqs[0].copy()
+    return seqs
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_small_bit_exact(lib, seed):
+    rng = np.random.Generator(np.random.PCG64(1000 + seed))
+    seqs = _random_case(rng, int(rng.integers(2, 6)), 12, 24)
+    trained = [rng.integers(0, 2, size=len(s)) for s in seqs] if seed % 3 == 0 else None
+    groups = rng.integers(0, 3, size=len(seqs)) if seed % 2 else None
+    m = int(rng.choice([0, 1, 2, 3, 5, 8, 100]))
+    cap = int(max(len(s) for s in seqs) + rng.integers(0, 40))
+    placement = "next_fit" if seed % 4 == 1 else "bfd"
+    _compare(seqs, trained, groups, m, cap, placement)
+
+
+def test_errors(lib):
+    from prefix_tree_packed_dfs_gb300 import binding as B, ops
+    with pytest.raises(B.TpkError) as e:
+        ops.Plan(np.array([1, 2, 3], np.int32), np.array([0, 3], np.int64), row_capacity=2)
+    assert e.value.status == -2
+    with pytest.raises(B.TpkError) as e:
+        ops.Plan(np.array([1, 2, 3], np.int32), np.array([0, 2, 2, 3], np.int64))
+    assert e.value.status == -1
+    with pytest.raises(B.TpkError) as e:
+        ops.Plan(np.array([1, -2, 3], np.int32), np.array([0, 3], np.int64))
+    assert e.value.status == -1
+    with pytest.raises(B.TpkError) as e:
+        ops.Plan(np.array([1, 2, 3], np.int32), np.array([1, 3], np.int64))
+    assert e.value.status == -1
+
+
+def _visible(parent, F):
+    vis = np.zeros((F, F), dtype=bool)
+    for i in range(F):
+        for j in op.visible_by_parent_walk(parent, i):
+            vis[i, j] = True
+    return vis
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_worklists_cover_exactly_the_tree_mask(lib, seed):
+    rng = np.random.Generator(np.random.PCG64(2000 + seed))
+    seqs = _random_case(rng, 3, 8, 300)
+    m = int(rng.choice([1, 16, 64]))
+    cap = int(max(len(s) for s in seqs) + rng.integers(0, 400))
+    ref = op.plan(seqs, min_shared=m, row_capacity=cap)
+    got = _cpp_plan(seqs, min_shared=m, cap=cap)
+    wl = got.worklists()
+    F = ref["n_fwd"]
+    vis = _visible(ref["parent"], F)
+    kb = wl["kb"].reshape(-1, 2)
+    covered = np.zeros((F, F), dtype=bool)
+    assert sorted(wl["qt_order"]) == list(range(len(wl["qt_q0"])))
+    for t in range(len(wl["qt_q0"])):
+        q0, nq = wl["qt_q0"][t], wl["qt_nq"][t]
+        assert 1 <= nq <= 128
+        keys = []
+        for b in range(wl["qt_kb_begin"][t], wl["qt_kb_begin"][t + 1]):
+            k0, meta = kb[b]
+            nk, full = meta & 0xFFFF, meta >> 16
+            assert 1 <= nk <= 128
+            keys.extend(range(k0, k0 + nk))
+            sub = vis[q0:q0 + nq, k0:k0 + nk]
+            if full:
+                assert sub.all()
+            covered[q0:q0 + nq, k0:k0 + nk] = True
+        assert len(keys) == len(set(keys))           # no key visited twice
+        assert (keys == sorted(keys))
+    assert np.all(covered[vis])                      # every visible pair visited
+    # backward: key tiles' query blocks
+    qb = wl["qb"].reshape(-1, 2)
+    covered[:] = False
+    for u in range(len(wl["kt_k0"])):
+        k0, nk = wl["kt_k0"][u], wl["kt_nk"][u]
+        for c in range(wl["kt_qb_begin"][u], wl["kt_qb_begin"][u + 1]):
+            qs, meta = qb[c]
+            nq, full = meta & 0xFFFF, meta >> 16
+            assert 1 <= nq <= 128
+            if full:
+                assert vis[qs:qs + nq, k0:k0 + nk].all()
+            covered[qs:qs + nq, k0:k0 + nk] = True
+    assert np.all(covered[vis])
+    # tiles stay inside rows
+    ro = ref["row_offsets"]
+    for t in range(len(wl["qt_q0"])):
+        r = np.searchsorted(ro, wl["qt_q0"][t], side="right") - 1
+        assert wl["qt_q0"][t] + wl["qt_nq"][t] <= ro[r + 1]
+
+
+def test_worklists_visit_only_the_ancestor_chain(lib):
+    # work follows forwarded tokens: in the rho=3.56 sweep row the visited key
+    # columns are close to the useful pairs
+    w = workloads.get("sweep_3.56")
+    got = _cpp_plan(w.sequences, groups=w.group_ids, min_shared=w.min_shared, cap=w.row_capacity)
+    info = got.info
+    assert info["visited_pairs"] < 1.1 * info["useful_pairs"] * 2  # diagonal blocks count full squares
+    assert info["visited_pairs"] >= info["useful_pairs"]
