@@ -142,7 +142,8 @@ int tpk_plan_export(const tpk_plan* plan, int64_t* row_offsets, int64_t* row_loa
  * Forward: query tile t covers forwarded [qt_q0[t], qt_q0[t]+qt_nq[t]) inside one
  * row; its key blocks are kb[2*b], kb[2*b+1] for b in [qt_kb_begin[t],
  * qt_kb_begin[t+1]): kb[2b] = first key, kb[2b+1] = count | (full << 16), where
- * full = every key of the block is visible to every query of the tile.  The
+ * full = the block has 128 keys and every one is visible to every query of the
+ * tile (the kernel then skips the mask).  The
  * key set of a tile is the ancestors of its first query plus the tile itself
  * (a contiguous ancestor chain of segment intervals, [ART] "Token-mixing layers").
  * Backward: key tile u covers [kt_k0[u], +kt_nk[u]); its query blocks qb[2c],

@@ -352,9 +352,11 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
       for (auto& iv : ivals) {
         for (int32_t k0 = iv.first; k0 < iv.second; k0 += kTile) {
           const int32_t nk = std::min(kTile, iv.second - k0);
-          // along an ancestor chain subtree ends do not increase, so the last
-          // key of the block has the smallest one
-          const bool full = (k0 + nk - 1 <= q0) && (P.subtree_end[k0 + nk - 1] >= q1);
+          // full: the kernel may skip the mask -- all 128 loaded keys belong
+          // to the block and every one is visible to every query of the tile.
+          // Along an ancestor chain subtree ends do not increase, so the last
+          // key of the block has the smallest one.
+          const bool full = nk == kTile && (k0 + nk - 1 <= q0) && (P.subtree_end[k0 + nk - 1] >= q1);
           P.kb.push_back(k0);
           P.kb.push_back(nk | (full ? (1 << 16) : 0));
           P.visited_pairs += int64_t{kTile} * kTile;
@@ -373,7 +375,7 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
       P.kt_qb_begin.push_back(static_cast<int32_t>(P.qb.size() / 2));
       for (int32_t qs = k0; qs < qend; qs += kTile) {
         const int32_t qe = std::min(qs + kTile, qend);
-        const bool full = (k1 - 1 <= qs) && (min_se >= qe);
+        const bool full = (qe - qs == kTile) && (k1 - 1 <= qs) && (min_se >= qe);
         P.qb.push_back(qs);
         P.qb.push_back((qe - qs) | (full ? (1 << 16) : 0));
       }
