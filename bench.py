@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Benchmark of the prefix-tree-packed DFS attention hot path on GB300.
+
+One step = the whole path over one batch of the deep-tree workload (root of
+4096 tokens, branching factor 1-3 every 256-1024 tokens down to depth 24000,
+128 leaves, rows of 65536 forwarded tokens, 32 query / 8 KV heads, head_dim
+128, bf16):
+    RoPE at depth (Q, K)  ->  tree attention forward (O, LSE)
+    ->  scatter to raw-token order (O, LSE)  ->  tree attention backward
+    (prep, dK/dV pass, dQ pass)  ->  inverse RoPE on dQ, dK.
+The plan (host) is built once for ``value``; the ``e2e`` leg rebuilds it
+every step and moves inputs from pinned host memory and the raw-order LSE
+back, through the same public API.
+
+Metric: raw tokens/s (whole job), with useful TFLOP/s and % of the measured
+dense bf16 peak alongside.  Useful FLOPs count visible (query, key) pairs
+only: 4*d*Hq*pairs forward + 10*d*Hq*pairs backward, pairs = sum(depth+1).
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload instead (rank 0 only).
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOAD = "deep"
+WORKLOAD_DESC = ("deep random tree: root 4096, branching {1,2,3} every 256-1024 tokens to depth 24000, "
+                 "128 leaves, rows 65536, Hq 32 / Hkv 8 / d 128, fwd+bwd")
+METRIC = "tree-attn raw tokens/s, useful TFLOP/s and % of GB300 bf16 dense peak"
+LAUNCHES_PER_STEP = 8   # rope, fwd, scatter rows, scatter lse, bwd prep, bwd dK/dV, bwd dQ, rope inverse
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+class OracleSampler:
+    """The fp64 oracle on a bounded sample of the workload: for raw tokens
+    drawn uniformly from two of its sequences, the forward row and the dQ row
+    (``oracle.attention.forward_rows`` / ``backward_rows_q``).  The input rows
+    of those two sequences are regenerated once, before any timing."""
+
+    def __init__(self, w, plan_ref, seed=0):
+        import torch
+        from workloads import rng as wrng
+        self.w, self.ref = w, plan_ref
+        rng = np.random.Generator(np.random.PCG64(seed))
+        off = plan_ref["seq_offsets"]
+        ti = plan_ref["token_index"]
+        self.seqs = rng.choice(len(off) - 1, size=2, replace=False)
+        rows = np.unique(np.concatenate([ti[off[x]:off[x + 1]] for x in self.seqs]))
+        self.pos = np.full(plan_ref["n_fwd"], -1, dtype=np.int64)
+        self.pos[rows] = np.arange(len(rows))
+        self.vals = {}
+        for key, heads in (("q", w.n_heads_q), ("k", w.n_heads_kv), ("v", w.n_heads_kv), ("do", w.n_heads_q)):
+            v = wrng.rows_bf16(w.seeds[key], rows, heads * w.head_dim).to(torch.float64).numpy()
+            self.vals[key] = v.reshape(len(rows), heads, w.head_dim)
+
+    def getter(self, key):
+        vals, pos = self.vals[key], self.pos
+        return lambda idx: vals[pos[np.asarray(idx, dtype=np.int64)]]
+
+    def run(self, budget_s, seed=0):
+        from oracle import attention as oa
+        rng = np.random.Generator(np.random.PCG64(1000 + seed))
+        off = self.ref["seq_offsets"]
+        Qr, Kr, Vr, dOr = (self.getter(k) for k in ("q", "k", "v", "do"))
+        done, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < budget_s:
+            x = int(rng.choice(self.seqs))
+            r = int(off[x] + rng.integers(0, off[x + 1] - off[x]))
+            oa.forward_rows(self.ref, Qr, Kr, Vr, [r], self.w.rope_base)
+            oa.backward_rows_q(self.ref, Qr, Kr, Vr, dOr, [r], self.w.rope_base)
+            done += 1
+        return done, time.perf_counter() - t0
+
+
+def run_reference(a):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import workloads
+    from oracle import planner as op
+    w = workloads.get(a.workload)
+    ref = op.plan(w.sequences, group_ids=w.group_ids, min_shared=w.min_shared, row_capacity=w.row_capacity)
+    per_step = max(1.0, min(a.cpu_seconds, 120.0 / max(1, a.steps + a.warmup)))
+    sampler = OracleSampler(w, ref)
+    for i in range(a.warmup):
+        sampler.run(per_step / 4, seed=100 + i)
+    n_tot, t_tot = 0, 0.0
+    for i in range(a.steps):
+        n, dt = sampler.run(per_step, seed=i)
+        n_tot += n
+        t_tot += dt
+    value = n_tot / t_tot
+    cores = _cpu_threads()
+    sample = ("fp64 oracle forward row + dQ row for %d raw tokens drawn uniformly from 2 of the 128 "
+              "24000-token sequences (%d steps of ~%.0f s); dK/dV rows not included" % (n_tot, a.steps, per_step))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "raw tokens/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * t_tot / a.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "raw_tokens": ref["n_raw"], "forwarded_tokens": ref["n_fwd"]},
+        "cpu_baseline": {"value": value, "unit": "raw tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "raw tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours(a):
+    import torch
+    import workloads
+    from prefix_tree_packed_dfs_gb300 import ops
+    from workloads import rng as wrng
+
+    world, rank, local = _dist()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (no CPU path exists)")
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    peaks = _peaks()
+    w = workloads.get(a.workload)
+    # weak scaling: every rank owns one batch of the same shape (rows are
+    # independent; no data crosses ranks)
+    seed_shift = 1000 * rank
+    t0 = time.perf_counter()
+    plan = ops.Plan.from_sequences(w.sequences, group_ids=w.group_ids, row_capacity=w.row_capacity,
+                                   min_shared=w.min_shared)
+    plan_s = time.perf_counter() - t0
+    info = plan.info
+    F, R, d, Hq, Hkv = info["n_fwd"], info["n_raw"], w.head_dim, w.n_heads_q, w.n_heads_kv
+    pairs = info["useful_pairs"]
+    dp = plan.to_device()
+    dev = torch.device("cuda", local)
+    s = {k: v + seed_shift for k, v in w.seeds.items()}
+    Q = wrng.normal_bf16(s["q"], (F, Hq, d), dev)
+    K = wrng.normal_bf16(s["k"], (F, Hkv, d), dev)
+    V = wrng.normal_bf16(s["v"], (F, Hkv, d), dev)
+    dO = wrng.normal_bf16(s["do"], (F, Hq, d), dev)
+    qr, kr = torch.empty_like(Q), torch.empty_like(K)
+    O = torch.empty_like(Q)
+    LSE = torch.empty((Hq, F), dtype=torch.float32, device=dev)
+    O_raw = torch.empty((R, Hq, d), dtype=torch.bfloat16, device=dev)
+    LSE_raw = torch.empty((Hq, R), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    ws = torch.empty(max(ops.attn_workspace_bytes(dp, Hq, Hkv, d, True), 256), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    names = ["rope", "fwd", "scatter", "bwd_prep", "bwd_dkdv", "bwd_dq", "rope_inv"]
+
+    def step(dplan, ev=None):
+        mark = (lambda i: ev[i].record()) if ev is not None else (lambda i: None)
+        mark(0)
+        ops.rope_by_depth(Q, K, dplan.depth, w.rope_base, q_out=qr, k_out=kr)
+        mark(1)
+        ops.tree_attn_fwd(dplan, qr, kr, V, out=O, lse=LSE, dev_err=err)
+        mark(2)
+        ops.scatter_token_index(dplan.token_index, O, LSE, dst=O_raw, lse_dst=LSE_raw)
+        mark(3)
+        ops.tree_attn_bwd(dplan, qr, kr, V, O, LSE, dO, dq=dq, dk=dk, dv=dv, workspace=ws, dev_err=err, phases=(0,))
+        mark(4)
+        ops.tree_attn_bwd(dplan, qr, kr, V, O, LSE, dO, dq=dq, dk=dk, dv=dv, workspace=ws, dev_err=err, phases=(1,))
+        mark(5)
+        ops.tree_attn_bwd(dplan, qr, kr, V, O, LSE, dO, dq=dq, dk=dk, dv=dv, workspace=ws, dev_err=err, phases=(2,))
+        mark(6)
+        ops.rope_by_depth(dq, dk, dplan.depth, w.rope_base, inverse=True)
+        mark(7)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(a.warmup):
+        step(dp)
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise SystemExit("device wait timed out (TPK_E_TIMEOUT)")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(a.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    start.record()
+    for i in range(a.steps):
+        step(dp, evs[i])
+    stop.record()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(stop) / a.steps
+    per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(a.steps))
+           for j, n in enumerate(names)}
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    if int(err.item()) != 0:
+        raise SystemExit("device wait timed out (TPK_E_TIMEOUT)")
+
+    # ---- end to end through the public API, host buffers -----------------
+    e2e = None
+    if a.e2e_steps > 0:
+        tokens = np.concatenate(w.sequences).astype(np.int32)
+        offs = w.seq_offsets()
+        hQ, hK, hV, hdO = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (Q, K, V, dO))
+        for h, x in zip((hQ, hK, hV, hdO), (Q, K, V, dO)):
+            h.copy_(x)
+        hLSE = torch.empty((Hq, R), dtype=torch.float32).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (hQ, hK, hV, hdO)) + plan.device_bytes()
+        d2h = hLSE.numel() * hLSE.element_size()
+
+        def e2e_step():
+            p2 = ops.Plan(tokens, offs, group_ids=w.group_ids, row_capacity=w.row_capacity, min_shared=w.min_shared)
+            d2 = p2.to_device(dev)
+            Q.copy_(hQ, non_blocking=True)
+            K.copy_(hK, non_blocking=True)
+            V.copy_(hV, non_blocking=True)
+            dO.copy_(hdO, non_blocking=True)
+            step(d2)
+            hLSE.copy_(LSE_raw, non_blocking=True)
+            torch.cuda.synchronize()
+            return p2, d2
+        e2e_step()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(a.e2e_steps):
+            keep = e2e_step()
+        dt = (time.perf_counter() - t0) / a.e2e_steps
+        del keep
+        if world > 1:
+            t = torch.tensor([dt], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": world * R / dt, "unit": "raw tokens/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": 1e3 * dt,
+               "includes": "plan build on host, plan image + Q/K/V/dO host->device, full step, "
+                           "raw-order LSE device->host"}
+        del hQ, hK, hV, hdO
+
+    # ---- CPU baseline (oracle), rank 0 only ----------------------------------
+    cpu = None
+    if rank == 0 and not a.no_cpu_baseline and a.cpu_seconds > 0:
+        from oracle import planner as op
+        ref = op.plan(w.sequences, group_ids=w.group_ids, min_shared=w.min_shared, row_capacity=w.row_capacity)
+        n, dt = OracleSampler(w, ref).run(a.cpu_seconds)
+        cpu = {"value": n / dt, "unit": "raw tokens/s", "cores": _cpu_threads(), "kind": "oracle",
+               "sample": "fp64 oracle forward row + dQ row for %d raw tokens drawn uniformly from 2 of the 128 "
+                         "24000-token sequences (%.1f s); dK/dV rows not included" % (n, dt)}
+
+    # ---- roofline of the dominant kernel ------------------------------------
+    fwd_flop = 4.0 * d * Hq * pairs
+    bwd_flop = 10.0 * d * Hq * pairs
+    algo = {   # algorithmic FLOPs (tensor kernels) or bytes (HBM kernels) per launch
+        "fwd": ("tensor", fwd_flop),
+        "bwd_dkdv": ("tensor", 8.0 * d * Hq * pairs),     # S^T, dP^T, dV, dK products
+        "bwd_dq": ("tensor", 2.0 * d * Hq * pairs),       # dQ product (S, dP recomputed on top)
+        "rope": ("hbm", F * (Hq + Hkv) * d * 2 * 2 + 4 * F),
+        "rope_inv": ("hbm", F * (Hq + Hkv) * d * 2 * 2 + 4 * F),
+        "scatter": ("hbm", R * Hq * (2 * d + 4) * 2 + 4 * R),
+        "bwd_prep": ("hbm", F * Hq * d * 2 * 2 + 4 * F * Hq),
+    }
+    dom = max(per, key=per.get)
+    bound, amount = algo[dom]
+    secs = per[dom] / 1e3
+    if bound == "tensor":
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": amount / secs / 1e12, "peak": peak,
+                "unit": "TFLOP/s", "frac": amount / secs / 1e12 / peak, "traffic": None,
+                "peak_kind": "sustained bf16 (%s)" % peaks["source"]}
+    else:
+        peak = peaks["hbm_gbs"]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": amount / secs / 1e9, "peak": peak, "unit": "GB/s",
+                "frac": amount / secs / 1e9 / peak, "traffic": None, "peak_kind": "copy bandwidth (%s)" % peaks["source"]}
+    kernels = {}
+    for n in names:
+        b, amt = algo[n]
+        t_s = per[n] / 1e3
+        kernels[n] = {"ms": per[n], ("tflops" if b == "tensor" else "gbs"):
+                      amt / t_s / (1e12 if b == "tensor" else 1e9)}
+
+    useful_tflops = (fwd_flop + bwd_flop) / (ms / 1e3) / 1e12
+    out = {
+        "metric": METRIC, "value": world * R / (ms / 1e3), "unit": "raw tokens/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "raw_tokens": R, "forwarded_tokens": F, "rows": info["n_rows"],
+                   "packing_ratio": info["packing_ratio"], "useful_pairs": pairs,
+                   "visited_pairs_fwd": info["visited_pairs"], "Hq": Hq, "Hkv": Hkv, "head_dim": d,
+                   "row_capacity": w.row_capacity, "l2": "inputs larger than L2 (Q alone %.1f GB)" % (F * Hq * d * 2 / 1e9),
+                   "parallelism": "rows per rank, no collective" if world > 1 else "single GPU"},
+        "useful_tflops": useful_tflops,
+        "pct_of_peak": 100.0 * useful_tflops / peaks["bf16_tflops_sustained"],
+        "pct_of_burst_peak": 100.0 * useful_tflops / peaks["bf16_tflops"],
+        "forwarded_tokens_per_s": world * F / (ms / 1e3),
+        "fwd_tflops": fwd_flop / (per["fwd"] / 1e3) / 1e12,
+        "bwd_tflops": bwd_flop / ((per["bwd_prep"] + per["bwd_dkdv"] + per["bwd_dq"]) / 1e3) / 1e12,
+        "kernels": kernels,
+        "plan_ms": plan_s * 1e3,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": LAUNCHES_PER_STEP * a.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    a = _args()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+
+
+if __name__ == "__main__":
+    main()

@@ -171,15 +171,17 @@ void tpk_plan_destroy(tpk_plan* plan);
 /* ---- GPU kernels (sm_103a) ---------------------------------------------- */
 
 /* RoPE at depth positions ([DAG] "Positions": position id = graph depth, so
- * every parent->child edge has relative distance 1).  In place on q [F,Hq,d]
- * and k [F,Hkv,d] (bf16; either may be NULL).  Pair i < d/2 is (x_i, x_{i+d/2})
- * rotated by angle depth[f] * base^(-2i/d) (by minus that angle when
- * `inverse` != 0, which maps gradients w.r.t. rotated inputs back to the
- * un-rotated ones).  Math in fp32 with the angle reduced in fp64; output
- * rounded to nearest even.  depth: device int32 [F].  d in {64, 128}. */
-int tpk_rope_by_depth(void* q, void* k, const int32_t* depth, int64_t F,
-                      int32_t Hq, int32_t Hkv, int32_t d, double base,
-                      int32_t inverse, void* stream);
+ * every parent->child edge has relative distance 1).  Rotates q_in [F,Hq,d]
+ * into q_out and k_in [F,Hkv,d] into k_out (bf16; out == in is allowed and
+ * rotates in place; a NULL pair skips that tensor).  Pair i < d/2 is
+ * (x_i, x_{i+d/2}) rotated by angle depth[f] * base^(-2i/d) (by minus that
+ * angle when `inverse` != 0, which maps gradients w.r.t. rotated inputs back
+ * to the un-rotated ones).  Math in fp32 with the angle reduced to a fraction
+ * of a turn in fp64; output rounded to nearest even.  depth: device int32
+ * [F].  d in {64, 128}.  Input and output must not partially overlap. */
+int tpk_rope_by_depth(const void* q_in, const void* k_in, void* q_out, void* k_out,
+                      const int32_t* depth, int64_t F, int32_t Hq, int32_t Hkv, int32_t d,
+                      double base, int32_t inverse, void* stream);
 
 /* Workspace bytes for the attention calls (0 for the forward). */
 size_t tpk_attn_workspace_bytes(const tpk_plan* plan, int32_t Hq, int32_t Hkv,
@@ -206,15 +208,35 @@ int tpk_tree_attn_fwd(const tpk_plan* plan, const void* dev_image,
 /* Tree attention backward: gradients of sum_{f,h} <dout[f,h], O[f,h]> w.r.t.
  * the rotated q and k and w.r.t. v (apply tpk_rope_by_depth(inverse=1) to dq
  * and dk for the un-rotated inputs).  o and lse are the forward's outputs.
- * dk, dv are summed over the query heads of each key/value head.
+ * dk, dv are summed over the query heads of each key/value head.  The result
+ * is deterministic (no atomics): dK/dV come from a key-major pass over each
+ * key tile's descendants, dQ from a query-major pass over the forward's
+ * ancestor blocks.
  *   workspace: >= tpk_attn_workspace_bytes(plan, Hq, Hkv, d, 1) bytes, 256-byte
- *   aligned (fp32 dQ accumulator and row terms); contents need not be cleared. */
+ *   aligned (fp32 row terms D = dO.O); contents need not be cleared. */
 int tpk_tree_attn_bwd(const tpk_plan* plan, const void* dev_image,
                       const void* q, const void* k, const void* v,
                       const void* o, const float* lse, const void* dout,
                       void* dq, void* dk, void* dv, int32_t Hq, int32_t Hkv,
                       int32_t d, float scale, void* workspace, size_t ws_bytes,
                       int32_t* dev_err, void* stream);
+
+/* One phase of tpk_tree_attn_bwd (same arguments), for callers that time or
+ * schedule the phases separately.  Phases must run in order 0, then 1 and 2
+ * (1 and 2 are independent of each other):
+ *   TPK_BWD_PREP  D[h,f] = dout[f,h] . o[f,h] into the workspace
+ *   TPK_BWD_DKDV  key-major pass: dk, dv
+ *   TPK_BWD_DQ    query-major pass: dq
+ * Arguments a phase does not read may be NULL. */
+#define TPK_BWD_PREP 0
+#define TPK_BWD_DKDV 1
+#define TPK_BWD_DQ   2
+int tpk_tree_attn_bwd_phase(int32_t phase, const tpk_plan* plan, const void* dev_image,
+                            const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, const void* dout,
+                            void* dq, void* dk, void* dv, int32_t Hq, int32_t Hkv,
+                            int32_t d, float scale, void* workspace, size_t ws_bytes,
+                            int32_t* dev_err, void* stream);
 
 /* Scatter forwarded outputs back to raw-token order ([TRL] "How tree packing
  * works": token_index maps each raw token to its forwarded position):

@@ -501,21 +501,31 @@ int set_smem(Kern kern, size_t bytes, bool& done) {
   return TPK_OK;
 }
 
-template <int D, int NS_KV, int NS_Q>
-int launch_bwd(const BwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const CUtensorMap& tdo, int64_t n_ktiles, int64_t n_qtiles, cudaStream_t stream) {
-  constexpr size_t smem_kv = sizeof(KVSmem<D, NS_KV>) + 1024;
-  constexpr size_t smem_q = sizeof(QSmem<D, NS_Q>) + 1024;
-  static_assert(smem_kv <= 227 * 1024 && smem_q <= 227 * 1024, "shared memory");
-  static bool cfg_kv = false, cfg_q = false;
-  int st = set_smem(bwd_kv_kernel<D, NS_KV>, smem_kv, cfg_kv);
+template <int D, int NS>
+int launch_kv(const BwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+              const CUtensorMap& tdo, int64_t n_ktiles, cudaStream_t stream) {
+  constexpr size_t smem = sizeof(KVSmem<D, NS>) + 1024;
+  static_assert(smem <= 227 * 1024, "shared memory");
+  static bool cfg = false;
+  int st = set_smem(bwd_kv_kernel<D, NS>, smem, cfg);
   if (st != TPK_OK) return st;
-  if ((st = set_smem(bwd_q_kernel<D, NS_Q>, smem_q, cfg_q)) != TPK_OK) return st;
-  const int64_t kv_items = n_ktiles * prm.Hkv, q_items = n_qtiles * prm.Hq;
-  if (kv_items > 0x7fffffff || q_items > 0x7fffffff) return TPK_E_OVERFLOW;
-  if (kv_items > 0) bwd_kv_kernel<D, NS_KV><<<static_cast<unsigned>(kv_items), 256, smem_kv, stream>>>(tq, tk, tv, tdo, prm);
-  if ((st = cuda_status(cudaGetLastError())) != TPK_OK) return st;
-  if (q_items > 0) bwd_q_kernel<D, NS_Q><<<static_cast<unsigned>(q_items), 256, smem_q, stream>>>(tq, tk, tv, tdo, prm);
+  const int64_t items = n_ktiles * prm.Hkv;
+  if (items > 0x7fffffff) return TPK_E_OVERFLOW;
+  if (items > 0) bwd_kv_kernel<D, NS><<<static_cast<unsigned>(items), 256, smem, stream>>>(tq, tk, tv, tdo, prm);
+  return cuda_status(cudaGetLastError());
+}
+
+template <int D, int NS>
+int launch_q(const BwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+             const CUtensorMap& tdo, int64_t n_qtiles, cudaStream_t stream) {
+  constexpr size_t smem = sizeof(QSmem<D, NS>) + 1024;
+  static_assert(smem <= 227 * 1024, "shared memory");
+  static bool cfg = false;
+  int st = set_smem(bwd_q_kernel<D, NS>, smem, cfg);
+  if (st != TPK_OK) return st;
+  const int64_t items = n_qtiles * prm.Hq;
+  if (items > 0x7fffffff) return TPK_E_OVERFLOW;
+  if (items > 0) bwd_q_kernel<D, NS><<<static_cast<unsigned>(items), 256, smem, stream>>>(tq, tk, tv, tdo, prm);
   return cuda_status(cudaGetLastError());
 }
 
@@ -530,14 +540,18 @@ extern "C" size_t tpk_attn_workspace_bytes(const tpk_plan* plan, int32_t Hq, int
   return (static_cast<size_t>(Hq) * static_cast<size_t>(plan->p.F) * 4 + 255) & ~size_t(255);
 }
 
-extern "C" int tpk_tree_attn_bwd(const tpk_plan* plan, const void* dev_image, const void* q, const void* k,
-                                 const void* v, const void* o, const float* lse, const void* dout, void* dq, void* dk,
-                                 void* dv, int32_t Hq, int32_t Hkv, int32_t d, float scale, void* workspace,
-                                 size_t ws_bytes, int32_t* dev_err, void* stream) {
+extern "C" int tpk_tree_attn_bwd_phase(int32_t phase, const tpk_plan* plan, const void* dev_image, const void* q,
+                                       const void* k, const void* v, const void* o, const float* lse,
+                                       const void* dout, void* dq, void* dk, void* dv, int32_t Hq, int32_t Hkv,
+                                       int32_t d, float scale, void* workspace, size_t ws_bytes, int32_t* dev_err,
+                                       void* stream) {
   using namespace tpk;
-  if (!plan || !dev_image || !q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return TPK_E_ARG;
+  if (!plan || phase < TPK_BWD_PREP || phase > TPK_BWD_DQ) return TPK_E_ARG;
   if (Hq <= 0 || Hkv <= 0 || !(scale > 0.f)) return TPK_E_ARG;
   if ((d != 64 && d != 128) || Hq % Hkv != 0) return TPK_E_UNSUPPORTED;
+  if (phase == TPK_BWD_PREP && (!o || !dout)) return TPK_E_ARG;
+  if (phase == TPK_BWD_DKDV && (!dev_image || !q || !k || !v || !lse || !dout || !dk || !dv)) return TPK_E_ARG;
+  if (phase == TPK_BWD_DQ && (!dev_image || !q || !k || !v || !lse || !dout || !dq)) return TPK_E_ARG;
   if ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv) |
        reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dout)) % 16)
     return TPK_E_ARG;
@@ -547,6 +561,17 @@ extern "C" int tpk_tree_attn_bwd(const tpk_plan* plan, const void* dev_image, co
   if (!workspace || ws_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256) return TPK_E_WORKSPACE;
   int st = check_device();
   if (st != TPK_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (phase == TPK_BWD_PREP) {
+    const int64_t warps = P.F * Hq;
+    int64_t blocks = (warps + 7) / 8;
+    const int64_t cap = int64_t{num_sms()} * 32;
+    if (blocks > cap) blocks = cap;
+    bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
+                                                                  static_cast<const __nv_bfloat16*>(dout),
+                                                                  static_cast<float*>(workspace), P.F, Hq, d);
+    return cuda_status(cudaGetLastError());
+  }
   CUtensorMap tq, tk, tv, tdo;
   if ((st = make_map_bf16(&tq, q, P.F, Hq, d, 128)) != TPK_OK) return st;
   if ((st = make_map_bf16(&tk, k, P.F, Hkv, d, 128)) != TPK_OK) return st;
@@ -577,18 +602,21 @@ extern "C" int tpk_tree_attn_bwd(const tpk_plan* plan, const void* dev_image, co
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
   prm.err = dev_err;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  {
-    const int64_t warps = P.F * Hq;
-    int64_t blocks = (warps + 7) / 8;
-    const int64_t cap = int64_t{num_sms()} * 32;
-    if (blocks > cap) blocks = cap;
-    bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
-                                                                  static_cast<const __nv_bfloat16*>(dout),
-                                                                  static_cast<float*>(workspace), P.F, Hq, d);
-    if ((st = cuda_status(cudaGetLastError())) != TPK_OK) return st;
-  }
   const int64_t nkt = static_cast<int64_t>(P.kt_k0.size()), nqt = static_cast<int64_t>(P.qt_q0.size());
-  if (d == 128) return launch_bwd<128, 2, 2>(prm, tq, tk, tv, tdo, nkt, nqt, s);
-  return launch_bwd<64, 4, 4>(prm, tq, tk, tv, tdo, nkt, nqt, s);
+  if (phase == TPK_BWD_DKDV)
+    return d == 128 ? launch_kv<128, 2>(prm, tq, tk, tv, tdo, nkt, s) : launch_kv<64, 4>(prm, tq, tk, tv, tdo, nkt, s);
+  return d == 128 ? launch_q<128, 2>(prm, tq, tk, tv, tdo, nqt, s) : launch_q<64, 4>(prm, tq, tk, tv, tdo, nqt, s);
+}
+
+extern "C" int tpk_tree_attn_bwd(const tpk_plan* plan, const void* dev_image, const void* q, const void* k,
+                                 const void* v, const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                                 void* dv, int32_t Hq, int32_t Hkv, int32_t d, float scale, void* workspace,
+                                 size_t ws_bytes, int32_t* dev_err, void* stream) {
+  if (!plan || !dev_image || !q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return TPK_E_ARG;
+  for (int32_t phase = TPK_BWD_PREP; phase <= TPK_BWD_DQ; ++phase) {
+    const int st = tpk_tree_attn_bwd_phase(phase, plan, dev_image, q, k, v, o, lse, dout, dq, dk, dv, Hq, Hkv, d,
+                                           scale, workspace, ws_bytes, dev_err, stream);
+    if (st != TPK_OK) return st;
+  }
+  return TPK_OK;
 }

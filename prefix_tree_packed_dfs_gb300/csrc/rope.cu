@@ -22,7 +22,8 @@ struct Turns {
   double v[64];   // base^(-2i/d) / (2 pi), i < d/2
 };
 
-__global__ void __launch_bounds__(kThreads) rope_kernel(__nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
+__global__ void __launch_bounds__(kThreads) rope_kernel(const __nv_bfloat16* q_in, const __nv_bfloat16* k_in,
+                                                        __nv_bfloat16* q_out, __nv_bfloat16* k_out,
                                                         const int32_t* __restrict__ depth, int64_t F, int Hq, int Hkv,
                                                         int D, Turns turns, int inverse) {
   __shared__ float cs[kPosPerBlock][64];
@@ -52,17 +53,18 @@ __global__ void __launch_bounds__(kThreads) rope_kernel(__nv_bfloat16* __restric
     const int h = rem / chunks, c = rem % chunks;
     const int64_t f = f0 + p;
     if (f >= F) continue;
-    __nv_bfloat16* row;
+    const __nv_bfloat16* src;
+    __nv_bfloat16* dst;
     if (h < Hq) {
-      if (!q) continue;
-      row = q + (f * Hq + h) * D;
+      src = q_in + (f * Hq + h) * D;
+      dst = q_out + (f * Hq + h) * D;
     } else {
-      if (!k) continue;
-      row = k + (f * Hkv + (h - Hq)) * D;
+      src = k_in + (f * Hkv + (h - Hq)) * D;
+      dst = k_out + (f * Hkv + (h - Hq)) * D;
     }
     const int i0 = c * 8;
-    uint4 ua = *reinterpret_cast<const uint4*>(row + i0);
-    uint4 ub = *reinterpret_cast<const uint4*>(row + half + i0);
+    uint4 ua = *reinterpret_cast<const uint4*>(src + i0);
+    uint4 ub = *reinterpret_cast<const uint4*>(src + half + i0);
     __nv_bfloat16* a = reinterpret_cast<__nv_bfloat16*>(&ua);
     __nv_bfloat16* b = reinterpret_cast<__nv_bfloat16*>(&ub);
 #pragma unroll
@@ -72,21 +74,25 @@ __global__ void __launch_bounds__(kThreads) rope_kernel(__nv_bfloat16* __restric
       a[j] = __float2bfloat16_rn(x * cc - y * ss);
       b[j] = __float2bfloat16_rn(x * ss + y * cc);
     }
-    *reinterpret_cast<uint4*>(row + i0) = ua;
-    *reinterpret_cast<uint4*>(row + half + i0) = ub;
+    *reinterpret_cast<uint4*>(dst + i0) = ua;
+    *reinterpret_cast<uint4*>(dst + half + i0) = ub;
   }
 }
 
 }  // namespace
 }  // namespace tpk
 
-extern "C" int tpk_rope_by_depth(void* q, void* k, const int32_t* depth, int64_t F, int32_t Hq, int32_t Hkv,
-                                 int32_t d, double base, int32_t inverse, void* stream) {
+extern "C" int tpk_rope_by_depth(const void* q_in, const void* k_in, void* q_out, void* k_out,
+                                 const int32_t* depth, int64_t F, int32_t Hq, int32_t Hkv, int32_t d, double base,
+                                 int32_t inverse, void* stream) {
   using namespace tpk;
   if (F < 0 || !depth || (d != 64 && d != 128) || Hq < 0 || Hkv < 0 || !(base > 1.0)) return TPK_E_ARG;
-  if ((q && Hq <= 0) || (k && Hkv <= 0)) return TPK_E_ARG;
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k)) % 16) return TPK_E_ARG;
-  if (F == 0 || (!q && !k)) return TPK_OK;
+  if ((q_in == nullptr) != (q_out == nullptr) || (k_in == nullptr) != (k_out == nullptr)) return TPK_E_ARG;
+  if ((q_in && Hq <= 0) || (k_in && Hkv <= 0)) return TPK_E_ARG;
+  if ((reinterpret_cast<uintptr_t>(q_in) | reinterpret_cast<uintptr_t>(k_in) | reinterpret_cast<uintptr_t>(q_out) |
+       reinterpret_cast<uintptr_t>(k_out)) % 16)
+    return TPK_E_ARG;
+  if (F == 0 || (!q_in && !k_in)) return TPK_OK;
   int st = check_device();
   if (st != TPK_OK) return st;
   Turns turns;
@@ -95,7 +101,8 @@ extern "C" int tpk_rope_by_depth(void* q, void* k, const int32_t* depth, int64_t
   const int64_t blocks = (F + kPosPerBlock - 1) / kPosPerBlock;
   if (blocks > 0x7fffffff) return TPK_E_OVERFLOW;
   rope_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<__nv_bfloat16*>(q), static_cast<__nv_bfloat16*>(k), depth, F, q ? Hq : 0, k ? Hkv : 0, d, turns,
-      inverse);
+      static_cast<const __nv_bfloat16*>(q_in), static_cast<const __nv_bfloat16*>(k_in),
+      static_cast<__nv_bfloat16*>(q_out), static_cast<__nv_bfloat16*>(k_out), depth, F, q_in ? Hq : 0,
+      k_in ? Hkv : 0, d, turns, inverse);
   return cuda_status(cudaGetLastError());
 }

@@ -162,22 +162,30 @@ class DevicePlan:
         return self.plan.info["n_raw"]
 
 
-def rope_by_depth(q, k, depth, base, inverse=False):
-    """In-place RoPE of q [F,Hq,d] and/or k [F,Hkv,d] at ``depth`` (int32 [F])."""
+def rope_by_depth(q, k, depth, base, inverse=False, q_out=None, k_out=None):
+    """RoPE of q [F,Hq,d] and/or k [F,Hkv,d] at ``depth`` (int32 [F]).
+
+    In place unless ``q_out`` / ``k_out`` are given.  Returns (q_out, k_out)."""
     lib = B.load()
     ref = q if q is not None else k
     F, _, d = ref.shape
     if q is not None:
         _need(q, torch.bfloat16, "q", 3)
+        q_out = q if q_out is None else q_out
+        _need(q_out, torch.bfloat16, "q_out", 3)
     if k is not None:
         _need(k, torch.bfloat16, "k", 3)
+        k_out = k if k_out is None else k_out
+        _need(k_out, torch.bfloat16, "k_out", 3)
     _need(depth, torch.int32, "depth", 1)
     if depth.numel() != F or (q is not None and k is not None and k.shape[0] != F):
         raise ValueError("shape mismatch")
     Hq = q.shape[1] if q is not None else 0
     Hkv = k.shape[1] if k is not None else 0
-    B.check(lib.tpk_rope_by_depth(_ptr(q), _ptr(k), _ptr(depth), F, Hq, Hkv, d, float(base),
-                                  1 if inverse else 0, _stream()), "tpk_rope_by_depth")
+    B.check(lib.tpk_rope_by_depth(_ptr(q), _ptr(k), _ptr(q_out) if q is not None else None,
+                                  _ptr(k_out) if k is not None else None, _ptr(depth), F, Hq, Hkv, d,
+                                  float(base), 1 if inverse else 0, _stream()), "tpk_rope_by_depth")
+    return q_out, k_out
 
 
 def tree_attn_fwd(dplan, q, k, v, scale=None, out=None, lse=None, dev_err=None):
@@ -208,8 +216,11 @@ def attn_workspace_bytes(dplan, Hq, Hkv, d, backward):
 
 
 def tree_attn_bwd(dplan, q, k, v, o, lse, do, scale=None, dq=None, dk=None, dv=None, workspace=None,
-                  dev_err=None):
-    """Backward tree attention; returns (dQ, dK, dV) w.r.t. the rotated q, k and v."""
+                  dev_err=None, phases=(0, 1, 2)):
+    """Backward tree attention; returns (dQ, dK, dV) w.r.t. the rotated q, k and v.
+
+    ``phases`` selects the launches (0 prep, 1 dK/dV pass, 2 dQ pass); the
+    default runs all three in order."""
     lib = B.load()
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
         _need(t, torch.bfloat16, n, 3)
@@ -223,10 +234,14 @@ def tree_attn_bwd(dplan, q, k, v, o, lse, do, scale=None, dq=None, dk=None, dv=N
     need = attn_workspace_bytes(dplan, Hq, Hkv, d, True)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    st = lib.tpk_tree_attn_bwd(dplan.plan.handle, _ptr(dplan.image), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
-                               _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), Hq, Hkv, d, scale,
-                               _ptr(workspace), workspace.numel(), _ptr(dev_err), _stream())
-    B.check(st, "tpk_tree_attn_bwd")
+    args = (dplan.plan.handle, _ptr(dplan.image), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+            _ptr(dq), _ptr(dk), _ptr(dv), Hq, Hkv, d, scale, _ptr(workspace), workspace.numel(), _ptr(dev_err),
+            _stream())
+    if tuple(phases) == (0, 1, 2):
+        B.check(lib.tpk_tree_attn_bwd(*args), "tpk_tree_attn_bwd")
+    else:
+        for ph in phases:
+            B.check(lib.tpk_tree_attn_bwd_phase(int(ph), *args), "tpk_tree_attn_bwd_phase")
     return dq, dk, dv
 
 

@@ -48,7 +48,9 @@ def test_gpu_entry_points_reject_bad_arguments_before_any_device_call(lib):
                                  None) == -1
     assert lib.tpk_tree_attn_bwd(None, None, None, None, None, None, None, None, None, None, None, 1, 1, 128,
                                  0.1, None, 0, None, None) == -1
-    assert lib.tpk_rope_by_depth(None, None, None, 10, 1, 1, 96, 1e4, 0, None) == -1
+    assert lib.tpk_rope_by_depth(None, None, None, None, None, 10, 1, 1, 96, 1e4, 0, None) == -1
+    assert lib.tpk_tree_attn_bwd_phase(7, None, None, None, None, None, None, None, None, None, None, None, 1, 1,
+                                       128, 0.1, None, 0, None, None) == -1
     assert lib.tpk_scatter_token_index(None, 1, 1, None, None, None, None, 1, 64, None) == -1
     # empty work is a no-op that never touches the device
     assert lib.tpk_scatter_token_index(ctypes.c_void_p(16), 0, 0, None, None, None, None, 1, 64, None) == 0
