@@ -59,6 +59,7 @@ extern "C" {
 #define TPK_E_CUDA          -5  /* a CUDA runtime/driver call failed */
 #define TPK_E_TIMEOUT       -6  /* a device wait gave up (read from dev_err) */
 #define TPK_E_WORKSPACE     -7  /* workspace missing or smaller than required */
+#define TPK_E_SCRATCH_LIMIT -8  /* problem too large for tpk_tree_attn_bwd_noalloc's static scratch */
 
 /* ---- placement rules ---------------------------------------------------- */
 #define TPK_PLACE_BFD       0   /* [ART] "Bin packing, with a twist": best-fit decreasing
@@ -237,6 +238,28 @@ int tpk_tree_attn_bwd_phase(int32_t phase, const tpk_plan* plan, const void* dev
                             void* dq, void* dk, void* dv, int32_t Hq, int32_t Hkv,
                             int32_t d, float scale, void* workspace, size_t ws_bytes,
                             int32_t* dev_err, void* stream);
+
+/* Backward for callers that cannot allocate device memory at call time.
+ * The pages have no counterpart: this is a deployment variant of
+ * tpk_tree_attn_bwd.  Some hosts own all device memory and give plugins
+ * none when they run; some callers must not call cudaMalloc/cudaFree because
+ * those can synchronise the device; some C runtimes have no device allocator.
+ * This entry point takes the same inputs and outputs as tpk_tree_attn_bwd but
+ * no workspace: its scratch (fp32 D = dO.O, Hq * F * 4 bytes) is a fixed
+ * 32 MiB array inside the library, which every GPU that loads the library
+ * keeps until the process exits.  Problems with Hq * F > 8,388,608 return
+ * TPK_E_SCRATCH_LIMIT (use tpk_tree_attn_bwd with a workspace instead).
+ * The first call on each device looks up the array's device address with
+ * that device current; make that first call before any stream capture.
+ * Every call on a device shares the one array, so calls that overlap on the
+ * GPU (different streams without ordering) race; calls on one stream are
+ * ordered and safe.  Nothing needs clearing: each call overwrites the part it
+ * reads.  Results are identical to tpk_tree_attn_bwd's. */
+int tpk_tree_attn_bwd_noalloc(const tpk_plan* plan, const void* dev_image,
+                              const void* q, const void* k, const void* v,
+                              const void* o, const float* lse, const void* dout,
+                              void* dq, void* dk, void* dv, int32_t Hq, int32_t Hkv,
+                              int32_t d, float scale, int32_t* dev_err, void* stream);
 
 /* Scatter forwarded outputs back to raw-token order ([TRL] "How tree packing
  * works": token_index maps each raw token to its forwarded position):

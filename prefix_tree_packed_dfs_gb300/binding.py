@@ -13,6 +13,7 @@ TPK_OK = 0
 STATUS = {
     0: "TPK_OK", -1: "TPK_E_ARG", -2: "TPK_E_SEQ_TOO_LONG", -3: "TPK_E_OVERFLOW",
     -4: "TPK_E_UNSUPPORTED", -5: "TPK_E_CUDA", -6: "TPK_E_TIMEOUT", -7: "TPK_E_WORKSPACE",
+    -8: "TPK_E_SCRATCH_LIMIT",
 }
 BWD_PREP, BWD_DKDV, BWD_DQ = 0, 1, 2
 PLACE_BFD = 0
@@ -24,7 +25,7 @@ EXPORTS = [
     "tpk_plan_build", "tpk_plan_info_get", "tpk_plan_export", "tpk_plan_worklists",
     "tpk_plan_device_bytes", "tpk_plan_field_offset", "tpk_plan_upload", "tpk_plan_destroy",
     "tpk_rope_by_depth", "tpk_attn_workspace_bytes", "tpk_tree_attn_fwd", "tpk_tree_attn_bwd",
-    "tpk_tree_attn_bwd_phase",
+    "tpk_tree_attn_bwd_phase", "tpk_tree_attn_bwd_noalloc",
     "tpk_scatter_token_index", "tpk_status_string", "tpk_version",
 ]
 
@@ -73,6 +74,7 @@ def _sig(lib):
     lib.tpk_tree_attn_fwd.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, ctypes.c_float, P, SZ, P, P]
     lib.tpk_tree_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, ctypes.c_float, P, SZ, P, P]
     lib.tpk_tree_attn_bwd_phase.argtypes = [I32] + lib.tpk_tree_attn_bwd.argtypes
+    lib.tpk_tree_attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, ctypes.c_float, P, P]
     lib.tpk_scatter_token_index.argtypes = [P, I64, I64, P, P, P, P, I32, I32, P]
     lib.tpk_status_string.argtypes = [ctypes.c_int]
     lib.tpk_status_string.restype = ctypes.c_char_p

@@ -138,6 +138,7 @@ const char* tpk_status_string(int status) {
     case TPK_E_CUDA: return "CUDA call failed";
     case TPK_E_TIMEOUT: return "a device wait gave up";
     case TPK_E_WORKSPACE: return "workspace missing or too small";
+    case TPK_E_SCRATCH_LIMIT: return "problem too large for the no-allocation backward's 32 MiB static scratch (Hq * F > 8388608)";
     default: return "unknown status";
   }
 }

@@ -620,3 +620,62 @@ extern "C" int tpk_tree_attn_bwd(const tpk_plan* plan, const void* dev_image, co
   }
   return TPK_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Backward without any device allocation by the caller.
+//
+// Some callers cannot hand the library a workspace: hosts that own all device
+// memory and give their plugins none at call time, code that must not call
+// cudaMalloc/cudaFree because those calls can synchronise the device, and C
+// runtimes with no device allocator at all.  For them the backward's only
+// scratch -- the fp32 row terms D[h, f] = dO . O -- lives in this fixed,
+// file-scope device array instead.  Every GPU that loads the library keeps it
+// (32 MiB) until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace tpk {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t{32} << 20;   // 32 MiB: Hq * F <= 8,388,608
+static __device__ __align__(256) uint8_t g_bwd_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_bwd_scratch on the current device, looked up once per
+// device (with that device current) and cached.
+int scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TPK_E_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return TPK_E_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) return TPK_E_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return TPK_OK;
+}
+
+}  // namespace
+}  // namespace tpk
+
+extern "C" int tpk_tree_attn_bwd_noalloc(const tpk_plan* plan, const void* dev_image, const void* q, const void* k,
+                                         const void* v, const void* o, const float* lse, const void* dout, void* dq,
+                                         void* dk, void* dv, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                                         int32_t* dev_err, void* stream) {
+  using namespace tpk;
+  if (!plan || Hq <= 0 || Hkv <= 0) return TPK_E_ARG;
+  const size_t need = tpk_attn_workspace_bytes(plan, Hq, Hkv, d, 1);
+  if (need > kStaticScratchBytes) return TPK_E_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  int st = scratch_address(&scratch);
+  if (st != TPK_OK) return st;
+  // D is written in full by the first phase before anything reads it, so the
+  // shared array needs no clearing between calls.
+  return tpk_tree_attn_bwd(plan, dev_image, q, k, v, o, lse, dout, dq, dk, dv, Hq, Hkv, d, scale, scratch,
+                           kStaticScratchBytes, dev_err, stream);
+}
