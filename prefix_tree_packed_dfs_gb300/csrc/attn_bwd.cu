@@ -94,19 +94,33 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
 }
 
 // ----------------------------------------------------------------- pass 2
+// Key-major dK/dV.  Each step (query block, query head) is split into two
+// 64-query halves that alternate between two TMEM slots, so the tensor cores
+// run one half's products while a softmax warpgroup works on the other:
+//   MMA order per step n:  S/dP(n, half 0) | dV/dK(n-1, half 1) | S/dP(n, half 1) | dV/dK(n, half 0)
+// TMEM: slot h at [128h, 128h+128): S^T (64 cols) then dP^T (64 cols);
+// dV at [256, 256+D), dK at [256+D, 256+2D).  P^T and dS^T (bf16) overwrite
+// the first 32 columns of S^T and dP^T of their slot.
+// Warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 2 loads LSE*log2(e) and D
+// of each step's 128 queries into shared memory, 4-7 softmax of half 0,
+// 8-11 softmax of half 1.
+constexpr int kHalf = 64;
+
 template <int D, int NS>
 struct KVSmem {
   uint8_t k[D / 64][kBox];
   uint8_t v[D / 64][kBox];
   uint8_t q[NS][D / 64][kBox];
   uint8_t dO[NS][D / 64][kBox];
-  uint64_t kv_full, q_full[NS], q_empty[NS], s_full, p_full, acc_done, drain;
+  float lse2[NS][BT];   // LSE * log2(e) of the step's queries (+inf past the block)
+  float dsum[NS][BT];   // D = dO . O
+  uint64_t kv_full, q_full[NS], q_empty[NS], stat_full[NS], s_full[2], p_full[2], acc_done, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
 template <int D, int NS>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
@@ -114,6 +128,7 @@ __global__ void __launch_bounds__(256, 1)
   extern __shared__ uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   volatile int* abort_flag = &S.abort_flag;
 
   const int item = blockIdx.x;
@@ -124,18 +139,19 @@ __global__ void __launch_bounds__(256, 1)
   const int nk = __ldg(p.kt_nk + tile);
   const int qb_begin = __ldg(p.kt_qb_begin + tile);
   const int n_steps = (__ldg(p.kt_qb_begin + tile + 1) - qb_begin) * G;
-
-  // TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+D), dK [256+D, 256+2D)
-  constexpr uint32_t cS = 0, cdP = 128, cdV = 256, cdK = 256 + D;
+  constexpr uint32_t cdV = 256, cdK = 256 + D;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&S.kv_full, 1);
     for (int s = 0; s < NS; ++s) {
       ptx::mbar_init(&S.q_full[s], 1);
       ptx::mbar_init(&S.q_empty[s], 1);
+      ptx::mbar_init(&S.stat_full[s], 1);
     }
-    ptx::mbar_init(&S.s_full, 1);
-    ptx::mbar_init(&S.p_full, 128);
+    for (int h = 0; h < 2; ++h) {
+      ptx::mbar_init(&S.s_full[h], 1);
+      ptx::mbar_init(&S.p_full[h], 128);
+    }
     ptx::mbar_init(&S.acc_done, 1);
     ptx::mbar_init(&S.drain, 1);
     S.abort_flag = 0;
@@ -151,6 +167,7 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t tmem = S.tmem_base;
 
   if (warp == 0) {
+    // ------------------------------------------------------------ producer
     if (ptx::elect_one()) {
       ptx::mbar_arrive_expect_tx(&S.kv_full, 2 * D * 256);
       for (int c = 0; c < D / 64; ++c) {
@@ -176,116 +193,171 @@ __global__ void __launch_bounds__(256, 1)
         ptx::mbar_drain(&S.kv_full, 0);
       }
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ row terms
+    for (int n = 0; n < n_steps; ++n) {
+      const int st = n % NS;
+      const uint32_t use = n / NS;
+      bool ok = n < NS || ptx::mbar_wait(&S.q_empty[st], (use - 1) & 1, abort_flag, kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int2 blk = __ldg(&p.qb[qb_begin + n / G]);
+      const int qs = blk.x, nq = blk.y & 0xFFFF;
+      const int h = g * G + n % G;
+      const float* lse_h = p.lse + static_cast<int64_t>(h) * p.F;
+      const float* dsum_h = p.dsum + static_cast<int64_t>(h) * p.F;
+      for (int c = lane; c < BT; c += 32) {
+        const bool in = c < nq;
+        S.lse2[st][c] = in ? __ldg(lse_h + qs + c) * kLog2e : INFINITY;
+        S.dsum[st][c] = in ? __ldg(dsum_h + qs + c) : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.stat_full[st]);
+    }
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (ptx::elect_one()) {
-      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(BT, BT, false, false);
+      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(BT, kHalf, false, false);
       constexpr uint32_t idesc_acc = ptx::idesc_bf16_f32(BT, D, false, true);
       bool ok = ptx::mbar_wait(&S.kv_full, 0, abort_flag, kWaitLimitNs);
       ptx::tc_fence_after();
       const uint32_t k_base = ptx::smem_addr(S.k[0]);
       const uint32_t v_base = ptx::smem_addr(S.v[0]);
-      for (int n = 0; ok && n < n_steps; ++n) {
-        const int st = n % NS;
-        if (!ptx::mbar_wait(&S.q_full[st], (n / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-        ptx::tc_fence_after();
-        const uint32_t q_base = ptx::smem_addr(S.q[st][0]);
-        const uint32_t do_base = ptx::smem_addr(S.dO[st][0]);
+      // S^T, dP^T of one 64-query half (rows half*64.. of the Q / dO stage)
+      auto issue_sdp = [&](int st, int half) {
+        const uint32_t qb = ptx::smem_addr(S.q[st][0]) + half * (kHalf * 128);
+        const uint32_t ob = ptx::smem_addr(S.dO[st][0]) + half * (kHalf * 128);
+        const uint32_t cS = BT * half, cdP = BT * half + kHalf;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cS, ptx::sw128_desc(k_base + koff, 16, 1024), ptx::sw128_desc(q_base + koff, 16, 1024),
+          ptx::mma_ss(tmem + cS, ptx::sw128_desc(k_base + koff, 16, 1024), ptx::sw128_desc(qb + koff, 16, 1024),
                       idesc_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cdP, ptx::sw128_desc(v_base + koff, 16, 1024),
-                      ptx::sw128_desc(do_base + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          ptx::mma_ss(tmem + cdP, ptx::sw128_desc(v_base + koff, 16, 1024), ptx::sw128_desc(ob + koff, 16, 1024),
+                      idesc_s, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(&S.s_full);
-        if (!ptx::mbar_wait(&S.p_full, n & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-        ptx::tc_fence_after();
+        ptx::mma_commit(&S.s_full[half]);
+      };
+      // dV += P^T dO_half, dK += dS^T Q_half (B operands MN-major: N = head dim)
+      auto issue_acc = [&](int st, int half, bool first) {
+        const uint32_t qb = ptx::smem_addr(S.q[st][0]) + half * (kHalf * 128);
+        const uint32_t ob = ptx::smem_addr(S.dO[st][0]) + half * (kHalf * 128);
+        const uint32_t cS = BT * half, cdP = BT * half + kHalf;
 #pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk) {
-          // B operands dO / Q blocks are MN-major: N = head dim, K = 16 queries per step
-          const uint32_t acc = (n > 0 || kk > 0) ? 1u : 0u;
-          ptx::mma_ts(tmem + cdV, tmem + cS + kk * 8, ptx::sw128_desc(do_base + kk * 2048, kBox, 1024), idesc_acc, acc);
-          ptx::mma_ts(tmem + cdK, tmem + cdP + kk * 8, ptx::sw128_desc(q_base + kk * 2048, kBox, 1024), idesc_acc, acc);
+        for (int kk = 0; kk < kHalf / 16; ++kk) {
+          const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+          ptx::mma_ts(tmem + cdV, tmem + cS + kk * 8, ptx::sw128_desc(ob + kk * 2048, kBox, 1024), idesc_acc, acc);
+          ptx::mma_ts(tmem + cdK, tmem + cdP + kk * 8, ptx::sw128_desc(qb + kk * 2048, kBox, 1024), idesc_acc, acc);
         }
-        ptx::mma_commit(&S.q_empty[st]);
+      };
+      for (int n = 0; ok && n < n_steps; ++n) {
+        const int st = n % NS;
+        if (!ptx::mbar_wait(&S.q_full[st], (n / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+        ptx::tc_fence_after();
+        issue_sdp(st, 0);
+        if (n > 0) {
+          if (!ptx::mbar_wait(&S.p_full[1], (n - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          ptx::tc_fence_after();
+          issue_acc((n - 1) % NS, 1, false);
+          ptx::mma_commit(&S.q_empty[(n - 1) % NS]);
+        }
+        issue_sdp(st, 1);
+        if (!ptx::mbar_wait(&S.p_full[0], n & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+        ptx::tc_fence_after();
+        issue_acc(st, 0, n == 0);
       }
-      if (ok) ptx::mma_commit(&S.acc_done);
+      if (ok && n_steps > 0) {
+        const int last = n_steps - 1;
+        if (ptx::mbar_wait(&S.p_full[1], last & 1, abort_flag, kWaitLimitNs)) {
+          ptx::tc_fence_after();
+          issue_acc(last % NS, 1, false);
+          ptx::mma_commit(&S.acc_done);
+        }
+      }
       ptx::mma_commit(&S.drain);
       ptx::mbar_drain(&S.drain, 0);
     }
   } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int half = (warp - 4) >> 2;        // which 64 queries of a step
     const int wq = warp & 3;
-    const int t = wq * 32 + (threadIdx.x & 31);
-    const int j = k0 + t;                        // this thread's key
+    const int t = wq * 32 + lane;
+    const int j = k0 + t;                    // this thread's key
     const int se_j = t < nk ? __ldg(p.subtree_end + j) : -1;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + BT * half, tdP = tS + kHalf;
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int n = 0; n < n_steps; ++n) {
-      ok = ptx::mbar_wait(&S.s_full, n & 1, abort_flag, kWaitLimitNs);
+      const int st = n % NS;
+      ok = ptx::mbar_wait(&S.s_full[half], n & 1, abort_flag, kWaitLimitNs) &&
+           ptx::mbar_wait(&S.stat_full[st], (n / NS) & 1, abort_flag, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
       const int2 blk = __ldg(&p.qb[qb_begin + n / G]);
       const int qs = blk.x, nq = blk.y & 0xFFFF;
       const bool full = (blk.y >> 16) & 1;
-      const int h = g * G + n % G;
-      const float* lse_h = p.lse + static_cast<int64_t>(h) * p.F;
-      const float* dsum_h = p.dsum + static_cast<int64_t>(h) * p.F;
+      // visible queries of this key form one column range [lo, hi) of the half:
+      // i >= j (causal) and i < subtree_end[j], inside the block
+      const int base = qs + half * kHalf;
+      const int lo = full ? 0 : max(0, j - base);
+      const int hi = full ? kHalf : min(min(nq - half * kHalf, kHalf), se_j - base);
+      const float* l2s = S.lse2[st] + half * kHalf;
+      const float* dds = S.dsum[st] + half * kHalf;
 #pragma unroll
-      for (int c = 0; c < BT / 32; ++c) {
+      for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t us[32], ud[32];
-        ptx::tmem_ld32(tmem + lane_off + cS + c * 32, us);
-        ptx::tmem_ld32(tmem + lane_off + cdP + c * 32, ud);
+        ptx::tmem_ld32(tS + c * 32, us);
+        ptx::tmem_ld32(tdP + c * 32, ud);
         ptx::tmem_wait_ld();
         uint32_t pp[16], pd[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], dv[2];
+        for (int e = 0; e < 32; e += 4) {
+          const float4 l4 = ptx::lds128(l2s + c * 32 + e);
+          const float4 d4 = ptx::lds128(dds + c * 32 + e);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], dv[4];
 #pragma unroll
-          for (int x = 0; x < 2; ++x) {
+          for (int x = 0; x < 4; ++x) {
             const int col = c * 32 + e + x;
-            const int i = qs + col;
-            const bool in = col < nq;
-            const bool vis = in && (full || (j <= i && i < se_j));
-            const float l2 = in ? __ldg(lse_h + i) * kLog2e : 0.f;
-            const float dd = in ? __ldg(dsum_h + i) : 0.f;
-            const float pr = vis ? ptx::ex2(fmaf(__uint_as_float(us[e + x]), sl2, -l2)) : 0.f;
-            pv[x] = pr;
-            dv[x] = pr * (__uint_as_float(ud[e + x]) - dd);
+            float arg = fmaf(__uint_as_float(us[e + x]), sl2, -lv[x]);
+            arg = (col >= lo && col < hi) ? arg : -INFINITY;
+            pv[x] = ptx::ex2(arg);
+            dv[x] = pv[x] * (__uint_as_float(ud[e + x]) - dvv[x]);
           }
           pp[e / 2] = ptx::pack_bf16x2(pv[0], pv[1]);
+          pp[e / 2 + 1] = ptx::pack_bf16x2(pv[2], pv[3]);
           pd[e / 2] = ptx::pack_bf16x2(dv[0], dv[1]);
+          pd[e / 2 + 1] = ptx::pack_bf16x2(dv[2], dv[3]);
         }
-        ptx::tmem_st16(tmem + lane_off + cS + c * 16, pp);
-        ptx::tmem_st16(tmem + lane_off + cdP + c * 16, pd);
+        ptx::tmem_st16(tS + c * 16, pp);
+        ptx::tmem_st16(tdP + c * 16, pd);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&S.p_full);
+      ptx::mbar_arrive(&S.p_full[half]);
     }
     if (ok) {
       ok = ptx::mbar_wait(&S.acc_done, 0, abort_flag, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
+      // epilogue: warpgroup of half 0 writes dV, the other dK
       ptx::tc_fence_after();
-      __nv_bfloat16* dv_row = p.dv + (static_cast<int64_t>(j) * p.Hkv + g) * D;
-      __nv_bfloat16* dk_row = p.dk + (static_cast<int64_t>(j) * p.Hkv + g) * D;
+      const uint32_t col = half == 0 ? cdV : cdK;
+      const float mul = half == 0 ? 1.f : p.scale;
+      __nv_bfloat16* row = (half == 0 ? p.dv : p.dk) + (static_cast<int64_t>(j) * p.Hkv + g) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t u[32];
-        ptx::tmem_ld32(tmem + lane_off + cdV + c * 32, u);
+        ptx::tmem_ld32(tmem + lane_off + col + c * 32, u);
         ptx::tmem_wait_ld();
-        if (t < nk) store_row32(dv_row + c * 32, u, 1.f);
-        ptx::tmem_ld32(tmem + lane_off + cdK + c * 32, u);
-        ptx::tmem_wait_ld();
-        if (t < nk) store_row32(dk_row + c * 32, u, p.scale);
+        if (t < nk) store_row32(row + c * 32, u, mul);
       }
     }
   }
@@ -300,19 +372,26 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 // ----------------------------------------------------------------- pass 3
+// Query-major dQ.  Each key block of the forward's list is split into two
+// 64-key halves alternating between two TMEM slots (same ping-pong as pass 2):
+//   MMA order per block i:  S/dP(i, half 0) | dQ(i-1, half 1) | S/dP(i, half 1) | dQ(i, half 0)
+// TMEM: slot h at [128h, 128h+128): S (64 cols) then dP (64 cols); dQ at
+// [256, 256+D).  dS (bf16) overwrites the first 32 columns of S of its slot.
+// Warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 4-7 softmax of half 0,
+// 8-11 softmax of half 1 (thread t owns query row t).
 template <int D, int NS>
 struct QSmem {
   uint8_t q[D / 64][kBox];
   uint8_t dO[D / 64][kBox];
   uint8_t k[NS][D / 64][kBox];
   uint8_t v[NS][D / 64][kBox];
-  uint64_t q_full, kv_full[NS], kv_empty[NS], s_full, p_full, acc_done, drain;
+  uint64_t q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], acc_done, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
 template <int D, int NS>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                  const BwdParams p) {
@@ -330,9 +409,7 @@ __global__ void __launch_bounds__(256, 1)
   const int nq = __ldg(p.qt_nq + tile);
   const int kb_begin = __ldg(p.qt_kb_begin + tile);
   const int n_blocks = __ldg(p.qt_kb_begin + tile + 1) - kb_begin;
-
-  // TMEM columns: S [0,128), dP [128,256), dQ [256, 256+D)
-  constexpr uint32_t cS = 0, cdP = 128, cdQ = 256;
+  constexpr uint32_t cdQ = 256;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&S.q_full, 1);
@@ -340,8 +417,10 @@ __global__ void __launch_bounds__(256, 1)
       ptx::mbar_init(&S.kv_full[s], 1);
       ptx::mbar_init(&S.kv_empty[s], 1);
     }
-    ptx::mbar_init(&S.s_full, 1);
-    ptx::mbar_init(&S.p_full, 128);
+    for (int x = 0; x < 2; ++x) {
+      ptx::mbar_init(&S.s_full[x], 1);
+      ptx::mbar_init(&S.p_full[x], 128);
+    }
     ptx::mbar_init(&S.acc_done, 1);
     ptx::mbar_init(&S.drain, 1);
     S.abort_flag = 0;
@@ -383,97 +462,130 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (warp == 1) {
     if (ptx::elect_one()) {
-      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(BT, BT, false, false);
+      constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(BT, kHalf, false, false);
       constexpr uint32_t idesc_dq = ptx::idesc_bf16_f32(BT, D, false, true);
       bool ok = ptx::mbar_wait(&S.q_full, 0, abort_flag, kWaitLimitNs);
       ptx::tc_fence_after();
       const uint32_t q_base = ptx::smem_addr(S.q[0]);
       const uint32_t do_base = ptx::smem_addr(S.dO[0]);
-      for (int i = 0; ok && i < n_blocks; ++i) {
-        const int st = i % NS;
-        if (!ptx::mbar_wait(&S.kv_full[st], (i / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-        ptx::tc_fence_after();
-        const uint32_t k_base = ptx::smem_addr(S.k[st][0]);
-        const uint32_t v_base = ptx::smem_addr(S.v[st][0]);
+      auto issue_sdp = [&](int st, int half) {
+        const uint32_t kb = ptx::smem_addr(S.k[st][0]) + half * (kHalf * 128);
+        const uint32_t vb = ptx::smem_addr(S.v[st][0]) + half * (kHalf * 128);
+        const uint32_t cS = BT * half, cdP = BT * half + kHalf;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cS, ptx::sw128_desc(q_base + koff, 16, 1024), ptx::sw128_desc(k_base + koff, 16, 1024),
+          ptx::mma_ss(tmem + cS, ptx::sw128_desc(q_base + koff, 16, 1024), ptx::sw128_desc(kb + koff, 16, 1024),
                       idesc_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cdP, ptx::sw128_desc(do_base + koff, 16, 1024),
-                      ptx::sw128_desc(v_base + koff, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          ptx::mma_ss(tmem + cdP, ptx::sw128_desc(do_base + koff, 16, 1024), ptx::sw128_desc(vb + koff, 16, 1024),
+                      idesc_s, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(&S.s_full);
-        if (!ptx::mbar_wait(&S.p_full, i & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-        ptx::tc_fence_after();
+        ptx::mma_commit(&S.s_full[half]);
+      };
+      // dQ += dS_half K_half (K block rows half*64.. as the MN-major B operand)
+      auto issue_dq = [&](int st, int half, bool first) {
+        const uint32_t kb = ptx::smem_addr(S.k[st][0]) + half * (kHalf * 128);
+        const uint32_t cS = BT * half;
 #pragma unroll
-        for (int kk = 0; kk < BT / 16; ++kk)
-          ptx::mma_ts(tmem + cdQ, tmem + cS + kk * 8, ptx::sw128_desc(k_base + kk * 2048, kBox, 1024), idesc_dq,
-                      (i > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(&S.kv_empty[st]);
+        for (int kk = 0; kk < kHalf / 16; ++kk)
+          ptx::mma_ts(tmem + cdQ, tmem + cS + kk * 8, ptx::sw128_desc(kb + kk * 2048, kBox, 1024), idesc_dq,
+                      (first && kk == 0) ? 0u : 1u);
+      };
+      for (int i = 0; ok && i < n_blocks; ++i) {
+        const int st = i % NS;
+        if (!ptx::mbar_wait(&S.kv_full[st], (i / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+        ptx::tc_fence_after();
+        issue_sdp(st, 0);
+        if (i > 0) {
+          if (!ptx::mbar_wait(&S.p_full[1], (i - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          ptx::tc_fence_after();
+          issue_dq((i - 1) % NS, 1, false);
+          ptx::mma_commit(&S.kv_empty[(i - 1) % NS]);
+        }
+        issue_sdp(st, 1);
+        if (!ptx::mbar_wait(&S.p_full[0], i & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+        ptx::tc_fence_after();
+        issue_dq(st, 0, i == 0);
       }
-      if (ok) ptx::mma_commit(&S.acc_done);
+      if (ok && n_blocks > 0) {
+        const int last = n_blocks - 1;
+        if (ptx::mbar_wait(&S.p_full[1], last & 1, abort_flag, kWaitLimitNs)) {
+          ptx::tc_fence_after();
+          issue_dq(last % NS, 1, false);
+          ptx::mma_commit(&S.acc_done);
+        }
+      }
       ptx::mma_commit(&S.drain);
       ptx::mbar_drain(&S.drain, 0);
     }
   } else if (warp >= 4) {
+    const int half = (warp - 4) >> 2;        // which 64 keys of a block
     const int wq = warp & 3;
     const int t = wq * 32 + (threadIdx.x & 31);
-    const int i = q0 + t;                         // this thread's query
+    const int i = q0 + t;                    // this thread's query
     const bool row_ok = t < nq;
     const float l2 = row_ok ? __ldg(p.lse + static_cast<int64_t>(h) * p.F + i) * kLog2e : 0.f;
     const float dd = row_ok ? __ldg(p.dsum + static_cast<int64_t>(h) * p.F + i) : 0.f;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + BT * half, tdP = tS + kHalf;
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int b = 0; b < n_blocks; ++b) {
-      ok = ptx::mbar_wait(&S.s_full, b & 1, abort_flag, kWaitLimitNs);
+      ok = ptx::mbar_wait(&S.s_full[half], b & 1, abort_flag, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
       const int2 blk = __ldg(&p.kb[kb_begin + b]);
       const int kb0 = blk.x, nkb = blk.y & 0xFFFF;
       const bool full = (blk.y >> 16) & 1;
+      const int base = kb0 + half * kHalf;     // first key of this half
 #pragma unroll
-      for (int c = 0; c < BT / 32; ++c) {
+      for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t us[32], ud[32];
-        ptx::tmem_ld32(tmem + lane_off + cS + c * 32, us);
-        ptx::tmem_ld32(tmem + lane_off + cdP + c * 32, ud);
+        ptx::tmem_ld32(tS + c * 32, us);
+        ptx::tmem_ld32(tdP + c * 32, ud);
         ptx::tmem_wait_ld();
+        float arg[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) arg[e] = fmaf(__uint_as_float(us[e]), sl2, -l2);
+        if (!(full && row_ok)) {
+          // partial block: key j visible iff j < block end, j <= i < subtree_end[j]
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = half * kHalf + c * 32 + e;
+            const int jj = base + c * 32 + e;
+            bool vis = row_ok && col < nkb && jj <= i;
+            if (vis) vis = i < __ldg(p.subtree_end + jj);
+            arg[e] = vis ? arg[e] : -INFINITY;
+          }
+        }
         uint32_t pd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float dv[2];
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            const int col = c * 32 + e + x;
-            const int jj = kb0 + col;
-            bool vis = row_ok;
-            if (!full) vis = vis && col < nkb && jj <= i && i < __ldg(p.subtree_end + jj);
-            const float pr = vis ? ptx::ex2(fmaf(__uint_as_float(us[e + x]), sl2, -l2)) : 0.f;
-            dv[x] = pr * (__uint_as_float(ud[e + x]) - dd);
-          }
-          pd[e / 2] = ptx::pack_bf16x2(dv[0], dv[1]);
+          const float d0 = ptx::ex2(arg[e]) * (__uint_as_float(ud[e]) - dd);
+          const float d1 = ptx::ex2(arg[e + 1]) * (__uint_as_float(ud[e + 1]) - dd);
+          pd[e / 2] = ptx::pack_bf16x2(d0, d1);
         }
-        ptx::tmem_st16(tmem + lane_off + cS + c * 16, pd);
+        ptx::tmem_st16(tS + c * 16, pd);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&S.p_full);
+      ptx::mbar_arrive(&S.p_full[half]);
     }
     if (ok) {
       ok = ptx::mbar_wait(&S.acc_done, 0, abort_flag, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
+      // epilogue: each warpgroup writes half of the head dimension
       ptx::tc_fence_after();
       __nv_bfloat16* row = p.dq + (static_cast<int64_t>(i) * p.Hq + h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
         uint32_t u[32];
         ptx::tmem_ld32(tmem + lane_off + cdQ + c * 32, u);
         ptx::tmem_wait_ld();
@@ -511,7 +623,7 @@ int launch_kv(const BwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk
   if (st != TPK_OK) return st;
   const int64_t items = n_ktiles * prm.Hkv;
   if (items > 0x7fffffff) return TPK_E_OVERFLOW;
-  if (items > 0) bwd_kv_kernel<D, NS><<<static_cast<unsigned>(items), 256, smem, stream>>>(tq, tk, tv, tdo, prm);
+  if (items > 0) bwd_kv_kernel<D, NS><<<static_cast<unsigned>(items), 384, smem, stream>>>(tq, tk, tv, tdo, prm);
   return cuda_status(cudaGetLastError());
 }
 
@@ -525,7 +637,7 @@ int launch_q(const BwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk,
   if (st != TPK_OK) return st;
   const int64_t items = n_qtiles * prm.Hq;
   if (items > 0x7fffffff) return TPK_E_OVERFLOW;
-  if (items > 0) bwd_q_kernel<D, NS><<<static_cast<unsigned>(items), 256, smem, stream>>>(tq, tk, tv, tdo, prm);
+  if (items > 0) bwd_q_kernel<D, NS><<<static_cast<unsigned>(items), 384, smem, stream>>>(tq, tk, tv, tdo, prm);
   return cuda_status(cudaGetLastError());
 }
 
