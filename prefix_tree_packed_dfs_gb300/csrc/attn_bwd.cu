@@ -83,6 +83,12 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   }
 }
 
+// Barrier over the `count` threads of one warpgroup (ids 1.. are free: 0 is
+// __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Row epilogue helper: 32 fp32 TMEM columns * mul -> 32 bf16 stored to dst.
 __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&u)[32], float mul) {
   uint32_t pk[16];
@@ -105,6 +111,7 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
 // of each step's 128 queries into shared memory, 4-7 softmax of half 0,
 // 8-11 softmax of half 1.
 constexpr int kHalf = 64;
+constexpr int kStat = 4;   // row-term ring depth of the dK/dV pass
 
 template <int D, int NS>
 struct KVSmem {
@@ -112,9 +119,11 @@ struct KVSmem {
   uint8_t v[D / 64][kBox];
   uint8_t q[NS][D / 64][kBox];
   uint8_t dO[NS][D / 64][kBox];
-  float lse2[NS][BT];   // LSE * log2(e) of the step's queries (+inf past the block)
-  float dsum[NS][BT];   // D = dO . O
-  uint64_t kv_full, q_full[NS], q_empty[NS], stat_full[NS], s_full[2], p_full[2], acc_done, drain;
+  float lse2[kStat][BT];   // LSE * log2(e) of the step's queries (+inf past the block)
+  float dsum[kStat][BT];   // D = dO . O
+  int2 blk[kStat];         // the step's query block (first query, count | full << 16)
+  uint64_t kv_full, q_full[NS], q_empty[NS], stat_full[kStat], stat_empty[kStat], s_full[2], p_full[2], acc_done,
+      drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -146,7 +155,10 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < NS; ++s) {
       ptx::mbar_init(&S.q_full[s], 1);
       ptx::mbar_init(&S.q_empty[s], 1);
+    }
+    for (int s = 0; s < kStat; ++s) {
       ptx::mbar_init(&S.stat_full[s], 1);
+      ptx::mbar_init(&S.stat_empty[s], 2);   // one arrival per softmax warpgroup
     }
     for (int h = 0; h < 2; ++h) {
       ptx::mbar_init(&S.s_full[h], 1);
@@ -195,23 +207,54 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ row terms
-    for (int n = 0; n < n_steps; ++n) {
-      const int st = n % NS;
-      const uint32_t use = n / NS;
-      bool ok = n < NS || ptx::mbar_wait(&S.q_empty[st], (use - 1) & 1, abort_flag, kWaitLimitNs);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      const int2 blk = __ldg(&p.qb[qb_begin + n / G]);
-      const int qs = blk.x, nq = blk.y & 0xFFFF;
-      const int h = g * G + n % G;
-      const float* lse_h = p.lse + static_cast<int64_t>(h) * p.F;
-      const float* dsum_h = p.dsum + static_cast<int64_t>(h) * p.F;
-      for (int c = lane; c < BT; c += 32) {
-        const bool in = c < nq;
-        S.lse2[st][c] = in ? __ldg(lse_h + qs + c) * kLog2e : INFINITY;
-        S.dsum[st][c] = in ? __ldg(dsum_h + qs + c) : 0.f;
+    // Loads kStat steps at a time (all their global loads in flight together)
+    // and fetches the next batch's block entries ahead, so the ring stays
+    // ahead of the softmax warpgroups.
+    int2 pre[kStat];
+#pragma unroll
+    for (int x = 0; x < kStat; ++x) pre[x] = x < n_steps ? __ldg(&p.qb[qb_begin + x / G]) : make_int2(0, 0);
+    bool ok = true;
+    for (int n0 = 0; ok && n0 < n_steps; n0 += kStat) {
+      int2 cur[kStat];
+      float lv[kStat][BT / 32], dv[kStat][BT / 32];
+#pragma unroll
+      for (int x = 0; x < kStat; ++x) {
+        cur[x] = pre[x];
+        const int nn = n0 + kStat + x;
+        pre[x] = nn < n_steps ? __ldg(&p.qb[qb_begin + nn / G]) : make_int2(0, 0);
       }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&S.stat_full[st]);
+#pragma unroll
+      for (int x = 0; x < kStat; ++x) {
+        const int n = n0 + x;
+        const int h = g * G + n % G;
+        const int qs = cur[x].x, nq = cur[x].y & 0xFFFF;
+        const float* lse_h = p.lse + static_cast<int64_t>(h) * p.F + qs;
+        const float* dsum_h = p.dsum + static_cast<int64_t>(h) * p.F + qs;
+#pragma unroll
+        for (int y = 0; y < BT / 32; ++y) {
+          const int c = lane + 32 * y;
+          const bool in = n < n_steps && c < nq;
+          lv[x][y] = in ? __ldg(lse_h + c) * kLog2e : INFINITY;
+          dv[x][y] = in ? __ldg(dsum_h + c) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int x = 0; x < kStat; ++x) {
+        const int n = n0 + x;
+        if (n >= n_steps) break;
+        const int st = n % kStat;
+        const uint32_t use = n / kStat;
+        ok = n < kStat || ptx::mbar_wait(&S.stat_empty[st], (use - 1) & 1, abort_flag, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+#pragma unroll
+        for (int y = 0; y < BT / 32; ++y) {
+          S.lse2[st][lane + 32 * y] = lv[x][y];
+          S.dsum[st][lane + 32 * y] = dv[x][y];
+        }
+        if (lane == 0) S.blk[st] = cur[x];
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&S.stat_full[st]);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -293,12 +336,13 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
     for (int n = 0; n < n_steps; ++n) {
       const int st = n % NS;
-      ok = ptx::mbar_wait(&S.s_full[half], n & 1, abort_flag, kWaitLimitNs) &&
-           ptx::mbar_wait(&S.stat_full[st], (n / NS) & 1, abort_flag, kWaitLimitNs);
+      const int sst = n % kStat;
+      ok = ptx::mbar_wait(&S.stat_full[sst], (n / kStat) & 1, abort_flag, kWaitLimitNs) &&
+           ptx::mbar_wait(&S.s_full[half], n & 1, abort_flag, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      const int2 blk = __ldg(&p.qb[qb_begin + n / G]);
+      const int2 blk = S.blk[sst];
       const int qs = blk.x, nq = blk.y & 0xFFFF;
       const bool full = (blk.y >> 16) & 1;
       // visible queries of this key form one column range [lo, hi) of the half:
@@ -306,28 +350,39 @@ __global__ void __launch_bounds__(384, 1)
       const int base = qs + half * kHalf;
       const int lo = full ? 0 : max(0, j - base);
       const int hi = full ? kHalf : min(min(nq - half * kHalf, kHalf), se_j - base);
-      const float* l2s = S.lse2[st] + half * kHalf;
-      const float* dds = S.dsum[st] + half * kHalf;
+      const float* l2s = S.lse2[sst] + half * kHalf;
+      const float* dds = S.dsum[sst] + half * kHalf;
 #pragma unroll
       for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t us[32], ud[32];
         ptx::tmem_ld32(tS + c * 32, us);
         ptx::tmem_ld32(tdP + c * 32, ud);
         ptx::tmem_wait_ld();
-        uint32_t pp[16], pd[16];
+        float arg[32];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const float4 l4 = ptx::lds128(l2s + c * 32 + e);
+          arg[e] = fmaf(__uint_as_float(us[e]), sl2, -l4.x);
+          arg[e + 1] = fmaf(__uint_as_float(us[e + 1]), sl2, -l4.y);
+          arg[e + 2] = fmaf(__uint_as_float(us[e + 2]), sl2, -l4.z);
+          arg[e + 3] = fmaf(__uint_as_float(us[e + 3]), sl2, -l4.w);
+        }
+        if (!full) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = c * 32 + e;
+            arg[e] = (col >= lo && col < hi) ? arg[e] : -INFINITY;
+          }
+        }
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
           const float4 d4 = ptx::lds128(dds + c * 32 + e);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
           const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
           float pv[4], dv[4];
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
-            const int col = c * 32 + e + x;
-            float arg = fmaf(__uint_as_float(us[e + x]), sl2, -lv[x]);
-            arg = (col >= lo && col < hi) ? arg : -INFINITY;
-            pv[x] = ptx::ex2(arg);
+            pv[x] = ptx::ex2(arg[e + x]);
             dv[x] = pv[x] * (__uint_as_float(ud[e + x]) - dvv[x]);
           }
           pp[e / 2] = ptx::pack_bf16x2(pv[0], pv[1]);
@@ -341,6 +396,9 @@ __global__ void __launch_bounds__(384, 1)
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&S.p_full[half]);
+      // the row terms of this step are no longer needed by this warpgroup
+      named_bar_sync(1 + half, 128);
+      if (t == 0) ptx::mbar_arrive(&S.stat_empty[sst]);
     }
     if (ok) {
       ok = ptx::mbar_wait(&S.acc_done, 0, abort_flag, kWaitLimitNs);
@@ -375,27 +433,31 @@ __global__ void __launch_bounds__(384, 1)
 // Query-major dQ.  Each key block of the forward's list is split into two
 // 64-key halves alternating between two TMEM slots (same ping-pong as pass 2):
 //   MMA order per block i:  S/dP(i, half 0) | dQ(i-1, half 1) | S/dP(i, half 1) | dQ(i, half 0)
+// K and V stream through an NH-deep ring of 64-key half-stages (64-row TMA
+// boxes), each released as soon as its half's dQ product is issued.
 // TMEM: slot h at [128h, 128h+128): S (64 cols) then dP (64 cols); dQ at
 // [256, 256+D).  dS (bf16) overwrites the first 32 columns of S of its slot.
 // Warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 4-7 softmax of half 0,
 // 8-11 softmax of half 1 (thread t owns query row t).
-template <int D, int NS>
+constexpr int kHalfBox = kHalf * 128;   // one 64-row x 64-element swizzled box
+
+template <int D, int NH>
 struct QSmem {
   uint8_t q[D / 64][kBox];
   uint8_t dO[D / 64][kBox];
-  uint8_t k[NS][D / 64][kBox];
-  uint8_t v[NS][D / 64][kBox];
-  uint64_t q_full, kv_full[NS], kv_empty[NS], s_full[2], p_full[2], acc_done, drain;
+  uint8_t k[NH][D / 64][kHalfBox];
+  uint8_t v[NH][D / 64][kHalfBox];
+  uint64_t q_full, kv_full[NH], kv_empty[NH], s_full[2], p_full[2], acc_done, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-template <int D, int NS>
+template <int D, int NH>
 __global__ void __launch_bounds__(384, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                  const BwdParams p) {
-  using Smem = QSmem<D, NS>;
+  using Smem = QSmem<D, NH>;
   extern __shared__ uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -413,7 +475,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&S.q_full, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NH; ++s) {
       ptx::mbar_init(&S.kv_full[s], 1);
       ptx::mbar_init(&S.kv_empty[s], 1);
     }
@@ -443,20 +505,20 @@ __global__ void __launch_bounds__(384, 1)
         ptx::tma_load_3d(S.dO[c], &tm_do, &S.q_full, c * 64, h, q0);
       }
       int issued = 0;
-      for (int i = 0; i < n_blocks; ++i) {
-        const int st = i % NS;
-        const uint32_t use = i / NS;
-        const int kb0 = __ldg(&p.kb[kb_begin + i].x);
-        if (i >= NS && !ptx::mbar_wait(&S.kv_empty[st], (use - 1) & 1, abort_flag, kWaitLimitNs)) break;
-        ptx::mbar_arrive_expect_tx(&S.kv_full[st], 2 * D * 256);
+      for (int m = 0; m < 2 * n_blocks; ++m) {   // half-steps: block m/2, keys (m%2)*64..
+        const int st = m % NH;
+        const uint32_t use = m / NH;
+        const int kb0 = __ldg(&p.kb[kb_begin + m / 2].x) + (m & 1) * kHalf;
+        if (m >= NH && !ptx::mbar_wait(&S.kv_empty[st], (use - 1) & 1, abort_flag, kWaitLimitNs)) break;
+        ptx::mbar_arrive_expect_tx(&S.kv_full[st], 2 * D * 128);
         for (int c = 0; c < D / 64; ++c) {
           ptx::tma_load_3d(S.k[st][c], &tm_k, &S.kv_full[st], c * 64, kvh, kb0);
           ptx::tma_load_3d(S.v[st][c], &tm_v, &S.kv_full[st], c * 64, kvh, kb0);
         }
-        issued = i + 1;
+        issued = m + 1;
       }
       if (*abort_flag) {
-        for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i) ptx::mbar_drain(&S.kv_full[i % NS], (i / NS) & 1);
+        for (int m = (issued > NH ? issued - NH : 0); m < issued; ++m) ptx::mbar_drain(&S.kv_full[m % NH], (m / NH) & 1);
         ptx::mbar_drain(&S.q_full, 0);
       }
     }
@@ -468,54 +530,62 @@ __global__ void __launch_bounds__(384, 1)
       ptx::tc_fence_after();
       const uint32_t q_base = ptx::smem_addr(S.q[0]);
       const uint32_t do_base = ptx::smem_addr(S.dO[0]);
-      auto issue_sdp = [&](int st, int half) {
-        const uint32_t kb = ptx::smem_addr(S.k[st][0]) + half * (kHalf * 128);
-        const uint32_t vb = ptx::smem_addr(S.v[st][0]) + half * (kHalf * 128);
-        const uint32_t cS = BT * half, cdP = BT * half + kHalf;
+      // S, dP of one 64-key half-stage (K-major B operands, 64 rows)
+      auto issue_sdp = [&](int m, int slot) {
+        const uint32_t kb = ptx::smem_addr(S.k[m % NH][0]);
+        const uint32_t vb = ptx::smem_addr(S.v[m % NH][0]);
+        const uint32_t cS = BT * slot, cdP = BT * slot + kHalf;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cS, ptx::sw128_desc(q_base + koff, 16, 1024), ptx::sw128_desc(kb + koff, 16, 1024),
+          const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
+          const uint32_t boff = (kk >> 2) * kHalfBox + (kk & 3) * 32;
+          ptx::mma_ss(tmem + cS, ptx::sw128_desc(q_base + aoff, 16, 1024), ptx::sw128_desc(kb + boff, 16, 1024),
                       idesc_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cdP, ptx::sw128_desc(do_base + koff, 16, 1024), ptx::sw128_desc(vb + koff, 16, 1024),
+          const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
+          const uint32_t boff = (kk >> 2) * kHalfBox + (kk & 3) * 32;
+          ptx::mma_ss(tmem + cdP, ptx::sw128_desc(do_base + aoff, 16, 1024), ptx::sw128_desc(vb + boff, 16, 1024),
                       idesc_s, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(&S.s_full[half]);
+        ptx::mma_commit(&S.s_full[slot]);
       };
-      // dQ += dS_half K_half (K block rows half*64.. as the MN-major B operand)
-      auto issue_dq = [&](int st, int half, bool first) {
-        const uint32_t kb = ptx::smem_addr(S.k[st][0]) + half * (kHalf * 128);
-        const uint32_t cS = BT * half;
+      // dQ += dS K_half (half-stage as the MN-major B operand: d-column groups
+      // one 64-row box apart, 16 keys = 2 KB per step); then release the stage
+      auto issue_dq = [&](int m, int slot, bool first) {
+        const uint32_t kb = ptx::smem_addr(S.k[m % NH][0]);
+        const uint32_t cS = BT * slot;
 #pragma unroll
         for (int kk = 0; kk < kHalf / 16; ++kk)
-          ptx::mma_ts(tmem + cdQ, tmem + cS + kk * 8, ptx::sw128_desc(kb + kk * 2048, kBox, 1024), idesc_dq,
+          ptx::mma_ts(tmem + cdQ, tmem + cS + kk * 8, ptx::sw128_desc(kb + kk * 2048, kHalfBox, 1024), idesc_dq,
                       (first && kk == 0) ? 0u : 1u);
+        ptx::mma_commit(&S.kv_empty[m % NH]);
+      };
+      auto wait_stage = [&](int m) {
+        const bool r = ptx::mbar_wait(&S.kv_full[m % NH], (m / NH) & 1, abort_flag, kWaitLimitNs);
+        ptx::tc_fence_after();
+        return r;
       };
       for (int i = 0; ok && i < n_blocks; ++i) {
-        const int st = i % NS;
-        if (!ptx::mbar_wait(&S.kv_full[st], (i / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-        ptx::tc_fence_after();
-        issue_sdp(st, 0);
+        if (!wait_stage(2 * i)) { ok = false; break; }
+        issue_sdp(2 * i, 0);
         if (i > 0) {
           if (!ptx::mbar_wait(&S.p_full[1], (i - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
           ptx::tc_fence_after();
-          issue_dq((i - 1) % NS, 1, false);
-          ptx::mma_commit(&S.kv_empty[(i - 1) % NS]);
+          issue_dq(2 * i - 1, 1, false);
         }
-        issue_sdp(st, 1);
+        if (!wait_stage(2 * i + 1)) { ok = false; break; }
+        issue_sdp(2 * i + 1, 1);
         if (!ptx::mbar_wait(&S.p_full[0], i & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
         ptx::tc_fence_after();
-        issue_dq(st, 0, i == 0);
+        issue_dq(2 * i, 0, i == 0);
       }
       if (ok && n_blocks > 0) {
         const int last = n_blocks - 1;
         if (ptx::mbar_wait(&S.p_full[1], last & 1, abort_flag, kWaitLimitNs)) {
           ptx::tc_fence_after();
-          issue_dq(last % NS, 1, false);
+          issue_dq(2 * last + 1, 1, false);
           ptx::mma_commit(&S.acc_done);
         }
       }
@@ -534,12 +604,14 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tmem + lane_off + BT * half, tdP = tS + kHalf;
     const float sl2 = p.scale_log2;
     bool ok = true;
+    int2 next = n_blocks > 0 ? __ldg(&p.kb[kb_begin]) : make_int2(0, 0);
     for (int b = 0; b < n_blocks; ++b) {
+      const int2 blk = next;   // fetched one block ahead
+      if (b + 1 < n_blocks) next = __ldg(&p.kb[kb_begin + b + 1]);
       ok = ptx::mbar_wait(&S.s_full[half], b & 1, abort_flag, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      const int2 blk = __ldg(&p.kb[kb_begin + b]);
       const int kb0 = blk.x, nkb = blk.y & 0xFFFF;
       const bool full = (blk.y >> 16) & 1;
       const int base = kb0 + half * kHalf;     // first key of this half
@@ -627,17 +699,17 @@ int launch_kv(const BwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk
   return cuda_status(cudaGetLastError());
 }
 
-template <int D, int NS>
+template <int D, int NH>
 int launch_q(const BwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
              const CUtensorMap& tdo, int64_t n_qtiles, cudaStream_t stream) {
-  constexpr size_t smem = sizeof(QSmem<D, NS>) + 1024;
+  constexpr size_t smem = sizeof(QSmem<D, NH>) + 1024;
   static_assert(smem <= 227 * 1024, "shared memory");
   static bool cfg = false;
-  int st = set_smem(bwd_q_kernel<D, NS>, smem, cfg);
+  int st = set_smem(bwd_q_kernel<D, NH>, smem, cfg);
   if (st != TPK_OK) return st;
   const int64_t items = n_qtiles * prm.Hq;
   if (items > 0x7fffffff) return TPK_E_OVERFLOW;
-  if (items > 0) bwd_q_kernel<D, NS><<<static_cast<unsigned>(items), 384, smem, stream>>>(tq, tk, tv, tdo, prm);
+  if (items > 0) bwd_q_kernel<D, NH><<<static_cast<unsigned>(items), 384, smem, stream>>>(tq, tk, tv, tdo, prm);
   return cuda_status(cudaGetLastError());
 }
 
@@ -717,7 +789,11 @@ extern "C" int tpk_tree_attn_bwd_phase(int32_t phase, const tpk_plan* plan, cons
   const int64_t nkt = static_cast<int64_t>(P.kt_k0.size()), nqt = static_cast<int64_t>(P.qt_q0.size());
   if (phase == TPK_BWD_DKDV)
     return d == 128 ? launch_kv<128, 2>(prm, tq, tk, tv, tdo, nkt, s) : launch_kv<64, 4>(prm, tq, tk, tv, tdo, nkt, s);
-  return d == 128 ? launch_q<128, 2>(prm, tq, tk, tv, tdo, nqt, s) : launch_q<64, 4>(prm, tq, tk, tv, tdo, nqt, s);
+  // the dQ pass streams K and V in 64-key half-stages
+  CUtensorMap tk64, tv64;
+  if ((st = make_map_bf16(&tk64, k, P.F, Hkv, d, 64)) != TPK_OK) return st;
+  if ((st = make_map_bf16(&tv64, v, P.F, Hkv, d, 64)) != TPK_OK) return st;
+  return d == 128 ? launch_q<128, 4>(prm, tq, tk64, tv64, tdo, nqt, s) : launch_q<64, 8>(prm, tq, tk64, tv64, tdo, nqt, s);
 }
 
 extern "C" int tpk_tree_attn_bwd(const tpk_plan* plan, const void* dev_image, const void* q, const void* k,
