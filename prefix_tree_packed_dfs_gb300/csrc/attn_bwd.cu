@@ -112,28 +112,29 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
 // 8-11 softmax of half 1.
 constexpr int kHalf = 64;
 constexpr int kStat = 4;   // row-term ring depth of the dK/dV pass
+constexpr int kHalfBox = kHalf * 128;   // one 64-row x 64-element swizzled box
 
-template <int D, int NS>
+template <int D, int NH>
 struct KVSmem {
   uint8_t k[D / 64][kBox];
   uint8_t v[D / 64][kBox];
-  uint8_t q[NS][D / 64][kBox];
-  uint8_t dO[NS][D / 64][kBox];
+  uint8_t q[NH][D / 64][kHalfBox];
+  uint8_t dO[NH][D / 64][kHalfBox];
   float lse2[kStat][BT];   // LSE * log2(e) of the step's queries (+inf past the block)
   float dsum[kStat][BT];   // D = dO . O
   int2 blk[kStat];         // the step's query block (first query, count | full << 16)
-  uint64_t kv_full, q_full[NS], q_empty[NS], stat_full[kStat], stat_empty[kStat], s_full[2], p_full[2], acc_done,
+  uint64_t kv_full, q_full[NH], q_empty[NH], stat_full[kStat], stat_empty[kStat], s_full[2], p_full[2], acc_done,
       drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-template <int D, int NS>
+template <int D, int NH>
 __global__ void __launch_bounds__(384, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
-  using Smem = KVSmem<D, NS>;
+  using Smem = KVSmem<D, NH>;
   extern __shared__ uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&S.kv_full, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NH; ++s) {
       ptx::mbar_init(&S.q_full[s], 1);
       ptx::mbar_init(&S.q_empty[s], 1);
     }
@@ -187,21 +188,22 @@ __global__ void __launch_bounds__(384, 1)
         ptx::tma_load_3d(S.v[c], &tm_v, &S.kv_full, c * 64, g, k0);
       }
       int issued = 0;
-      for (int n = 0; n < n_steps; ++n) {
-        const int st = n % NS;
-        const uint32_t use = n / NS;
-        const int qs = __ldg(&p.qb[qb_begin + n / G].x);
+      for (int m = 0; m < 2 * n_steps; ++m) {   // half-steps: step m/2, queries (m%2)*64..
+        const int n = m >> 1;
+        const int st = m % NH;
+        const uint32_t use = m / NH;
+        const int qs = __ldg(&p.qb[qb_begin + n / G].x) + (m & 1) * kHalf;
         const int h = g * G + n % G;
-        if (n >= NS && !ptx::mbar_wait(&S.q_empty[st], (use - 1) & 1, abort_flag, kWaitLimitNs)) break;
-        ptx::mbar_arrive_expect_tx(&S.q_full[st], 2 * D * 256);
+        if (m >= NH && !ptx::mbar_wait(&S.q_empty[st], (use - 1) & 1, abort_flag, kWaitLimitNs)) break;
+        ptx::mbar_arrive_expect_tx(&S.q_full[st], 2 * D * 128);
         for (int c = 0; c < D / 64; ++c) {
           ptx::tma_load_3d(S.q[st][c], &tm_q, &S.q_full[st], c * 64, h, qs);
           ptx::tma_load_3d(S.dO[st][c], &tm_do, &S.q_full[st], c * 64, h, qs);
         }
-        issued = n + 1;
+        issued = m + 1;
       }
       if (*abort_flag) {
-        for (int n = (issued > NS ? issued - NS : 0); n < issued; ++n) ptx::mbar_drain(&S.q_full[n % NS], (n / NS) & 1);
+        for (int m = (issued > NH ? issued - NH : 0); m < issued; ++m) ptx::mbar_drain(&S.q_full[m % NH], (m / NH) & 1);
         ptx::mbar_drain(&S.kv_full, 0);
       }
     }
@@ -265,58 +267,66 @@ __global__ void __launch_bounds__(384, 1)
       ptx::tc_fence_after();
       const uint32_t k_base = ptx::smem_addr(S.k[0]);
       const uint32_t v_base = ptx::smem_addr(S.v[0]);
-      // S^T, dP^T of one 64-query half (rows half*64.. of the Q / dO stage)
-      auto issue_sdp = [&](int st, int half) {
-        const uint32_t qb = ptx::smem_addr(S.q[st][0]) + half * (kHalf * 128);
-        const uint32_t ob = ptx::smem_addr(S.dO[st][0]) + half * (kHalf * 128);
-        const uint32_t cS = BT * half, cdP = BT * half + kHalf;
+      // S^T, dP^T of one 64-query half-stage (K-major B operands, 64 rows)
+      auto issue_sdp = [&](int m, int slot) {
+        const uint32_t qb = ptx::smem_addr(S.q[m % NH][0]);
+        const uint32_t ob = ptx::smem_addr(S.dO[m % NH][0]);
+        const uint32_t cS = BT * slot, cdP = BT * slot + kHalf;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cS, ptx::sw128_desc(k_base + koff, 16, 1024), ptx::sw128_desc(qb + koff, 16, 1024),
+          const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
+          const uint32_t boff = (kk >> 2) * kHalfBox + (kk & 3) * 32;
+          ptx::mma_ss(tmem + cS, ptx::sw128_desc(k_base + aoff, 16, 1024), ptx::sw128_desc(qb + boff, 16, 1024),
                       idesc_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cdP, ptx::sw128_desc(v_base + koff, 16, 1024), ptx::sw128_desc(ob + koff, 16, 1024),
+          const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
+          const uint32_t boff = (kk >> 2) * kHalfBox + (kk & 3) * 32;
+          ptx::mma_ss(tmem + cdP, ptx::sw128_desc(v_base + aoff, 16, 1024), ptx::sw128_desc(ob + boff, 16, 1024),
                       idesc_s, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(&S.s_full[half]);
+        ptx::mma_commit(&S.s_full[slot]);
       };
-      // dV += P^T dO_half, dK += dS^T Q_half (B operands MN-major: N = head dim)
-      auto issue_acc = [&](int st, int half, bool first) {
-        const uint32_t qb = ptx::smem_addr(S.q[st][0]) + half * (kHalf * 128);
-        const uint32_t ob = ptx::smem_addr(S.dO[st][0]) + half * (kHalf * 128);
-        const uint32_t cS = BT * half, cdP = BT * half + kHalf;
+      // dV += P^T dO_half, dK += dS^T Q_half (half-stages as MN-major B
+      // operands: d-column groups one 64-row box apart), then release the stage
+      auto issue_acc = [&](int m, int slot, bool first) {
+        const uint32_t qb = ptx::smem_addr(S.q[m % NH][0]);
+        const uint32_t ob = ptx::smem_addr(S.dO[m % NH][0]);
+        const uint32_t cS = BT * slot, cdP = BT * slot + kHalf;
 #pragma unroll
         for (int kk = 0; kk < kHalf / 16; ++kk) {
           const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-          ptx::mma_ts(tmem + cdV, tmem + cS + kk * 8, ptx::sw128_desc(ob + kk * 2048, kBox, 1024), idesc_acc, acc);
-          ptx::mma_ts(tmem + cdK, tmem + cdP + kk * 8, ptx::sw128_desc(qb + kk * 2048, kBox, 1024), idesc_acc, acc);
+          ptx::mma_ts(tmem + cdV, tmem + cS + kk * 8, ptx::sw128_desc(ob + kk * 2048, kHalfBox, 1024), idesc_acc, acc);
+          ptx::mma_ts(tmem + cdK, tmem + cdP + kk * 8, ptx::sw128_desc(qb + kk * 2048, kHalfBox, 1024), idesc_acc,
+                      acc);
         }
+        ptx::mma_commit(&S.q_empty[m % NH]);
+      };
+      auto wait_stage = [&](int m) {
+        const bool r = ptx::mbar_wait(&S.q_full[m % NH], (m / NH) & 1, abort_flag, kWaitLimitNs);
+        ptx::tc_fence_after();
+        return r;
       };
       for (int n = 0; ok && n < n_steps; ++n) {
-        const int st = n % NS;
-        if (!ptx::mbar_wait(&S.q_full[st], (n / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-        ptx::tc_fence_after();
-        issue_sdp(st, 0);
+        if (!wait_stage(2 * n)) { ok = false; break; }
+        issue_sdp(2 * n, 0);
         if (n > 0) {
           if (!ptx::mbar_wait(&S.p_full[1], (n - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
           ptx::tc_fence_after();
-          issue_acc((n - 1) % NS, 1, false);
-          ptx::mma_commit(&S.q_empty[(n - 1) % NS]);
+          issue_acc(2 * n - 1, 1, false);
         }
-        issue_sdp(st, 1);
+        if (!wait_stage(2 * n + 1)) { ok = false; break; }
+        issue_sdp(2 * n + 1, 1);
         if (!ptx::mbar_wait(&S.p_full[0], n & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
         ptx::tc_fence_after();
-        issue_acc(st, 0, n == 0);
+        issue_acc(2 * n, 0, n == 0);
       }
       if (ok && n_steps > 0) {
         const int last = n_steps - 1;
         if (ptx::mbar_wait(&S.p_full[1], last & 1, abort_flag, kWaitLimitNs)) {
           ptx::tc_fence_after();
-          issue_acc(last % NS, 1, false);
+          issue_acc(2 * last + 1, 1, false);
           ptx::mma_commit(&S.acc_done);
         }
       }
@@ -335,7 +345,6 @@ __global__ void __launch_bounds__(384, 1)
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int n = 0; n < n_steps; ++n) {
-      const int st = n % NS;
       const int sst = n % kStat;
       ok = ptx::mbar_wait(&S.stat_full[sst], (n / kStat) & 1, abort_flag, kWaitLimitNs) &&
            ptx::mbar_wait(&S.s_full[half], n & 1, abort_flag, kWaitLimitNs);
@@ -439,8 +448,6 @@ __global__ void __launch_bounds__(384, 1)
 // [256, 256+D).  dS (bf16) overwrites the first 32 columns of S of its slot.
 // Warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 4-7 softmax of half 0,
 // 8-11 softmax of half 1 (thread t owns query row t).
-constexpr int kHalfBox = kHalf * 128;   // one 64-row x 64-element swizzled box
-
 template <int D, int NH>
 struct QSmem {
   uint8_t q[D / 64][kBox];
@@ -685,17 +692,17 @@ int set_smem(Kern kern, size_t bytes, bool& done) {
   return TPK_OK;
 }
 
-template <int D, int NS>
+template <int D, int NH>
 int launch_kv(const BwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
               const CUtensorMap& tdo, int64_t n_ktiles, cudaStream_t stream) {
-  constexpr size_t smem = sizeof(KVSmem<D, NS>) + 1024;
+  constexpr size_t smem = sizeof(KVSmem<D, NH>) + 1024;
   static_assert(smem <= 227 * 1024, "shared memory");
   static bool cfg = false;
-  int st = set_smem(bwd_kv_kernel<D, NS>, smem, cfg);
+  int st = set_smem(bwd_kv_kernel<D, NH>, smem, cfg);
   if (st != TPK_OK) return st;
   const int64_t items = n_ktiles * prm.Hkv;
   if (items > 0x7fffffff) return TPK_E_OVERFLOW;
-  if (items > 0) bwd_kv_kernel<D, NS><<<static_cast<unsigned>(items), 384, smem, stream>>>(tq, tk, tv, tdo, prm);
+  if (items > 0) bwd_kv_kernel<D, NH><<<static_cast<unsigned>(items), 384, smem, stream>>>(tq, tk, tv, tdo, prm);
   return cuda_status(cudaGetLastError());
 }
 
@@ -787,8 +794,14 @@ extern "C" int tpk_tree_attn_bwd_phase(int32_t phase, const tpk_plan* plan, cons
   prm.scale_log2 = scale * kLog2e;
   prm.err = dev_err;
   const int64_t nkt = static_cast<int64_t>(P.kt_k0.size()), nqt = static_cast<int64_t>(P.qt_q0.size());
-  if (phase == TPK_BWD_DKDV)
-    return d == 128 ? launch_kv<128, 2>(prm, tq, tk, tv, tdo, nkt, s) : launch_kv<64, 4>(prm, tq, tk, tv, tdo, nkt, s);
+  if (phase == TPK_BWD_DKDV) {
+    // the dK/dV pass streams Q and dO in 64-query half-stages
+    CUtensorMap tq64, tdo64;
+    if ((st = make_map_bf16(&tq64, q, P.F, Hq, d, 64)) != TPK_OK) return st;
+    if ((st = make_map_bf16(&tdo64, dout, P.F, Hq, d, 64)) != TPK_OK) return st;
+    return d == 128 ? launch_kv<128, 4>(prm, tq64, tk, tv, tdo64, nkt, s)
+                    : launch_kv<64, 8>(prm, tq64, tk, tv, tdo64, nkt, s);
+  }
   // the dQ pass streams K and V in 64-key half-stages
   CUtensorMap tk64, tv64;
   if ((st = make_map_bf16(&tk64, k, P.F, Hkv, d, 64)) != TPK_OK) return st;
