@@ -52,6 +52,9 @@ def _args():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="packing-ratio sweep (32,768-token rows): forward time against forwarded and raw "
+                         "tokens, tree layout vs sequence packing of the same raw tokens; one line per point")
     return ap.parse_args()
 
 
@@ -409,9 +412,72 @@ def run_ours(a):
         torch.distributed.destroy_process_group()
 
 
+def run_sweep(a):
+    """Forward attention over one 32,768-forwarded-token row at packing ratios
+    1.00 .. 3.56, and over the same raw tokens laid out without sharing
+    (sequence packing: min shared length above every run).  L2 is flushed
+    (a 256 MiB write) before every timed launch; CUDA events bracket the
+    attention kernel alone on the current stream."""
+    import torch
+    import workloads
+    from prefix_tree_packed_dfs_gb300 import ops
+    from workloads import rng as wrng
+    peaks = _peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def time_fwd(name):
+        w = workloads.get(name)
+        plan = ops.Plan.from_sequences(w.sequences, group_ids=w.group_ids, row_capacity=w.row_capacity,
+                                       min_shared=w.min_shared)
+        dp = plan.to_device()
+        info = plan.info
+        F, Hq, Hkv, d = info["n_fwd"], w.n_heads_q, w.n_heads_kv, w.head_dim
+        q = wrng.normal_bf16(w.seeds["q"], (F, Hq, d), "cuda")
+        k = wrng.normal_bf16(w.seeds["k"], (F, Hkv, d), "cuda")
+        v = wrng.normal_bf16(w.seeds["v"], (F, Hkv, d), "cuda")
+        ops.rope_by_depth(q, k, dp.depth, w.rope_base)
+        o = torch.empty_like(q)
+        lse = torch.empty((Hq, F), dtype=torch.float32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for _ in range(a.warmup):
+            ops.tree_attn_fwd(dp, q, k, v, out=o, lse=lse, dev_err=err)
+        times = []
+        for _ in range(max(a.steps, 3)):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            ops.tree_attn_fwd(dp, q, k, v, out=o, lse=lse, dev_err=err)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        if int(err.item()) != 0:
+            raise SystemExit("device wait timed out (TPK_E_TIMEOUT)")
+        ms = statistics.median(times)
+        flops = 4.0 * d * Hq * info["useful_pairs"]
+        return {"raw_tokens": info["n_raw"], "forwarded_tokens": F, "rows": info["n_rows"],
+                "useful_pairs": info["useful_pairs"], "visited_pairs": info["visited_pairs"], "ms": ms,
+                "useful_tflops": flops / ms / 1e9, "raw_tokens_per_s": info["n_raw"] / ms * 1e3,
+                "forwarded_tokens_per_s": F / ms * 1e3}
+
+    for rho in workloads.SWEEP_RHOS:
+        tree = time_fwd("sweep_%.2f" % rho)
+        seq = time_fwd("sweep_%.2f_seqpack" % rho)
+        tree["pct_of_peak"] = 100.0 * tree["useful_tflops"] / peaks["bf16_tflops"]
+        print(json.dumps({
+            "mode": "sweep", "metric": METRIC, "packing_ratio": tree["raw_tokens"] / tree["forwarded_tokens"],
+            "tree": tree, "sequence_packing": seq, "speedup_vs_sequence_packing": seq["ms"] / tree["ms"],
+            "peak_tflops": peaks["bf16_tflops"], "peak_kind": "burst bf16 (%s): kernel timed alone" % peaks["source"],
+            "config": {"workload": "one row of 32768 forwarded tokens from 4 rollouts sharing a prefix; Hq 16 / Hkv 8 "
+                                   "/ d 128; sequence packing = the same raw tokens with no sharing, rows of 32768",
+                       "l2": "flushed (256 MiB write) before every timed launch"},
+        }), flush=True)
+
+
 def main():
     a = _args()
-    if a.impl == "reference":
+    if a.sweep:
+        run_sweep(a)
+    elif a.impl == "reference":
         run_reference(a)
     else:
         run_ours(a)

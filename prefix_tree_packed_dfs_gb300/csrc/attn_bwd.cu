@@ -276,14 +276,14 @@ __global__ void __launch_bounds__(384, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
           const uint32_t boff = (kk >> 2) * kHalfBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cS, ptx::sw128_desc(k_base + aoff, 16, 1024), ptx::sw128_desc(qb + boff, 16, 1024),
+          ptx::mma_ss(tmem + cS, ptx::desc_add(ptx::sw128_desc(k_base, 16, 1024), aoff), ptx::desc_add(ptx::sw128_desc(qb, 16, 1024), boff),
                       idesc_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
           const uint32_t boff = (kk >> 2) * kHalfBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cdP, ptx::sw128_desc(v_base + aoff, 16, 1024), ptx::sw128_desc(ob + boff, 16, 1024),
+          ptx::mma_ss(tmem + cdP, ptx::desc_add(ptx::sw128_desc(v_base, 16, 1024), aoff), ptx::desc_add(ptx::sw128_desc(ob, 16, 1024), boff),
                       idesc_s, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(&S.s_full[slot]);
@@ -297,8 +297,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int kk = 0; kk < kHalf / 16; ++kk) {
           const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-          ptx::mma_ts(tmem + cdV, tmem + cS + kk * 8, ptx::sw128_desc(ob + kk * 2048, kHalfBox, 1024), idesc_acc, acc);
-          ptx::mma_ts(tmem + cdK, tmem + cdP + kk * 8, ptx::sw128_desc(qb + kk * 2048, kHalfBox, 1024), idesc_acc,
+          ptx::mma_ts(tmem + cdV, tmem + cS + kk * 8, ptx::desc_add(ptx::sw128_desc(ob, kHalfBox, 1024), kk * 2048), idesc_acc, acc);
+          ptx::mma_ts(tmem + cdK, tmem + cdP + kk * 8, ptx::desc_add(ptx::sw128_desc(qb, kHalfBox, 1024), kk * 2048), idesc_acc,
                       acc);
         }
         ptx::mma_commit(&S.q_empty[m % NH]);
@@ -546,14 +546,14 @@ __global__ void __launch_bounds__(384, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
           const uint32_t boff = (kk >> 2) * kHalfBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cS, ptx::sw128_desc(q_base + aoff, 16, 1024), ptx::sw128_desc(kb + boff, 16, 1024),
+          ptx::mma_ss(tmem + cS, ptx::desc_add(ptx::sw128_desc(q_base, 16, 1024), aoff), ptx::desc_add(ptx::sw128_desc(kb, 16, 1024), boff),
                       idesc_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
           const uint32_t boff = (kk >> 2) * kHalfBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cdP, ptx::sw128_desc(do_base + aoff, 16, 1024), ptx::sw128_desc(vb + boff, 16, 1024),
+          ptx::mma_ss(tmem + cdP, ptx::desc_add(ptx::sw128_desc(do_base, 16, 1024), aoff), ptx::desc_add(ptx::sw128_desc(vb, 16, 1024), boff),
                       idesc_s, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(&S.s_full[slot]);
@@ -565,7 +565,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t cS = BT * slot;
 #pragma unroll
         for (int kk = 0; kk < kHalf / 16; ++kk)
-          ptx::mma_ts(tmem + cdQ, tmem + cS + kk * 8, ptx::sw128_desc(kb + kk * 2048, kHalfBox, 1024), idesc_dq,
+          ptx::mma_ts(tmem + cdQ, tmem + cS + kk * 8, ptx::desc_add(ptx::sw128_desc(kb, kHalfBox, 1024), kk * 2048), idesc_dq,
                       (first && kk == 0) ? 0u : 1u);
         ptx::mma_commit(&S.kv_empty[m % NH]);
       };

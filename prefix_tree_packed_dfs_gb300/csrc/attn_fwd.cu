@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
         for (int kk = 0; kk < BN / 16; ++kk) {
           // V block as the MN-major B operand: N = head dim (64-wide column
           // groups one box apart), K = 16 keys = 2 KB further per step
-          const uint64_t bdesc = ptx::sw128_desc(v_base + kk * 2048, kBox, 1024);
+          const uint64_t bdesc = ptx::desc_add(ptx::sw128_desc(v_base, kBox, 1024), kk * 2048);
           ptx::mma_ts(o_col, p_col + kk * 8, bdesc, idesc_pv, (blk > 0 || kk > 0) ? 1u : 0u);
         }
       };
@@ -199,8 +199,8 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
             // Q and K as K-major operands: 16 elements = 32 bytes per step
             // inside a 64-element box, next box after 4 steps
             const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
-            const uint64_t adesc = ptx::sw128_desc(q_base[s] + koff, 16, 1024);
-            const uint64_t bdesc = ptx::sw128_desc(k_base + koff, 16, 1024);
+            const uint64_t adesc = ptx::desc_add(ptx::sw128_desc(q_base[s], 16, 1024), koff);
+            const uint64_t bdesc = ptx::desc_add(ptx::sw128_desc(k_base, 16, 1024), koff);
             ptx::mma_ss(s_col, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit(&S.s_full[s]);

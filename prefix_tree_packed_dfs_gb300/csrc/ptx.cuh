@@ -131,6 +131,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_byte
   return d;
 }
 
+// Descriptor of the same matrix `bytes` further on (bytes a multiple of 16;
+// the start-address field cannot carry out for addresses inside the 228 KB
+// shared window).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Instruction descriptor for kind::f16 with bf16 inputs and fp32 accumulate.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
 //   bit 15 A major (0 = K-major, 1 = MN-major), bit 16 B major,
