@@ -270,6 +270,15 @@ int tpk_scatter_token_index(const int32_t* token_index, int64_t R, int64_t F,
                             const void* src, void* dst, const float* lse_src,
                             float* lse_dst, int32_t H, int32_t d, void* stream);
 
+/* Self-test of the device-side failure path (no counterpart on the pages):
+ * launches one small kernel that waits, with the same bounded mbarrier wait
+ * the attention kernels use, on a barrier nothing ever arrives at.  After
+ * limit_ns nanoseconds (1 .. 2e9) the wait gives up, TPK_E_TIMEOUT is written
+ * to *dev_err (device int32) and the kernel exits; the context stays usable.
+ * Used by the tests to check timeout reporting without faulting or hanging
+ * the GPU. */
+int tpk_selftest_wait_timeout(uint64_t limit_ns, int32_t* dev_err, void* stream);
+
 const char* tpk_status_string(int status);
 
 /* Library version string. */

@@ -25,7 +25,7 @@ EXPORTS = [
     "tpk_plan_build", "tpk_plan_info_get", "tpk_plan_export", "tpk_plan_worklists",
     "tpk_plan_device_bytes", "tpk_plan_field_offset", "tpk_plan_upload", "tpk_plan_destroy",
     "tpk_rope_by_depth", "tpk_attn_workspace_bytes", "tpk_tree_attn_fwd", "tpk_tree_attn_bwd",
-    "tpk_tree_attn_bwd_phase", "tpk_tree_attn_bwd_noalloc",
+    "tpk_tree_attn_bwd_phase", "tpk_tree_attn_bwd_noalloc", "tpk_selftest_wait_timeout",
     "tpk_scatter_token_index", "tpk_status_string", "tpk_version",
 ]
 
@@ -75,6 +75,7 @@ def _sig(lib):
     lib.tpk_tree_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, ctypes.c_float, P, SZ, P, P]
     lib.tpk_tree_attn_bwd_phase.argtypes = [I32] + lib.tpk_tree_attn_bwd.argtypes
     lib.tpk_tree_attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, ctypes.c_float, P, P]
+    lib.tpk_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P, P]
     lib.tpk_scatter_token_index.argtypes = [P, I64, I64, P, P, P, P, I32, I32, P]
     lib.tpk_status_string.argtypes = [ctypes.c_int]
     lib.tpk_status_string.restype = ctypes.c_char_p
