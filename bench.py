@@ -126,6 +126,29 @@ def _dist():
     return world, rank, local
 
 
+def rank_seeds(w, rank):
+    """Seeds of this rank's batch.  Weak scaling: every rank owns one batch of
+    the same shape (rows are independent, nothing crosses ranks on the data
+    path), drawn with seeds shifted by 1000 per rank."""
+    return {k: v + 1000 * rank for k, v in w.seeds.items()}
+
+
+def max_over_ranks(x, device, world):
+    """The slowest rank's value (step time): the only cross-rank reduction."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, raw_tokens_per_rank, seconds):
+    """Whole-job raw tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * raw_tokens_per_rank / seconds
+
+
 def _cpu_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -226,7 +249,6 @@ def run_ours(a):
     w = workloads.get(a.workload)
     # weak scaling: every rank owns one batch of the same shape (rows are
     # independent; no data crosses ranks)
-    seed_shift = 1000 * rank
     t0 = time.perf_counter()
     plan = ops.Plan.from_sequences(w.sequences, group_ids=w.group_ids, row_capacity=w.row_capacity,
                                    min_shared=w.min_shared)
@@ -236,7 +258,7 @@ def run_ours(a):
     pairs = info["useful_pairs"]
     dp = plan.to_device()
     dev = torch.device("cuda", local)
-    s = {k: v + seed_shift for k, v in w.seeds.items()}
+    s = rank_seeds(w, rank)
     Q = wrng.normal_bf16(s["q"], (F, Hq, d), dev)
     K = wrng.normal_bf16(s["k"], (F, Hkv, d), dev)
     V = wrng.normal_bf16(s["v"], (F, Hkv, d), dev)
@@ -294,10 +316,7 @@ def run_ours(a):
     ms = start.elapsed_time(stop) / a.steps
     per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(a.steps))
            for j, n in enumerate(names)}
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev, world)
     if int(err.item()) != 0:
         raise SystemExit("device wait timed out (TPK_E_TIMEOUT)")
 
@@ -331,11 +350,8 @@ def run_ours(a):
             keep = e2e_step()
         dt = (time.perf_counter() - t0) / a.e2e_steps
         del keep
-        if world > 1:
-            t = torch.tensor([dt], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            dt = float(t.item())
-        e2e = {"value": world * R / dt, "unit": "raw tokens/s", "h2d_bytes_per_step": int(h2d),
+        dt = max_over_ranks(dt, dev, world)
+        e2e = {"value": job_value(world, R, dt), "unit": "raw tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": 1e3 * dt,
                "includes": "plan build on host, plan image + Q/K/V/dO host->device, full step, "
                            "raw-order LSE device->host"}
@@ -384,7 +400,7 @@ def run_ours(a):
 
     useful_tflops = (fwd_flop + bwd_flop) / (ms / 1e3) / 1e12
     out = {
-        "metric": METRIC, "value": world * R / (ms / 1e3), "unit": "raw tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": job_value(world, R, ms / 1e3), "unit": "raw tokens/s", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC, "raw_tokens": R, "forwarded_tokens": F, "rows": info["n_rows"],
