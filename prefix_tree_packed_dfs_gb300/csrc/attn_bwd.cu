@@ -120,8 +120,8 @@ struct KVSmem {
   uint8_t v[D / 64][kBox];
   uint8_t q[NH][D / 64][kHalfBox];
   uint8_t dO[NH][D / 64][kHalfBox];
-  float lse2[kStat][BT];   // LSE * log2(e) of the step's queries (+inf past the block)
-  float dsum[kStat][BT];   // D = dO . O
+  float lse2[kStat][BT];   // -LSE * log2(e) of the step's queries (-inf past the block)
+  float dsum[kStat][BT];   // -D = -(dO . O)
   int2 blk[kStat];         // the step's query block (first query, count | full << 16)
   uint64_t kv_full, q_full[NH], q_empty[NH], stat_full[kStat], stat_empty[kStat], s_full[2], p_full[2], acc_done,
       drain;
@@ -236,8 +236,8 @@ __global__ void __launch_bounds__(384, 1)
         for (int y = 0; y < BT / 32; ++y) {
           const int c = lane + 32 * y;
           const bool in = n < n_steps && c < nq;
-          lv[x][y] = in ? __ldg(lse_h + c) * kLog2e : INFINITY;
-          dv[x][y] = in ? __ldg(dsum_h + c) : 0.f;
+          lv[x][y] = in ? -__ldg(lse_h + c) * kLog2e : -INFINITY;
+          dv[x][y] = in ? -__ldg(dsum_h + c) : 0.f;
         }
       }
 #pragma unroll
@@ -343,6 +343,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + BT * half, tdP = tS + kHalf;
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = ptx::f2(sl2, sl2);
     bool ok = true;
     for (int n = 0; n < n_steps; ++n) {
       const int sst = n % kStat;
@@ -367,14 +368,16 @@ __global__ void __launch_bounds__(384, 1)
         ptx::tmem_ld32(tS + c * 32, us);
         ptx::tmem_ld32(tdP + c * 32, ud);
         ptx::tmem_wait_ld();
+        // exponent arguments s*scale*log2(e) - LSE*log2(e), two per instruction
+        // (the row terms are stored negated, so a 16-byte load is two pairs)
         float arg[32];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float4 l4 = ptx::lds128(l2s + c * 32 + e);
-          arg[e] = fmaf(__uint_as_float(us[e]), sl2, -l4.x);
-          arg[e + 1] = fmaf(__uint_as_float(us[e + 1]), sl2, -l4.y);
-          arg[e + 2] = fmaf(__uint_as_float(us[e + 2]), sl2, -l4.z);
-          arg[e + 3] = fmaf(__uint_as_float(us[e + 3]), sl2, -l4.w);
+          const ulonglong2 nl = ptx::lds128u(l2s + c * 32 + e);
+          ptx::unf2(ptx::fma2(ptx::f2(__uint_as_float(us[e]), __uint_as_float(us[e + 1])), sl2x2, nl.x), arg[e],
+                    arg[e + 1]);
+          ptx::unf2(ptx::fma2(ptx::f2(__uint_as_float(us[e + 2]), __uint_as_float(us[e + 3])), sl2x2, nl.y),
+                    arg[e + 2], arg[e + 3]);
         }
         if (!full) {
 #pragma unroll
@@ -383,21 +386,22 @@ __global__ void __launch_bounds__(384, 1)
             arg[e] = (col >= lo && col < hi) ? arg[e] : -INFINITY;
           }
         }
+        // P = 2^arg; dS = P * (dP - D), two per instruction
         uint32_t pp[16], pd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float4 d4 = ptx::lds128(dds + c * 32 + e);
-          const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], dv[4];
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            pv[x] = ptx::ex2(arg[e + x]);
-            dv[x] = pv[x] * (__uint_as_float(ud[e + x]) - dvv[x]);
-          }
-          pp[e / 2] = ptx::pack_bf16x2(pv[0], pv[1]);
-          pp[e / 2 + 1] = ptx::pack_bf16x2(pv[2], pv[3]);
-          pd[e / 2] = ptx::pack_bf16x2(dv[0], dv[1]);
-          pd[e / 2 + 1] = ptx::pack_bf16x2(dv[2], dv[3]);
+          const ulonglong2 nd = ptx::lds128u(dds + c * 32 + e);
+          const float p0 = ptx::ex2(arg[e]), p1 = ptx::ex2(arg[e + 1]);
+          const float p2 = ptx::ex2(arg[e + 2]), p3 = ptx::ex2(arg[e + 3]);
+          const uint64_t pa = ptx::f2(p0, p1), pb = ptx::f2(p2, p3);
+          float d0, d1, d2, d3;
+          ptx::unf2(ptx::mul2(pa, ptx::add2(ptx::f2(__uint_as_float(ud[e]), __uint_as_float(ud[e + 1])), nd.x)), d0, d1);
+          ptx::unf2(ptx::mul2(pb, ptx::add2(ptx::f2(__uint_as_float(ud[e + 2]), __uint_as_float(ud[e + 3])), nd.y)), d2,
+                    d3);
+          pp[e / 2] = ptx::pack_bf16x2(p0, p1);
+          pp[e / 2 + 1] = ptx::pack_bf16x2(p2, p3);
+          pd[e / 2] = ptx::pack_bf16x2(d0, d1);
+          pd[e / 2 + 1] = ptx::pack_bf16x2(d2, d3);
         }
         ptx::tmem_st16(tS + c * 16, pp);
         ptx::tmem_st16(tdP + c * 16, pd);
@@ -610,6 +614,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + BT * half, tdP = tS + kHalf;
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = ptx::f2(sl2, sl2), nl2x2 = ptx::f2(-l2, -l2), ndd2 = ptx::f2(-dd, -dd);
     bool ok = true;
     int2 next = n_blocks > 0 ? __ldg(&p.kb[kb_begin]) : make_int2(0, 0);
     for (int b = 0; b < n_blocks; ++b) {
@@ -630,7 +635,9 @@ __global__ void __launch_bounds__(384, 1)
         ptx::tmem_wait_ld();
         float arg[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) arg[e] = fmaf(__uint_as_float(us[e]), sl2, -l2);
+        for (int e = 0; e < 32; e += 2)
+          ptx::unf2(ptx::fma2(ptx::f2(__uint_as_float(us[e]), __uint_as_float(us[e + 1])), sl2x2, nl2x2), arg[e],
+                    arg[e + 1]);
         if (!(full && row_ok)) {
           // partial block: key j visible iff j < block end, j <= i < subtree_end[j]
 #pragma unroll
@@ -645,8 +652,9 @@ __global__ void __launch_bounds__(384, 1)
         uint32_t pd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float d0 = ptx::ex2(arg[e]) * (__uint_as_float(ud[e]) - dd);
-          const float d1 = ptx::ex2(arg[e + 1]) * (__uint_as_float(ud[e + 1]) - dd);
+          const uint64_t pp = ptx::f2(ptx::ex2(arg[e]), ptx::ex2(arg[e + 1]));
+          float d0, d1;
+          ptx::unf2(ptx::mul2(pp, ptx::add2(ptx::f2(__uint_as_float(ud[e]), __uint_as_float(ud[e + 1])), ndd2)), d0, d1);
           pd[e / 2] = ptx::pack_bf16x2(d0, d1);
         }
         ptx::tmem_st16(tS + c * 16, pd);

@@ -246,13 +246,14 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
       const int k0 = blk.x, nk = blk.y & 0xFFFF;
       const bool full = (blk.y >> 16) & 1;
       float sv[BN];
+      {
+        uint32_t u[BN];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t u[32];
-        ptx::tmem_ld32(s_tm + c * 32, u);
+        for (int c = 0; c < BN / 32; ++c)
+          ptx::tmem_ld32(s_tm + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sv[c * 32 + j] = __uint_as_float(u[j]);
+        for (int j = 0; j < BN; ++j) sv[j] = __uint_as_float(u[j]);
       }
       if (!full) {
 #pragma unroll
@@ -262,9 +263,14 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
           if (!vis) sv[c] = -INFINITY;
         }
       }
-      float mx = -INFINITY;
+      // row maximum: 3-input max, four independent chains
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, sv[c]);
+      for (int c = 0; c < BN; c += 8) {   // columns c .. c+7, exactly 0 .. BN-1
+#pragma unroll
+        for (int x = 0; x < 4; ++x) m4[x] = ptx::max3(m4[x], sv[c + 2 * x], sv[c + 2 * x + 1]);
+      }
+      const float mx = ptx::max3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
       const float m_blk = mx * sl2;
       float alpha = 1.f;
       const bool raise = m_blk > m_used + kRescaleThreshold;
@@ -273,19 +279,26 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
         m_used = m_blk;
       }
       const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
-      float sum = 0.f;
+      // exponent arguments and the row sum on packed fp32 pairs
+      const uint64_t sl2x2 = ptx::f2(sl2, sl2), negm = ptx::f2(-m_sub, -m_sub);
+      uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < BN / 64; ++c) {
         uint32_t pk[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float p0 = ptx::ex2(fmaf(sv[c * 64 + 2 * j], sl2, -m_sub));
-          const float p1 = ptx::ex2(fmaf(sv[c * 64 + 2 * j + 1], sl2, -m_sub));
-          sum += p0 + p1;
+          float a0, a1;
+          ptx::unf2(ptx::fma2(ptx::f2(sv[c * 64 + 2 * j], sv[c * 64 + 2 * j + 1]), sl2x2, negm), a0, a1);
+          const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
+          sum2[j & 1] = ptx::add2(sum2[j & 1], ptx::f2(p0, p1));
           pk[j] = ptx::pack_bf16x2(p0, p1);
         }
         ptx::tmem_st32(s_tm + c * 32, pk);
       }
+      float s0, s1, s2, s3;
+      ptx::unf2(sum2[0], s0, s1);
+      ptx::unf2(sum2[1], s2, s3);
+      const float sum = (s0 + s1) + (s2 + s3);
       l = l * alpha + sum;
       if (i > 0 && __any_sync(0xffffffffu, raise)) {
         // O accumulated through block i-1 is complete: the S(i) commit this
