@@ -42,6 +42,12 @@ constexpr int BM = 128;          // query rows per tile
 constexpr int BN = 128;          // keys per block
 constexpr int kBox = BM * 128;   // bytes of one 128-row x 64-element swizzled box
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+// Register split of the two-slot kernel (384 threads): the producer / MMA
+// warpgroup gives registers up to the two softmax warpgroups, which hold a
+// whole 128-column score row per thread.
+constexpr uint32_t kRegsCtl = 120;
+constexpr uint32_t kRegsSoftmax = 184;
+constexpr int kRegsNeeded = 128 * kRegsCtl + 256 * kRegsSoftmax;
 
 struct FwdParams {
   const int32_t* qt_q0;
@@ -120,6 +126,8 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
   ptx::tc_fence_after();
   const uint32_t tmem = S.tmem_base;
 
+  if (warp < 4) {
+  if constexpr (HPC == 2) ptx::regs_dec<kRegsCtl>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (ptx::elect_one()) {
@@ -224,8 +232,10 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
       ptx::mma_commit(&S.drain);
       ptx::mbar_drain(&S.drain, 0);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
     // ------------------------------------------------------------ softmax
+    if constexpr (HPC == 2) ptx::regs_inc<kRegsSoftmax>();
     const int slot = (warp - 4) >> 2;
     const int wq = warp & 3;                 // TMEM lane quarter of this warp
     const int r = wq * 32 + (threadIdx.x & 31);
@@ -368,6 +378,12 @@ int launch(const FwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, c
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
       return TPK_E_CUDA;
+    if constexpr (HPC == 2) {
+      // the warpgroups' register shares must fit in what the CTA launches with
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return TPK_E_CUDA;
+      if (fa.numRegs * 128 * (1 + HPC) < kRegsNeeded) return TPK_E_UNSUPPORTED;
+    }
     configured = true;
   }
   if (items <= 0) return TPK_OK;

@@ -108,6 +108,19 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// ---- per-warpgroup register budget ---------------------------------------------
+// Every thread of a warpgroup executes these together.  The shares of all
+// warpgroups must add up to no more than the registers the CTA was launched
+// with (threads x registers per thread at launch).
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---- tcgen05: descriptors ----------------------------------------------------
 // Shared-memory matrix descriptor, 128-byte swizzle (the layout a TMA load with
 // CU_TENSOR_MAP_SWIZZLE_128B writes: rows of 128 bytes, 16-byte chunks XOR-ed
