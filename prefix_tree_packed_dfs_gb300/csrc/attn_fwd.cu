@@ -45,8 +45,8 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units
 // Register split of the two-slot kernel (384 threads): the producer / MMA
 // warpgroup gives registers up to the two softmax warpgroups, which hold a
 // whole 128-column score row per thread.
-constexpr uint32_t kRegsCtl = 120;
-constexpr uint32_t kRegsSoftmax = 184;
+constexpr uint32_t kRegsCtl = 56;
+constexpr uint32_t kRegsSoftmax = 216;
 constexpr int kRegsNeeded = 128 * kRegsCtl + 256 * kRegsSoftmax;
 
 struct FwdParams {
