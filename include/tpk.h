@@ -149,7 +149,11 @@ int tpk_plan_export(const tpk_plan* plan, int64_t* row_offsets, int64_t* row_loa
  * (a contiguous ancestor chain of segment intervals, [ART] "Token-mixing layers").
  * Backward: key tile u covers [kt_k0[u], +kt_nk[u]); its query blocks qb[2c],
  * qb[2c+1] for c in [kt_qb_begin[u], kt_qb_begin[u+1]) cover [k0, max subtree_end).
- * qt_order / kt_order list the tiles by decreasing work (longest first). */
+ * qt_order / kt_order: launch order of the tiles.  Tiles are cut into runs of
+ * 128 consecutive tiles (depth-first order); runs come by decreasing total
+ * work, and inside a run tiles come by decreasing work.  Neighbouring tiles
+ * share ancestor (query tiles) or descendant (key tiles) blocks, so CTAs that
+ * run together reuse them from L2. */
 int tpk_plan_worklists(const tpk_plan* plan, int32_t* qt_q0, int32_t* qt_nq,
                        int32_t* qt_kb_begin, int32_t* kb, int32_t* qt_order,
                        int32_t* kt_k0, int32_t* kt_nk, int32_t* kt_qb_begin,

@@ -26,7 +26,12 @@
 //     ([ART] "Token-mixing layers": [enter, exit] intervals);
 //  5. the kernels' work lists: per 128-query tile, the key blocks of the
 //     ancestor chain of its first query plus the tile itself; per 128-key tile,
-//     the query blocks of [k0, max subtree_end); both in longest-first order.
+//     the query blocks of [k0, max subtree_end).  Launch order: runs of
+//     kOrderChunk consecutive tiles (depth-first order, so neighbouring
+//     subtrees), runs in decreasing total work, tiles of a run longest first.
+//     CTAs resident at the same time then read the same ancestor K/V blocks
+//     (query tiles) or descendant Q/dO blocks (key tiles) and share them in
+//     L2, while long work still starts before short work.
 #include "planner.h"
 
 #include <algorithm>
@@ -42,6 +47,7 @@ namespace {
 
 constexpr int64_t kNoTarget = -2;  // untrained position: target not part of the key
 constexpr int64_t kEos = -1;       // target of the last position
+constexpr int32_t kOrderChunk = 128;   // tiles per run of the launch order (16384 tokens)
 
 inline uint64_t pack_symbol(int32_t token, int flag, int64_t target) {
   // lexicographic (token, flag, target) as one unsigned integer: tokens are
@@ -384,16 +390,26 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   if (P.kb.size() / 2 >= (size_t{1} << 31) || P.qb.size() / 2 >= (size_t{1} << 31)) return TPK_E_OVERFLOW;
   P.qt_kb_begin.push_back(static_cast<int32_t>(P.kb.size() / 2));
   P.kt_qb_begin.push_back(static_cast<int32_t>(P.qb.size() / 2));
-  auto lpt = [](const std::vector<int32_t>& begin) {
-    std::vector<int32_t> o(begin.size() - 1);
-    std::iota(o.begin(), o.end(), 0);
-    std::stable_sort(o.begin(), o.end(), [&](int32_t a, int32_t b) {
-      return begin[a + 1] - begin[a] > begin[b + 1] - begin[b];
-    });
+  auto launch_order = [](const std::vector<int32_t>& begin) {
+    const int32_t n = static_cast<int32_t>(begin.size()) - 1;
+    const int32_t n_runs = (n + kOrderChunk - 1) / kOrderChunk;
+    auto work = [&](int32_t t) { return begin[t + 1] - begin[t]; };
+    std::vector<int64_t> run_work(n_runs, 0);
+    for (int32_t t = 0; t < n; ++t) run_work[t / kOrderChunk] += work(t);
+    std::vector<int32_t> runs(n_runs);
+    std::iota(runs.begin(), runs.end(), 0);
+    std::stable_sort(runs.begin(), runs.end(), [&](int32_t a, int32_t b) { return run_work[a] > run_work[b]; });
+    std::vector<int32_t> o;
+    o.reserve(n);
+    for (int32_t r : runs) {
+      const size_t first = o.size();
+      for (int32_t t = r * kOrderChunk; t < std::min(n, (r + 1) * kOrderChunk); ++t) o.push_back(t);
+      std::stable_sort(o.begin() + first, o.end(), [&](int32_t a, int32_t b) { return work(a) > work(b); });
+    }
     return o;
   };
-  P.qt_order = lpt(P.qt_kb_begin);
-  P.kt_order = lpt(P.kt_qb_begin);
+  P.qt_order = launch_order(P.qt_kb_begin);
+  P.kt_order = launch_order(P.kt_qb_begin);
 
   // ---- device image -------------------------------------------------------
   size_t off = 0;

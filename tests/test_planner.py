@@ -166,3 +166,36 @@ def test_worklists_visit_only_the_ancestor_chain(lib):
     info = got.info
     assert info["visited_pairs"] < 1.1 * info["useful_pairs"] * 2  # diagonal blocks count full squares
     assert info["visited_pairs"] >= info["useful_pairs"]
+
+
+def _check_launch_order(order, begin, run=128):
+    work = np.diff(begin)
+    n = len(work)
+    assert sorted(order) == list(range(n))
+    runs = [order[i:i + min(run, n - i)] for i in range(0, n, run)]
+    # the order is a sequence of whole runs of consecutive tiles ...
+    pos, run_work = 0, []
+    seen = set()
+    while pos < n:
+        r = order[pos] // run
+        assert r not in seen
+        seen.add(r)
+        size = min(run, n - r * run)
+        chunk = order[pos:pos + size]
+        assert sorted(chunk) == list(range(r * run, r * run + size))
+        # ... longest first inside a run ...
+        assert all(work[a] >= work[b] for a, b in zip(chunk, chunk[1:]))
+        run_work.append(int(work[chunk].sum()))
+        pos += size
+    # ... and runs by decreasing total work
+    assert all(a >= b for a, b in zip(run_work, run_work[1:]))
+    assert len(runs) == len(seen)
+
+
+@pytest.mark.parametrize("name", ["deep_small", "grpo", "sweep_2.00"])
+def test_launch_order_runs_longest_first(lib, name):
+    w = workloads.get(name)
+    got = _cpp_plan(w.sequences, groups=w.group_ids, min_shared=w.min_shared, cap=w.row_capacity)
+    wl = got.worklists()
+    _check_launch_order(list(wl["qt_order"]), wl["qt_kb_begin"])
+    _check_launch_order(list(wl["kt_order"]), wl["kt_qb_begin"])
