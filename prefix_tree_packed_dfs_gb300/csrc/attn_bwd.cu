@@ -83,12 +83,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   }
 }
 
-// Barrier over the `count` threads of one warpgroup (ids 1.. are free: 0 is
-// __syncthreads).
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // Row epilogue helper: 32 fp32 TMEM columns * mul -> 32 bf16 stored to dst.
 __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&u)[32], float mul) {
   uint32_t pk[16];
@@ -159,7 +153,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int s = 0; s < kStat; ++s) {
       ptx::mbar_init(&S.stat_full[s], 1);
-      ptx::mbar_init(&S.stat_empty[s], 2);   // one arrival per softmax warpgroup
+      ptx::mbar_init(&S.stat_empty[s], 8);   // one arrival per softmax warp
     }
     for (int h = 0; h < 2; ++h) {
       ptx::mbar_init(&S.s_full[h], 1);
@@ -409,9 +403,9 @@ __global__ void __launch_bounds__(384, 1)
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(&S.p_full[half]);
-      // the row terms of this step are no longer needed by this warpgroup
-      named_bar_sync(1 + half, 128);
-      if (t == 0) ptx::mbar_arrive(&S.stat_empty[sst]);
+      // the row terms of this step are no longer needed by this warp
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&S.stat_empty[sst]);
     }
     if (ok) {
       ok = ptx::mbar_wait(&S.acc_done, 0, abort_flag, kWaitLimitNs);
@@ -449,7 +443,11 @@ __global__ void __launch_bounds__(384, 1)
 // K and V stream through an NH-deep ring of 64-key half-stages (64-row TMA
 // boxes), each released as soon as its half's dQ product is issued.
 // TMEM: slot h at [128h, 128h+128): S (64 cols) then dP (64 cols); dQ at
-// [256, 256+D).  dS (bf16) overwrites the first 32 columns of S of its slot.
+// [256, 256+D); the query tile's Q and dO (bf16, D/2 cols each) after it.
+// dS (bf16) overwrites the first 32 columns of S of its slot.  Q and dO are
+// the A operands of the S and dP products straight from TMEM: shared memory
+// then only feeds the 64-key K / V halves (an A tile from shared memory as
+// well would need 6 KB per 32-cycle N=64 product, above the port's rate).
 // Warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 4-7 softmax of half 0,
 // 8-11 softmax of half 1 (thread t owns query row t).
 template <int D, int NH>
@@ -458,7 +456,7 @@ struct QSmem {
   uint8_t dO[D / 64][kBox];
   uint8_t k[NH][D / 64][kHalfBox];
   uint8_t v[NH][D / 64][kHalfBox];
-  uint64_t q_full, kv_full[NH], kv_empty[NH], s_full[2], p_full[2], acc_done, drain;
+  uint64_t q_full, qt_full, kv_full[NH], kv_empty[NH], s_full[2], p_full[2], acc_done, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -483,9 +481,11 @@ __global__ void __launch_bounds__(384, 1)
   const int kb_begin = __ldg(p.qt_kb_begin + tile);
   const int n_blocks = __ldg(p.qt_kb_begin + tile + 1) - kb_begin;
   constexpr uint32_t cdQ = 256;
+  constexpr uint32_t cQt = 256 + D, cOt = 256 + D + D / 2;   // Q, dO (bf16 pairs)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&S.q_full, 1);
+    ptx::mbar_init(&S.qt_full, 256);   // every softmax thread, after its TMEM row copy
     for (int s = 0; s < NH; ++s) {
       ptx::mbar_init(&S.kv_full[s], 1);
       ptx::mbar_init(&S.kv_empty[s], 1);
@@ -537,10 +537,8 @@ __global__ void __launch_bounds__(384, 1)
     if (ptx::elect_one()) {
       constexpr uint32_t idesc_s = ptx::idesc_bf16_f32(BT, kHalf, false, false);
       constexpr uint32_t idesc_dq = ptx::idesc_bf16_f32(BT, D, false, true);
-      bool ok = ptx::mbar_wait(&S.q_full, 0, abort_flag, kWaitLimitNs);
+      bool ok = ptx::mbar_wait(&S.qt_full, 0, abort_flag, kWaitLimitNs);
       ptx::tc_fence_after();
-      const uint32_t q_base = ptx::smem_addr(S.q[0]);
-      const uint32_t do_base = ptx::smem_addr(S.dO[0]);
       // S, dP of one 64-key half-stage (K-major B operands, 64 rows)
       auto issue_sdp = [&](int m, int slot) {
         const uint32_t kb = ptx::smem_addr(S.k[m % NH][0]);
@@ -548,17 +546,15 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t cS = BT * slot, cdP = BT * slot + kHalf;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
           const uint32_t boff = (kk >> 2) * kHalfBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cS, ptx::desc_add(ptx::sw128_desc(q_base, 16, 1024), aoff), ptx::desc_add(ptx::sw128_desc(kb, 16, 1024), boff),
-                      idesc_s, kk > 0 ? 1u : 0u);
+          ptx::mma_ts(tmem + cS, tmem + cQt + kk * 8, ptx::desc_add(ptx::sw128_desc(kb, 16, 1024), boff), idesc_s,
+                      kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
           const uint32_t boff = (kk >> 2) * kHalfBox + (kk & 3) * 32;
-          ptx::mma_ss(tmem + cdP, ptx::desc_add(ptx::sw128_desc(do_base, 16, 1024), aoff), ptx::desc_add(ptx::sw128_desc(vb, 16, 1024), boff),
-                      idesc_s, kk > 0 ? 1u : 0u);
+          ptx::mma_ts(tmem + cdP, tmem + cOt + kk * 8, ptx::desc_add(ptx::sw128_desc(vb, 16, 1024), boff), idesc_s,
+                      kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(&S.s_full[slot]);
       };
@@ -615,9 +611,35 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tmem + lane_off + BT * half, tdP = tS + kHalf;
     const float sl2 = p.scale_log2;
     const uint64_t sl2x2 = ptx::f2(sl2, sl2), nl2x2 = ptx::f2(-l2, -l2), ndd2 = ptx::f2(-dd, -dd);
-    bool ok = true;
+    // row t of the query tile into TMEM lane t: warpgroup 0 copies Q, 1 copies
+    // dO.  The tile sits in shared memory as 128-byte-swizzled boxes of 64
+    // elements (16-byte chunk c of row t at chunk c ^ (t % 8)); TMEM column w
+    // holds elements 2w, 2w+1.
+    bool ok = ptx::mbar_wait(&S.q_full, 0, abort_flag, kWaitLimitNs);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      const uint8_t* box0 = half == 0 ? S.q[0] : S.dO[0];
+      const uint32_t dst = tmem + lane_off + (half == 0 ? cQt : cOt);
+#pragma unroll
+      for (int b = 0; b < D / 64; ++b) {
+        uint32_t w[32];
+        const uint8_t* row = box0 + b * kBox + t * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ (t & 7)) << 4));
+          w[4 * c] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
+        }
+        ptx::tmem_st32(dst + b * 32, w);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&S.qt_full);
+    }
     int2 next = n_blocks > 0 ? __ldg(&p.kb[kb_begin]) : make_int2(0, 0);
-    for (int b = 0; b < n_blocks; ++b) {
+    for (int b = 0; ok && b < n_blocks; ++b) {
       const int2 blk = next;   // fetched one block ahead
       if (b + 1 < n_blocks) next = __ldg(&p.kb[kb_begin + b + 1]);
       ok = ptx::mbar_wait(&S.s_full[half], b & 1, abort_flag, kWaitLimitNs);

@@ -46,3 +46,14 @@ def test_two_gloo_ranks_share_only_timing():
     assert slow0 == slow1 == pytest.approx(1.5)     # max over ranks on both
     import workloads
     assert v0 == v1 == pytest.approx(2 * workloads.get("tiny").n_raw / 1.5)
+
+
+def test_recorded_traffic_only_for_the_sources_it_was_taken_on(monkeypatch):
+    import bench
+    digest = bench.source_digest()
+    monkeypatch.setattr(bench, "TRAFFIC", {"digest": digest, "fwd": 123, "bwd_dkdv": 456, "bwd_dq": None})
+    assert bench.recorded_traffic("bwd_dkdv", bench.WORKLOAD) == 456
+    assert bench.recorded_traffic("bwd_dq", bench.WORKLOAD) is None
+    assert bench.recorded_traffic("fwd", "deep_small") is None          # another workload
+    monkeypatch.setattr(bench, "TRAFFIC", {"digest": "0" * 64, "fwd": 123, "bwd_dkdv": 456, "bwd_dq": 7})
+    assert bench.recorded_traffic("bwd_dkdv", bench.WORKLOAD) is None   # sources changed since
