@@ -117,7 +117,7 @@ struct KVSmem {
   float lse2[kStat][BT];   // -LSE * log2(e) of the step's queries (-inf past the block)
   float dsum[kStat][BT];   // -D = -(dO . O)
   int2 blk[kStat];         // the step's query block (first query, count | full << 16)
-  uint64_t kv_full, q_full[NH], q_empty[NH], stat_full[kStat], stat_empty[kStat], s_full[2], p_full[2], acc_done,
+  uint64_t kv_full, q_full[NH], q_empty[NH], stat_full[kStat], stat_empty[kStat], s_full[2], p_part[2], p_full[2], acc_done,
       drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int h = 0; h < 2; ++h) {
       ptx::mbar_init(&S.s_full[h], 1);
+      ptx::mbar_init(&S.p_part[h], 128);   // P^T, dS^T of the half's first 32 queries stored
       ptx::mbar_init(&S.p_full[h], 128);
     }
     ptx::mbar_init(&S.acc_done, 1);
@@ -284,18 +285,27 @@ __global__ void __launch_bounds__(384, 1)
       };
       // dV += P^T dO_half, dK += dS^T Q_half (half-stages as MN-major B
       // operands: d-column groups one 64-row box apart), then release the stage
-      auto issue_acc = [&](int m, int slot, bool first) {
+      // in two parts of 32 queries, each issued as soon as the softmax has
+      // stored that part's P^T and dS^T (p_part, then p_full)
+      auto issue_acc = [&](int m, int slot, bool first, uint32_t parity) {
         const uint32_t qb = ptx::smem_addr(S.q[m % NH][0]);
         const uint32_t ob = ptx::smem_addr(S.dO[m % NH][0]);
         const uint32_t cS = BT * slot, cdP = BT * slot + kHalf;
+        for (int part = 0; part < 2; ++part) {
+          if (!ptx::mbar_wait(part == 0 ? &S.p_part[slot] : &S.p_full[slot], parity, abort_flag, kWaitLimitNs))
+            return false;
+          ptx::tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kHalf / 16; ++kk) {
-          const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-          ptx::mma_ts(tmem + cdV, tmem + cS + kk * 8, ptx::desc_add(ptx::sw128_desc(ob, kHalfBox, 1024), kk * 2048), idesc_acc, acc);
-          ptx::mma_ts(tmem + cdK, tmem + cdP + kk * 8, ptx::desc_add(ptx::sw128_desc(qb, kHalfBox, 1024), kk * 2048), idesc_acc,
-                      acc);
+          for (int kk = part * (kHalf / 32); kk < (part + 1) * (kHalf / 32); ++kk) {
+            const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+            ptx::mma_ts(tmem + cdV, tmem + cS + kk * 8, ptx::desc_add(ptx::sw128_desc(ob, kHalfBox, 1024), kk * 2048),
+                        idesc_acc, acc);
+            ptx::mma_ts(tmem + cdK, tmem + cdP + kk * 8, ptx::desc_add(ptx::sw128_desc(qb, kHalfBox, 1024), kk * 2048),
+                        idesc_acc, acc);
+          }
         }
         ptx::mma_commit(&S.q_empty[m % NH]);
+        return true;
       };
       auto wait_stage = [&](int m) {
         const bool r = ptx::mbar_wait(&S.q_full[m % NH], (m / NH) & 1, abort_flag, kWaitLimitNs);
@@ -305,24 +315,14 @@ __global__ void __launch_bounds__(384, 1)
       for (int n = 0; ok && n < n_steps; ++n) {
         if (!wait_stage(2 * n)) { ok = false; break; }
         issue_sdp(2 * n, 0);
-        if (n > 0) {
-          if (!ptx::mbar_wait(&S.p_full[1], (n - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-          ptx::tc_fence_after();
-          issue_acc(2 * n - 1, 1, false);
-        }
+        if (n > 0 && !issue_acc(2 * n - 1, 1, false, (n - 1) & 1)) { ok = false; break; }
         if (!wait_stage(2 * n + 1)) { ok = false; break; }
         issue_sdp(2 * n + 1, 1);
-        if (!ptx::mbar_wait(&S.p_full[0], n & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-        ptx::tc_fence_after();
-        issue_acc(2 * n, 0, n == 0);
+        if (!issue_acc(2 * n, 0, n == 0, n & 1)) { ok = false; break; }
       }
       if (ok && n_steps > 0) {
         const int last = n_steps - 1;
-        if (ptx::mbar_wait(&S.p_full[1], last & 1, abort_flag, kWaitLimitNs)) {
-          ptx::tc_fence_after();
-          issue_acc(2 * last + 1, 1, false);
-          ptx::mma_commit(&S.acc_done);
-        }
+        if (issue_acc(2 * last + 1, 1, false, last & 1)) ptx::mma_commit(&S.acc_done);
       }
       ptx::mma_commit(&S.drain);
       ptx::mbar_drain(&S.drain, 0);
@@ -399,10 +399,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         ptx::tmem_st16(tS + c * 16, pp);
         ptx::tmem_st16(tdP + c * 16, pd);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(c == 0 ? &S.p_part[half] : &S.p_full[half]);
       }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&S.p_full[half]);
       // the row terms of this step are no longer needed by this warp
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&S.stat_empty[sst]);
@@ -456,7 +456,7 @@ struct QSmem {
   uint8_t dO[D / 64][kBox];
   uint8_t k[NH][D / 64][kHalfBox];
   uint8_t v[NH][D / 64][kHalfBox];
-  uint64_t q_full, qt_full, kv_full[NH], kv_empty[NH], s_full[2], p_full[2], acc_done, drain;
+  uint64_t q_full, qt_full, kv_full[NH], kv_empty[NH], s_full[2], p_part[2], p_full[2], acc_done, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -492,6 +492,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int x = 0; x < 2; ++x) {
       ptx::mbar_init(&S.s_full[x], 1);
+      ptx::mbar_init(&S.p_part[x], 128);   // dS of the half's first 32 keys stored
       ptx::mbar_init(&S.p_full[x], 128);
     }
     ptx::mbar_init(&S.acc_done, 1);
@@ -560,14 +561,22 @@ __global__ void __launch_bounds__(384, 1)
       };
       // dQ += dS K_half (half-stage as the MN-major B operand: d-column groups
       // one 64-row box apart, 16 keys = 2 KB per step); then release the stage
-      auto issue_dq = [&](int m, int slot, bool first) {
+      // in two parts of 32 keys, each issued as soon as the softmax has
+      // stored that part's dS (p_part, then p_full)
+      auto issue_dq = [&](int m, int slot, bool first, uint32_t parity) {
         const uint32_t kb = ptx::smem_addr(S.k[m % NH][0]);
         const uint32_t cS = BT * slot;
+        for (int part = 0; part < 2; ++part) {
+          if (!ptx::mbar_wait(part == 0 ? &S.p_part[slot] : &S.p_full[slot], parity, abort_flag, kWaitLimitNs))
+            return false;
+          ptx::tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kHalf / 16; ++kk)
-          ptx::mma_ts(tmem + cdQ, tmem + cS + kk * 8, ptx::desc_add(ptx::sw128_desc(kb, kHalfBox, 1024), kk * 2048), idesc_dq,
-                      (first && kk == 0) ? 0u : 1u);
+          for (int kk = part * (kHalf / 32); kk < (part + 1) * (kHalf / 32); ++kk)
+            ptx::mma_ts(tmem + cdQ, tmem + cS + kk * 8, ptx::desc_add(ptx::sw128_desc(kb, kHalfBox, 1024), kk * 2048),
+                        idesc_dq, (first && kk == 0) ? 0u : 1u);
+        }
         ptx::mma_commit(&S.kv_empty[m % NH]);
+        return true;
       };
       auto wait_stage = [&](int m) {
         const bool r = ptx::mbar_wait(&S.kv_full[m % NH], (m / NH) & 1, abort_flag, kWaitLimitNs);
@@ -577,24 +586,14 @@ __global__ void __launch_bounds__(384, 1)
       for (int i = 0; ok && i < n_blocks; ++i) {
         if (!wait_stage(2 * i)) { ok = false; break; }
         issue_sdp(2 * i, 0);
-        if (i > 0) {
-          if (!ptx::mbar_wait(&S.p_full[1], (i - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-          ptx::tc_fence_after();
-          issue_dq(2 * i - 1, 1, false);
-        }
+        if (i > 0 && !issue_dq(2 * i - 1, 1, false, (i - 1) & 1)) { ok = false; break; }
         if (!wait_stage(2 * i + 1)) { ok = false; break; }
         issue_sdp(2 * i + 1, 1);
-        if (!ptx::mbar_wait(&S.p_full[0], i & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-        ptx::tc_fence_after();
-        issue_dq(2 * i, 0, i == 0);
+        if (!issue_dq(2 * i, 0, i == 0, i & 1)) { ok = false; break; }
       }
       if (ok && n_blocks > 0) {
         const int last = n_blocks - 1;
-        if (ptx::mbar_wait(&S.p_full[1], last & 1, abort_flag, kWaitLimitNs)) {
-          ptx::tc_fence_after();
-          issue_dq(2 * last + 1, 1, false);
-          ptx::mma_commit(&S.acc_done);
-        }
+        if (issue_dq(2 * last + 1, 1, false, last & 1)) ptx::mma_commit(&S.acc_done);
       }
       ptx::mma_commit(&S.drain);
       ptx::mbar_drain(&S.drain, 0);
@@ -680,10 +679,10 @@ __global__ void __launch_bounds__(384, 1)
           pd[e / 2] = ptx::pack_bf16x2(d0, d1);
         }
         ptx::tmem_st16(tS + c * 16, pd);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(c == 0 ? &S.p_part[half] : &S.p_full[half]);
       }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&S.p_full[half]);
     }
     if (ok) {
       ok = ptx::mbar_wait(&S.acc_done, 0, abort_flag, kWaitLimitNs);

@@ -70,7 +70,7 @@ struct FwdSmem {
   uint8_t v[NS][D / 64][kBox];
   uint64_t q_full;
   uint64_t k_full[NS], v_full[NS], k_empty[NS], v_empty[NS];
-  uint64_t s_full[HPC], p_full[HPC], o_done[HPC];
+  uint64_t s_full[HPC], p_half[HPC], p_full[HPC], o_done[HPC];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
     }
     for (int h = 0; h < HPC; ++h) {
       ptx::mbar_init(&S.s_full[h], 1);
+      ptx::mbar_init(&S.p_half[h], 128);   // P of keys 0..63 stored
       ptx::mbar_init(&S.p_full[h], 128);
       ptx::mbar_init(&S.o_done[h], 1);
     }
@@ -171,13 +172,15 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
       bool ok = ptx::mbar_wait(&S.q_full, 0, abort_flag, kWaitLimitNs);
       ptx::tc_fence_after();
       const uint32_t q_base[2] = {ptx::smem_addr(S.q[0][0]), ptx::smem_addr(S.q[HPC - 1][0])};
-      auto issue_pv = [&](int s, int blk) {
+      // PV of one key half (keys 64*part ..), so the first half's products
+      // run while the softmax still computes the second half's P
+      auto issue_pv = [&](int s, int blk, int part) {
         const int st = blk % NS;
         const uint32_t v_base = ptx::smem_addr(S.v[st][0]);
         const uint32_t o_col = tmem + BM * HPC + D * s;
         const uint32_t p_col = tmem + BM * s;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
+        for (int kk = part * (BN / 32); kk < (part + 1) * (BN / 32); ++kk) {
           // V block as the MN-major B operand: N = head dim (64-wide column
           // groups one box apart), K = 16 keys = 2 KB further per step
           const uint64_t bdesc = ptx::desc_add(ptx::sw128_desc(v_base, kBox, 1024), kk * 2048);
@@ -197,9 +200,12 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
               ok = false;
               break;
             }
+            if (!ptx::mbar_wait(&S.p_half[s], (i - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+            ptx::tc_fence_after();
+            issue_pv(s, i - 1, 0);
             if (!ptx::mbar_wait(&S.p_full[s], (i - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
             ptx::tc_fence_after();
-            issue_pv(s, i - 1);
+            issue_pv(s, i - 1, 1);
           }
           const uint32_t s_col = tmem + BM * s;
 #pragma unroll
@@ -221,9 +227,12 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
         const int last = n_blocks - 1;
         if (ptx::mbar_wait(&S.v_full[last % NS], (last / NS) & 1, abort_flag, kWaitLimitNs)) {
           for (int s = 0; s < HPC; ++s) {
+            if (!ptx::mbar_wait(&S.p_half[s], last & 1, abort_flag, kWaitLimitNs)) break;
+            ptx::tc_fence_after();
+            issue_pv(s, last, 0);
             if (!ptx::mbar_wait(&S.p_full[s], last & 1, abort_flag, kWaitLimitNs)) break;
             ptx::tc_fence_after();
-            issue_pv(s, last);
+            issue_pv(s, last, 1);
             ptx::mma_commit(&S.o_done[s]);
           }
         }
@@ -288,8 +297,23 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
         alpha = ptx::ex2(m_used - m_blk);   // 0 when m_used = -inf
         m_used = m_blk;
       }
+      if (i > 0 && __any_sync(0xffffffffu, raise)) {
+        // O accumulated through block i-1 is complete: the S(i) commit this
+        // warp waited on tracks every earlier MMA, including PV(i-1).  It is
+        // rescaled before any P of block i is released to the PV products.
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          ptx::tmem_ld32(o_tm + c * 32, u);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * alpha);
+          ptx::tmem_st32(o_tm + c * 32, u);
+        }
+      }
       const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
-      // exponent arguments and the row sum on packed fp32 pairs
+      // exponent arguments and the row sum on packed fp32 pairs; P of keys
+      // 0..63 is released (p_half) before the second half is computed
       const uint64_t sl2x2 = ptx::f2(sl2, sl2), negm = ptx::f2(-m_sub, -m_sub);
       uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
@@ -304,28 +328,15 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
           pk[j] = ptx::pack_bf16x2(p0, p1);
         }
         ptx::tmem_st32(s_tm + c * 32, pk);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(c == 0 ? &S.p_half[slot] : &S.p_full[slot]);
       }
       float s0, s1, s2, s3;
       ptx::unf2(sum2[0], s0, s1);
       ptx::unf2(sum2[1], s2, s3);
       const float sum = (s0 + s1) + (s2 + s3);
       l = l * alpha + sum;
-      if (i > 0 && __any_sync(0xffffffffu, raise)) {
-        // O accumulated through block i-1 is complete: the S(i) commit this
-        // warp waited on tracks every earlier MMA, including PV(i-1)
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t u[32];
-          ptx::tmem_ld32(o_tm + c * 32, u);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * alpha);
-          ptx::tmem_st32(o_tm + c * 32, u);
-        }
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(&S.p_full[slot]);
     }
     if (ok) {
       ok = ptx::mbar_wait(&S.o_done[slot], 0, abort_flag, kWaitLimitNs);

@@ -282,6 +282,18 @@ def test_backward_full_size_sampled(ops):
     q, k, o, lse, _, _ = gpu_forward(ops, case, Q, K, V)
     del Q, K
     dq, dk, dv = gpu_backward(ops, case, q, k, V, o, lse, dO)
+    # every key at full size, the root's included: per KV head the keys' dV
+    # add up to dO summed over all queries and the group's query heads
+    # (softmax rows sum to one).  Rounding P and each dV to bf16 adds
+    # independent zero-mean errors of at most 2^-9 relative, so the gap is
+    # held to six standard deviations of their sum.
+    G = w.n_heads_q // w.n_heads_kv
+    for g in range(w.n_heads_kv):   # one KV head at a time, fp32 sums (error far below the bound)
+        grp, dvg = dO[:, g * G:(g + 1) * G].float(), dv[:, g].float()
+        lhs, rhs = dvg.sum(0).double(), grp.sum((0, 1)).double()
+        sigma = 2.0 ** -9 / 3 ** 0.5 * torch.sqrt((grp ** 2).sum((0, 1)).double() + (dvg ** 2).sum(0).double())
+        assert bool(((lhs - rhs).abs() <= 6 * sigma + 1e-3).all()), ("dV sum identity", g)
+        del grp, dvg
     del q, k, V, dO, o
     rows = (case.rows("q", w.n_heads_q), case.rows("k", w.n_heads_kv), case.rows("v", w.n_heads_kv),
             case.rows("do", w.n_heads_q))

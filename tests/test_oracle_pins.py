@@ -461,3 +461,18 @@ def test_backward_rows_match_full_backward():
     dk, dv = oa.backward_rows_kv(p, rows(Q), rows(K), rows(V), rows(dO), fw, 1e4)
     assert np.allclose(dk, dK[fw], atol=1e-12)
     assert np.allclose(dv, dV[fw], atol=1e-12)
+
+
+def test_backward_dv_sums_to_do_per_kv_head():
+    # every softmax row sums to one, so over all keys dV adds up to dO summed
+    # over all queries and the query heads that share the KV head; a wrong
+    # head grouping, a transposed P or a missing normalisation breaks it
+    seqs, p, Q, K, V = _tiny_tree(4, hq=4, hkv=2, d=8)
+    rng = np.random.Generator(np.random.PCG64(13))
+    dO = rng.standard_normal(Q.shape)
+    _, _, dV = oa.backward(p, Q, K, V, dO, 1e4)
+    G = Q.shape[1] // K.shape[1]
+    for g in range(K.shape[1]):
+        lhs = dV[:, g, :].sum(axis=0)
+        rhs = dO[:, g * G:(g + 1) * G, :].sum(axis=(0, 1))
+        assert np.allclose(lhs, rhs, rtol=1e-12, atol=1e-10)
