@@ -6,7 +6,8 @@ One step = the whole path over one batch of the deep-tree workload (root of
 128 leaves, rows of 65536 forwarded tokens, 32 query / 8 KV heads, head_dim
 128, bf16):
     RoPE at depth (Q, K)  ->  tree attention forward (O, LSE)
-    ->  scatter to raw-token order (O, LSE)  ->  tree attention backward
+    ->  scatter to raw-token order (O, LSE)  ->  raw-order dO summed into the
+    packed layout (the scatter's transpose)  ->  tree attention backward
     (prep, dK/dV pass, dQ pass)  ->  inverse RoPE on dQ, dK.
 The plan (host) is built once for ``value``; the ``e2e`` leg rebuilds it
 every step and moves inputs from pinned host memory and the raw-order LSE
@@ -39,7 +40,7 @@ WORKLOAD = "deep"
 WORKLOAD_DESC = ("deep random tree: root 4096, branching {1,2,3} every 256-1024 tokens to depth 24000, "
                  "128 leaves, rows 65536, Hq 32 / Hkv 8 / d 128, fwd+bwd")
 METRIC = "tree-attn raw tokens/s, useful TFLOP/s and % of GB300 bf16 dense peak"
-LAUNCHES_PER_STEP = 8   # rope, fwd, scatter rows, scatter lse, bwd prep, bwd dK/dV, bwd dQ, rope inverse
+LAUNCHES_PER_STEP = 9   # rope, fwd, scatter rows, scatter lse, dO sum, bwd prep, bwd dK/dV, bwd dQ, rope inverse
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # attention kernels on the deep-tree workload, from one ncu capture of
@@ -81,6 +82,9 @@ def _args():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layout", action="store_true",
+                    help="raw order <-> packed layout kernels (materialisation gather, sum of raw-order rows) "
+                         "on --workload; one line")
     ap.add_argument("--sweep", action="store_true",
                     help="packing-ratio sweep (32,768-token rows): forward time against forwarded and raw "
                          "tokens, tree layout vs sequence packing of the same raw tokens; one line per point")
@@ -291,7 +295,10 @@ def run_ours(a):
     Q = wrng.normal_bf16(s["q"], (F, Hq, d), dev)
     K = wrng.normal_bf16(s["k"], (F, Hkv, d), dev)
     V = wrng.normal_bf16(s["v"], (F, Hkv, d), dev)
-    dO = wrng.normal_bf16(s["do"], (F, Hq, d), dev)
+    # the output gradient arrives in raw order, one row per raw token, and is
+    # summed into the packed layout inside the step (transpose of the scatter)
+    dO_raw = wrng.normal_bf16(s["do"], (R, Hq, d), dev)
+    dO = torch.empty((F, Hq, d), dtype=torch.bfloat16, device=dev)
     qr, kr = torch.empty_like(Q), torch.empty_like(K)
     O = torch.empty_like(Q)
     LSE = torch.empty((Hq, F), dtype=torch.float32, device=dev)
@@ -300,7 +307,7 @@ def run_ours(a):
     dq, dk, dv = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     ws = torch.empty(max(ops.attn_workspace_bytes(dp, Hq, Hkv, d, True), 256), dtype=torch.uint8, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    names = ["rope", "fwd", "scatter", "bwd_prep", "bwd_dkdv", "bwd_dq", "rope_inv"]
+    names = ["rope", "fwd", "scatter", "dO_sum", "bwd_prep", "bwd_dkdv", "bwd_dq", "rope_inv"]
 
     def step(dplan, ev=None, ready=None):
         """One pass of the path.  ``ready`` (end to end only): events of the
@@ -321,14 +328,16 @@ def run_ours(a):
             ready["out"].record()
         mark(3)
         wait("do")
-        ops.tree_attn_bwd(dplan, qr, kr, V, O, LSE, dO, dq=dq, dk=dk, dv=dv, workspace=ws, dev_err=err, phases=(0,))
+        ops.sum_to_forwarded(dplan, dO_raw, dst=dO)
         mark(4)
-        ops.tree_attn_bwd(dplan, qr, kr, V, O, LSE, dO, dq=dq, dk=dk, dv=dv, workspace=ws, dev_err=err, phases=(1,))
+        ops.tree_attn_bwd(dplan, qr, kr, V, O, LSE, dO, dq=dq, dk=dk, dv=dv, workspace=ws, dev_err=err, phases=(0,))
         mark(5)
-        ops.tree_attn_bwd(dplan, qr, kr, V, O, LSE, dO, dq=dq, dk=dk, dv=dv, workspace=ws, dev_err=err, phases=(2,))
+        ops.tree_attn_bwd(dplan, qr, kr, V, O, LSE, dO, dq=dq, dk=dk, dv=dv, workspace=ws, dev_err=err, phases=(1,))
         mark(6)
-        ops.rope_by_depth(dq, dk, dplan.depth, w.rope_base, inverse=True)
+        ops.tree_attn_bwd(dplan, qr, kr, V, O, LSE, dO, dq=dq, dk=dk, dv=dv, workspace=ws, dev_err=err, phases=(2,))
         mark(7)
+        ops.rope_by_depth(dq, dk, dplan.depth, w.rope_base, inverse=True)
+        mark(8)
 
     def barrier():
         if world > 1:
@@ -339,7 +348,7 @@ def run_ours(a):
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise SystemExit("device wait timed out (TPK_E_TIMEOUT)")
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(a.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(a.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = Clocks(local)
     barrier()
@@ -364,8 +373,8 @@ def run_ours(a):
     if a.e2e_steps > 0:
         tokens = np.concatenate(w.sequences).astype(np.int32)
         offs = w.seq_offsets()
-        hQ, hK, hV, hdO = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (Q, K, V, dO))
-        for h, x in zip((hQ, hK, hV, hdO), (Q, K, V, dO)):
+        hQ, hK, hV, hdO = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (Q, K, V, dO_raw))
+        for h, x in zip((hQ, hK, hV, hdO), (Q, K, V, dO_raw)):
             h.copy_(x)
         hLSE = torch.empty((Hq, R), dtype=torch.float32).pin_memory()
         h2d = sum(x.numel() * x.element_size() for x in (hQ, hK, hV, hdO)) + plan.device_bytes()
@@ -386,7 +395,7 @@ def run_ours(a):
                 ready["qk"].record()
                 V.copy_(hV, non_blocking=True)
                 ready["v"].record()
-                dO.copy_(hdO, non_blocking=True)
+                dO_raw.copy_(hdO, non_blocking=True)
                 ready["do"].record()
             p2 = ops.Plan(tokens, offs, group_ids=w.group_ids, row_capacity=w.row_capacity, min_shared=w.min_shared)
             d2 = p2.to_device(dev)
@@ -406,7 +415,7 @@ def run_ours(a):
         dt = max_over_ranks(dt, dev, world)
         e2e = {"value": job_value(world, R, dt), "unit": "raw tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": 1e3 * dt,
-               "includes": "plan build on host, plan image + Q/K/V/dO host->device, full step, "
+               "includes": "plan build on host, plan image + Q/K/V + raw-order dO host->device, full step, "
                            "raw-order LSE device->host; uploads on a copy stream in first-use order, "
                            "overlapping the host plan build and the forward; one step at a time "
                            "(synchronised at the end of every step)"}
@@ -432,6 +441,7 @@ def run_ours(a):
         "rope": ("hbm", F * (Hq + Hkv) * d * 2 * 2 + 4 * F),
         "rope_inv": ("hbm", F * (Hq + Hkv) * d * 2 * 2 + 4 * F),
         "scatter": ("hbm", R * Hq * (2 * d + 4) * 2 + 4 * R),
+        "dO_sum": ("hbm", (R + F) * Hq * d * 2 + 4 * (F + 1) + 4 * R),
         "bwd_prep": ("hbm", F * Hq * d * 2 * 2 + 4 * F * Hq),
     }
     dom = max(per, key=per.get)
@@ -544,10 +554,62 @@ def run_sweep(a):
         }), flush=True)
 
 
+def run_layout(a):
+    """Raw order <-> packed layout kernels on one workload (default: the deep
+    tree): materialisation of a per-token payload by owner (int32 token ids,
+    and rows of Hq*d bf16) and the sum of raw-order rows into the packed
+    layout.  L2 flushed before every timed launch; one JSON line."""
+    import torch
+    import workloads
+    from prefix_tree_packed_dfs_gb300 import ops
+    from workloads import rng as wrng
+    peaks = _peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    w = workloads.get(a.workload)
+    plan = ops.Plan.from_sequences(w.sequences, group_ids=w.group_ids, row_capacity=w.row_capacity,
+                                   min_shared=w.min_shared)
+    dp = plan.to_device()
+    F, R, Hq, d = plan.info["n_fwd"], plan.info["n_raw"], w.n_heads_q, w.head_dim
+    tokens = torch.from_numpy(np.concatenate(w.sequences).astype(np.int32)).cuda()
+    rows = wrng.normal_bf16(w.seeds["do"], (R, Hq, d), "cuda")
+    tok_f = torch.empty(F, dtype=torch.int32, device="cuda")
+    rows_f = torch.empty((F, Hq, d), dtype=torch.bfloat16, device="cuda")
+
+    def timed(fn):
+        for _ in range(a.warmup):
+            fn()
+        times = []
+        for _ in range(max(a.steps, 3)):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    idx = 4 * (F + 1) + 4 * F   # CSR begin + one raw index per position
+    out = {}
+    for name, fn, nbytes in (
+            ("gather_token_ids", lambda: ops.gather_to_forwarded(dp, tokens, dst=tok_f), 8 * F + idx),
+            ("gather_rows_bf16", lambda: ops.gather_to_forwarded(dp, rows, dst=rows_f), 2 * F * Hq * d * 2 + idx),
+            ("sum_rows_bf16", lambda: ops.sum_to_forwarded(dp, rows, dst=rows_f), (R + F) * Hq * d * 2 + 4 * (F + 1 + R))):
+        ms = timed(fn)
+        out[name] = {"ms": ms, "gbs": nbytes / ms / 1e6, "frac_of_copy_peak": nbytes / ms / 1e6 / peaks["hbm_gbs"],
+                     "algorithmic_bytes": nbytes}
+    print(json.dumps({"mode": "layout", "workload": a.workload, "raw_tokens": R, "forwarded_tokens": F,
+                      "row_bytes": Hq * d * 2, "kernels": out, "peak_gbs": peaks["hbm_gbs"],
+                      "peak_kind": "copy bandwidth (%s)" % peaks["source"],
+                      "l2": "flushed (256 MiB write) before every timed launch"}), flush=True)
+
+
 def main():
     a = _args()
     if a.sweep:
         run_sweep(a)
+    elif a.layout:
+        run_layout(a)
     elif a.impl == "reference":
         run_reference(a)
     else:

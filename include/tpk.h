@@ -159,6 +159,15 @@ int tpk_plan_worklists(const tpk_plan* plan, int32_t* qt_q0, int32_t* qt_nq,
                        int32_t* kt_k0, int32_t* kt_nk, int32_t* kt_qb_begin,
                        int32_t* qb, int32_t* kt_order);
 
+/* Raw tokens of each forwarded position: token_index read the other way, as
+ * a CSR (int32 host copies; either pointer may be NULL).
+ * fwd_raw[fwd_raw_begin[f] .. fwd_raw_begin[f+1]) lists, ascending, the raw
+ * tokens that map to forwarded position f; the first is fwd_src[f], its owner.
+ * fwd_raw_begin has F+1 entries, fwd_raw R.  The device image holds the same
+ * arrays (TPK_FIELD_FWD_RAW_BEGIN, TPK_FIELD_FWD_RAW) for
+ * tpk_gather_to_forwarded and tpk_sum_to_forwarded. */
+int tpk_plan_raw_of_forwarded(const tpk_plan* plan, int32_t* fwd_raw_begin, int32_t* fwd_raw);
+
 /* Device image of the plan.  The caller allocates tpk_plan_device_bytes()
  * bytes of device memory (256-byte aligned) and uploads the image with
  * tpk_plan_upload (async on `stream`; the plan keeps the host image alive until
@@ -168,6 +177,8 @@ int tpk_plan_worklists(const tpk_plan* plan, int32_t* qt_q0, int32_t* qt_nq,
 #define TPK_FIELD_TOKEN_INDEX  1   /* int32 [R] */
 #define TPK_FIELD_SUBTREE_END  2   /* int32 [F] */
 #define TPK_FIELD_PARENT       3   /* int32 [F] */
+#define TPK_FIELD_FWD_RAW_BEGIN 4  /* int32 [F+1] */
+#define TPK_FIELD_FWD_RAW      5   /* int32 [R] */
 size_t tpk_plan_device_bytes(const tpk_plan* plan);
 int tpk_plan_field_offset(const tpk_plan* plan, int32_t field, size_t* offset);
 int tpk_plan_upload(const tpk_plan* plan, void* dev_image, void* stream);
@@ -273,6 +284,38 @@ int tpk_tree_attn_bwd_noalloc(const tpk_plan* plan, const void* dev_image,
 int tpk_scatter_token_index(const int32_t* token_index, int64_t R, int64_t F,
                             const void* src, void* dst, const float* lse_src,
                             float* lse_dst, int32_t H, int32_t d, void* stream);
+
+/* Materialisation of per-token data into the packed layout ([ART] "Metadata
+ * space first": once the plan is fixed, one pass slices token ids, logprobs,
+ * advantages and other per-token payloads into the packed tensors).  Every
+ * forwarded position takes the row of its owner, the lowest raw token that
+ * maps to it (fwd_raw[fwd_raw_begin[f]], = fwd_src[f]):
+ *   dst[f, :] = src[fwd_src[f], :]      src [R, row_bytes] -> dst [F, row_bytes]
+ * Rows are opaque bytes (any element type); row_bytes >= 1.  Merged raw
+ * tokens carry the same token and target, so for payloads that are functions
+ * of (prefix, target) -- token ids, reference logprobs -- every raw token of
+ * a position holds the owner's value.  fwd_raw_begin / fwd_raw: device
+ * pointers into the plan image (TPK_FIELD_FWD_RAW_BEGIN / _FWD_RAW).
+ * src/dst are device buffers that must not overlap.  Returns TPK_E_ARG on a
+ * NULL pointer or negative size, TPK_E_CUDA on a launch error. */
+int tpk_gather_to_forwarded(const int32_t* fwd_raw_begin, const int32_t* fwd_raw, int64_t F, int64_t R,
+                            const void* src, void* dst, int64_t row_bytes, void* stream);
+
+/* Adjoint of tpk_scatter_token_index: per-raw-token quantities summed into
+ * the forwarded position every raw token maps to (no counterpart on the pages
+ * beyond [TRL]'s token_index; it is the transpose of that gather, which is how
+ * raw-order output gradients -- and per-token loss weights such as
+ * advantages -- reach the packed layout):
+ *   dst[f]        = sum over r with token_index[r] = f of src[r]      [R,H,d] -> [F,H,d] bf16
+ *   lse_dst[h, f] = sum over the same r of lse_src[h, r]               [H,R]  -> [H,F]  fp32
+ * Sums run in fp32 over the raw tokens in ascending order (deterministic),
+ * then round to bf16 (RNE) for dst.  A per-token fp32 weight [R] is the lse
+ * pair with H = 1.  src/dst may both be NULL; lse_src/lse_dst may both be
+ * NULL.  H*d*2 must be a multiple of 16 and src/dst 16-byte aligned
+ * (TPK_E_ARG otherwise). */
+int tpk_sum_to_forwarded(const int32_t* fwd_raw_begin, const int32_t* fwd_raw, int64_t F, int64_t R,
+                         const void* src, void* dst, const float* lse_src, float* lse_dst,
+                         int32_t H, int32_t d, void* stream);
 
 /* Self-test of the device-side failure path (no counterpart on the pages):
  * launches one small kernel that waits, with the same bounded mbarrier wait

@@ -24,6 +24,12 @@ Contents
                0..L-1, ordinary causal softmax attention in fp64 ("DAG
                packing", section "The mask"; "Prefix Tree Packing in ART",
                section "Token-mixing layers"), and its backward.
+``layout``     per-token data between raw order and the packed layout: the
+               materialisation gather by owner ("Prefix Tree Packing in ART",
+               section "Metadata space first"), the raw-order scatter through
+               token_index and its transpose, the sum over a position's raw
+               tokens ("TRL Tree Packing for AsyncGRPO", section "How tree
+               packing works").
 ``bf16``       round-to-nearest-even rounding of fp64 values to bfloat16.
 
 Every function is pinned by a ``-m "not gpu"`` test against values the pages

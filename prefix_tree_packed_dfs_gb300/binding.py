@@ -19,14 +19,16 @@ BWD_PREP, BWD_DKDV, BWD_DQ = 0, 1, 2
 PLACE_BFD = 0
 PLACE_NEXT_FIT = 1
 FIELD_DEPTH, FIELD_TOKEN_INDEX, FIELD_SUBTREE_END, FIELD_PARENT = 0, 1, 2, 3
+FIELD_FWD_RAW_BEGIN, FIELD_FWD_RAW = 4, 5
 
 # every symbol include/tpk.h declares
 EXPORTS = [
-    "tpk_plan_build", "tpk_plan_info_get", "tpk_plan_export", "tpk_plan_worklists",
+    "tpk_plan_build", "tpk_plan_info_get", "tpk_plan_export", "tpk_plan_worklists", "tpk_plan_raw_of_forwarded",
     "tpk_plan_device_bytes", "tpk_plan_field_offset", "tpk_plan_upload", "tpk_plan_destroy",
     "tpk_rope_by_depth", "tpk_attn_workspace_bytes", "tpk_tree_attn_fwd", "tpk_tree_attn_bwd",
     "tpk_tree_attn_bwd_phase", "tpk_tree_attn_bwd_noalloc", "tpk_selftest_wait_timeout",
-    "tpk_scatter_token_index", "tpk_status_string", "tpk_version",
+    "tpk_scatter_token_index", "tpk_gather_to_forwarded", "tpk_sum_to_forwarded", "tpk_status_string",
+    "tpk_version",
 ]
 
 
@@ -62,6 +64,7 @@ def _sig(lib):
     lib.tpk_plan_info_get.argtypes = [P, ctypes.POINTER(PlanInfo)]
     lib.tpk_plan_export.argtypes = [P] * 10
     lib.tpk_plan_worklists.argtypes = [P] * 11
+    lib.tpk_plan_raw_of_forwarded.argtypes = [P, P, P]
     lib.tpk_plan_device_bytes.argtypes = [P]
     lib.tpk_plan_device_bytes.restype = SZ
     lib.tpk_plan_field_offset.argtypes = [P, I32, ctypes.POINTER(SZ)]
@@ -77,6 +80,8 @@ def _sig(lib):
     lib.tpk_tree_attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, ctypes.c_float, P, P]
     lib.tpk_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P, P]
     lib.tpk_scatter_token_index.argtypes = [P, I64, I64, P, P, P, P, I32, I32, P]
+    lib.tpk_gather_to_forwarded.argtypes = [P, P, I64, I64, P, P, I64, P]
+    lib.tpk_sum_to_forwarded.argtypes = [P, P, I64, I64, P, P, P, P, I32, I32, P]
     lib.tpk_status_string.argtypes = [ctypes.c_int]
     lib.tpk_status_string.restype = ctypes.c_char_p
     lib.tpk_version.argtypes = []

@@ -103,6 +103,13 @@ int tpk_plan_worklists(const tpk_plan* plan, int32_t* qt_q0, int32_t* qt_nq,
   return TPK_OK;
 }
 
+int tpk_plan_raw_of_forwarded(const tpk_plan* plan, int32_t* fwd_raw_begin, int32_t* fwd_raw) {
+  if (!plan) return TPK_E_ARG;
+  copy_out(fwd_raw_begin, plan->p.fwd_raw_begin);
+  copy_out(fwd_raw, plan->p.fwd_raw);
+  return TPK_OK;
+}
+
 size_t tpk_plan_device_bytes(const tpk_plan* plan) { return plan ? plan->p.image.size() : 0; }
 
 int tpk_plan_field_offset(const tpk_plan* plan, int32_t field, size_t* offset) {
@@ -112,6 +119,8 @@ int tpk_plan_field_offset(const tpk_plan* plan, int32_t field, size_t* offset) {
     case TPK_FIELD_TOKEN_INDEX: *offset = plan->p.off_token_index; return TPK_OK;
     case TPK_FIELD_SUBTREE_END: *offset = plan->p.off_subtree_end; return TPK_OK;
     case TPK_FIELD_PARENT: *offset = plan->p.off_parent; return TPK_OK;
+    case TPK_FIELD_FWD_RAW_BEGIN: *offset = plan->p.off_fwd_raw_begin; return TPK_OK;
+    case TPK_FIELD_FWD_RAW: *offset = plan->p.off_fwd_raw; return TPK_OK;
     default: return TPK_E_ARG;
   }
 }

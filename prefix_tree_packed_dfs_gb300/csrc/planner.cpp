@@ -411,6 +411,16 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   P.qt_order = launch_order(P.qt_kb_begin);
   P.kt_order = launch_order(P.kt_qb_begin);
 
+  // ---- raw tokens of each forwarded position (counting sort of token_index) --
+  P.fwd_raw_begin.assign(static_cast<size_t>(P.F) + 1, 0);
+  for (int32_t f : P.token_index) ++P.fwd_raw_begin[static_cast<size_t>(f) + 1];
+  for (int64_t f = 0; f < P.F; ++f) P.fwd_raw_begin[f + 1] += P.fwd_raw_begin[f];
+  P.fwd_raw.assign(P.token_index.size(), 0);
+  {
+    std::vector<int32_t> fill(P.fwd_raw_begin.begin(), P.fwd_raw_begin.end() - 1);
+    for (size_t r = 0; r < P.token_index.size(); ++r) P.fwd_raw[fill[P.token_index[r]]++] = static_cast<int32_t>(r);
+  }
+
   // ---- device image -------------------------------------------------------
   size_t off = 0;
   auto place = [&](size_t& field, size_t bytes) { field = off; off = align256(off + bytes); };
@@ -418,6 +428,8 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   place(P.off_token_index, 4 * P.token_index.size());
   place(P.off_subtree_end, 4 * P.subtree_end.size());
   place(P.off_parent, 4 * P.parent.size());
+  place(P.off_fwd_raw_begin, 4 * P.fwd_raw_begin.size());
+  place(P.off_fwd_raw, 4 * P.fwd_raw.size());
   place(P.off_qt_q0, 4 * P.qt_q0.size());
   place(P.off_qt_nq, 4 * P.qt_nq.size());
   place(P.off_qt_kb_begin, 4 * P.qt_kb_begin.size());
@@ -436,6 +448,8 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   put(P.off_token_index, P.token_index);
   put(P.off_subtree_end, P.subtree_end);
   put(P.off_parent, P.parent);
+  put(P.off_fwd_raw_begin, P.fwd_raw_begin);
+  put(P.off_fwd_raw, P.fwd_raw);
   put(P.off_qt_q0, P.qt_q0);
   put(P.off_qt_nq, P.qt_nq);
   put(P.off_qt_kb_begin, P.qt_kb_begin);

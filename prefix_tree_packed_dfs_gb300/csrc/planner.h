@@ -27,6 +27,9 @@ struct Plan {
   // layout
   std::vector<int64_t> row_offsets, row_loads;
   std::vector<int32_t> row_of_seq, fwd_token, fwd_src, parent, depth, token_index, subtree_end;
+  // raw tokens of each forwarded position (the inverse of token_index, CSR):
+  // fwd_raw[fwd_raw_begin[f] .. fwd_raw_begin[f+1]) ascending, first = fwd_src[f]
+  std::vector<int32_t> fwd_raw_begin, fwd_raw;
 
   // forward work list: query tiles and their key blocks
   std::vector<int32_t> qt_q0, qt_nq, qt_kb_begin, kb, qt_order;
@@ -36,6 +39,7 @@ struct Plan {
   // device image: every array above that a kernel reads, 256-byte aligned sections
   std::vector<uint8_t> image;
   size_t off_depth = 0, off_token_index = 0, off_subtree_end = 0, off_parent = 0;
+  size_t off_fwd_raw_begin = 0, off_fwd_raw = 0;
   size_t off_qt_q0 = 0, off_qt_nq = 0, off_qt_kb_begin = 0, off_kb = 0, off_qt_order = 0;
   size_t off_kt_k0 = 0, off_kt_nk = 0, off_kt_qb_begin = 0, off_qb = 0, off_kt_order = 0;
 };

@@ -110,6 +110,14 @@ class Plan:
         B.check(self._lib.tpk_plan_worklists(self._h, *[out[k].ctypes.data for k in order]), "tpk_plan_worklists")
         return out
 
+    def raw_of_forwarded(self):
+        """(fwd_raw_begin [F+1], fwd_raw [R]): the raw tokens of each forwarded position, ascending."""
+        F, R = self.info["n_fwd"], self.info["n_raw"]
+        begin, raw = np.zeros(F + 1, np.int32), np.zeros(R, np.int32)
+        B.check(self._lib.tpk_plan_raw_of_forwarded(self._h, begin.ctypes.data, raw.ctypes.data),
+                "tpk_plan_raw_of_forwarded")
+        return begin, raw
+
     def device_bytes(self):
         return int(self._lib.tpk_plan_device_bytes(self._h))
 
@@ -148,6 +156,8 @@ class DevicePlan:
         self.token_index = self._field(B.FIELD_TOKEN_INDEX, R)
         self.subtree_end = self._field(B.FIELD_SUBTREE_END, F)
         self.parent = self._field(B.FIELD_PARENT, F)
+        self.fwd_raw_begin = self._field(B.FIELD_FWD_RAW_BEGIN, F + 1)
+        self.fwd_raw = self._field(B.FIELD_FWD_RAW, R)
 
     def _field(self, field, n):
         off = self.plan.field_offset(field)
@@ -265,4 +275,54 @@ def scatter_token_index(token_index, src=None, lse_src=None, dst=None, lse_dst=N
     d = src.shape[2] if src is not None else 8
     B.check(lib.tpk_scatter_token_index(_ptr(token_index), R, F, _ptr(src), _ptr(dst), _ptr(lse_src),
                                         _ptr(lse_dst), H, d, _stream()), "tpk_scatter_token_index")
+    return dst, lse_dst
+
+
+def gather_to_forwarded(dplan, src, dst=None):
+    """Packed-layout copy of a per-raw-token payload: dst[f] = src[owner of f].
+
+    ``src`` is any contiguous device tensor whose first dimension is the raw
+    token (R); every forwarded position takes its owner's row (the lowest
+    raw token mapping to it)."""
+    lib = B.load()
+    R, F = dplan.n_raw, dplan.n_fwd
+    if not src.is_cuda or not src.is_contiguous() or src.shape[0] != R:
+        raise ValueError("src must be a contiguous device tensor with %d rows" % R)
+    if dst is None:
+        dst = torch.empty((F,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+    if dst.dtype != src.dtype or tuple(dst.shape) != (F,) + tuple(src.shape[1:]) or not dst.is_contiguous():
+        raise ValueError("dst must be a contiguous %s tensor of shape %s" % (src.dtype, (F,) + tuple(src.shape[1:])))
+    row_bytes = src[0].numel() * src.element_size() if R else 1
+    B.check(lib.tpk_gather_to_forwarded(_ptr(dplan.fwd_raw_begin), _ptr(dplan.fwd_raw), F, R, _ptr(src), _ptr(dst),
+                                        row_bytes, _stream()), "tpk_gather_to_forwarded")
+    return dst
+
+
+def sum_to_forwarded(dplan, src=None, lse_src=None, dst=None, lse_dst=None):
+    """Adjoint of the raw-order scatter: dst[f] = sum of src[r] over the raw tokens r of f.
+
+    ``src`` [R, H, d] bf16 -> [F, H, d] bf16; ``lse_src`` [H, R] fp32 -> [H, F]
+    (a per-token fp32 weight is the case H = 1).  fp32 sums in ascending raw
+    order."""
+    lib = B.load()
+    R, F = dplan.n_raw, dplan.n_fwd
+    H, d = 1, 8
+    if src is not None:
+        _need(src, torch.bfloat16, "src", 3)
+        if src.shape[0] != R:
+            raise ValueError("src must have %d rows" % R)
+        _, H, d = src.shape
+        if dst is None:
+            dst = torch.empty((F, H, d), dtype=src.dtype, device=src.device)
+    if lse_src is not None:
+        _need(lse_src, torch.float32, "lse_src", 2)
+        if lse_src.shape[1] != R or (src is not None and lse_src.shape[0] != H):
+            raise ValueError("lse_src must be [H, %d]" % R)
+        H = lse_src.shape[0]
+        if lse_dst is None:
+            lse_dst = torch.empty((H, F), dtype=torch.float32, device=lse_src.device)
+    if src is None and lse_src is None:
+        return None, None
+    B.check(lib.tpk_sum_to_forwarded(_ptr(dplan.fwd_raw_begin), _ptr(dplan.fwd_raw), F, R, _ptr(src), _ptr(dst),
+                                     _ptr(lse_src), _ptr(lse_dst), H, d, _stream()), "tpk_sum_to_forwarded")
     return dst, lse_dst

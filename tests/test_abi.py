@@ -54,3 +54,14 @@ def test_gpu_entry_points_reject_bad_arguments_before_any_device_call(lib):
     assert lib.tpk_scatter_token_index(None, 1, 1, None, None, None, None, 1, 64, None) == -1
     # empty work is a no-op that never touches the device
     assert lib.tpk_scatter_token_index(ctypes.c_void_p(16), 0, 0, None, None, None, None, 1, 64, None) == 0
+    # materialisation gather and its transpose: NULL pointers, negative or
+    # inconsistent sizes and misaligned rows are host-side errors
+    P = ctypes.c_void_p
+    assert lib.tpk_gather_to_forwarded(None, P(16), 1, 1, P(16), P(16), 4, None) == -1
+    assert lib.tpk_gather_to_forwarded(P(16), P(16), 2, 1, P(16), P(16), 4, None) == -1     # F > R
+    assert lib.tpk_gather_to_forwarded(P(16), P(16), 1, 1, P(16), P(16), 0, None) == -1     # empty rows
+    assert lib.tpk_gather_to_forwarded(P(16), P(16), 0, 0, P(16), P(16), 4, None) == 0      # no work
+    assert lib.tpk_sum_to_forwarded(P(16), P(16), 1, 1, P(16), None, None, None, 1, 64, None) == -1
+    assert lib.tpk_sum_to_forwarded(P(16), P(16), 1, 1, P(16), P(16), None, None, 1, 60, None) == -1  # H*d*2 % 16
+    assert lib.tpk_sum_to_forwarded(P(16), P(16), 1, 1, P(8), P(16), None, None, 1, 64, None) == -1   # alignment
+    assert lib.tpk_sum_to_forwarded(P(16), P(16), 0, 0, None, None, P(16), P(16), 1, 8, None) == 0

@@ -476,3 +476,37 @@ def test_backward_dv_sums_to_do_per_kv_head():
         lhs = dV[:, g, :].sum(axis=0)
         rhs = dO[:, g * G:(g + 1) * G, :].sum(axis=(0, 1))
         assert np.allclose(lhs, rhs, rtol=1e-12, atol=1e-10)
+
+
+# ------------------------------------------------- raw order <-> packed layout
+@pytest.mark.parametrize("seed", range(6))
+def test_sum_to_forwarded_is_the_transpose_of_the_scatter(seed):
+    # <scatter(x), y> over raw tokens equals <x, sum_to_forwarded(y)> over
+    # forwarded positions for every x, y: the defining property of a transpose
+    from oracle import layout as ol
+    rng = np.random.Generator(np.random.PCG64(400 + seed))
+    seqs = [rng.integers(0, 3, size=int(rng.integers(1, 40))) for _ in range(int(rng.integers(2, 9)))]
+    p = op.plan(seqs, min_shared=int(rng.choice([1, 4])), row_capacity=400)
+    F, R = p["n_fwd"], p["n_raw"]
+    x = rng.standard_normal((F, 3, 4))
+    y = rng.standard_normal((R, 3, 4))
+    lhs = np.sum(ol.scatter_to_raw(p, x) * y)
+    rhs = np.sum(x * ol.sum_to_forwarded(p, y))
+    assert abs(lhs - rhs) <= 1e-10 * max(1.0, abs(lhs))
+    # unit vectors: a raw token's weight lands on its own position only
+    e = np.zeros((R, 1))
+    r = int(rng.integers(0, R))
+    e[r] = 1.0
+    s = ol.sum_to_forwarded(p, e)
+    assert s[p["token_index"][r], 0] == 1.0 and s.sum() == 1.0
+
+
+def test_gather_to_forwarded_reproduces_the_packed_tokens():
+    # token ids gathered by owner are the planner's forwarded tokens, and
+    # every raw token of a position carries that position's token
+    from oracle import layout as ol
+    seqs, p, _, _, _ = _tiny_tree(5, hq=1, hkv=1, d=8)
+    tokens = np.concatenate(seqs).astype(np.int32)
+    g = ol.gather_to_forwarded(p, tokens)
+    assert np.array_equal(g, np.asarray(p["fwd_token"]))
+    assert np.array_equal(g[p["token_index"]], tokens)

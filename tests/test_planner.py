@@ -199,3 +199,19 @@ def test_launch_order_runs_longest_first(lib, name):
     wl = got.worklists()
     _check_launch_order(list(wl["qt_order"]), wl["qt_kb_begin"])
     _check_launch_order(list(wl["kt_order"]), wl["kt_qb_begin"])
+
+
+@pytest.mark.parametrize("name", ["tiny", "grpo", "deep_small", "sweep_1.00"])
+def test_raw_of_forwarded_is_token_index_inverted(lib, name):
+    # the CSR of raw tokens per forwarded position, built from the oracle's
+    # token_index: stable order of raw tokens by position, first = owner
+    w = workloads.get(name)
+    ref = op.plan(w.sequences, group_ids=w.group_ids, min_shared=w.min_shared, row_capacity=w.row_capacity)
+    got = _cpp_plan(w.sequences, groups=w.group_ids, min_shared=w.min_shared, cap=w.row_capacity)
+    begin, raw = got.raw_of_forwarded()
+    ti = np.asarray(ref["token_index"])
+    exp_begin = np.concatenate([[0], np.cumsum(np.bincount(ti, minlength=ref["n_fwd"]))]).astype(np.int32)
+    exp_raw = np.argsort(ti, kind="stable").astype(np.int32)
+    assert np.array_equal(begin, exp_begin)
+    assert np.array_equal(raw, exp_raw)
+    assert np.array_equal(raw[begin[:-1]], np.asarray(ref["fwd_src"]))
