@@ -79,7 +79,7 @@ def _args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
-    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layout", action="store_true",
@@ -384,21 +384,23 @@ def run_ours(a):
 
         def e2e_step():
             # this step's inputs go up on a copy stream in the order the
-            # kernels first read them (Q, K for RoPE, V for the forward, dO
-            # for the backward) while the host builds the plan; each kernel
-            # waits only for what it reads, and the raw-order LSE comes back
-            # on the copy stream while the backward runs
+            # kernels first read them (Q, K and the plan image for RoPE, V for
+            # the forward, dO for the backward); the host builds the plan while
+            # Q and K are in flight; each kernel waits only for what it reads,
+            # and the raw-order LSE comes back on the copy stream while the
+            # backward runs
             ready = {k: torch.cuda.Event() for k in ("qk", "v", "do", "out")}
             with torch.cuda.stream(copy_stream):
                 Q.copy_(hQ, non_blocking=True)
                 K.copy_(hK, non_blocking=True)
+            p2 = ops.Plan(tokens, offs, group_ids=w.group_ids, row_capacity=w.row_capacity, min_shared=w.min_shared)
+            with torch.cuda.stream(copy_stream):
+                d2 = p2.to_device(dev)   # the plan image right behind Q, K on the copy stream
                 ready["qk"].record()
                 V.copy_(hV, non_blocking=True)
                 ready["v"].record()
                 dO_raw.copy_(hdO, non_blocking=True)
                 ready["do"].record()
-            p2 = ops.Plan(tokens, offs, group_ids=w.group_ids, row_capacity=w.row_capacity, min_shared=w.min_shared)
-            d2 = p2.to_device(dev)
             step(d2, ready=ready)
             with torch.cuda.stream(copy_stream):
                 copy_stream.wait_event(ready["out"])

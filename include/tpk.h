@@ -171,7 +171,12 @@ int tpk_plan_raw_of_forwarded(const tpk_plan* plan, int32_t* fwd_raw_begin, int3
 /* Device image of the plan.  The caller allocates tpk_plan_device_bytes()
  * bytes of device memory (256-byte aligned) and uploads the image with
  * tpk_plan_upload (async on `stream`; the plan keeps the host image alive until
- * destroyed).  tpk_plan_field_offset gives the byte offset of a field inside
+ * destroyed, so keep the plan until the copy has completed).  The first upload
+ * copies the image once into page-locked host memory owned by the plan, so
+ * every upload is an asynchronous DMA; tpk_plan_destroy frees it (and may
+ * wait for the device to do so).  If page-locked memory cannot be had, the
+ * upload copies from pageable memory (same bytes, not asynchronous).
+ * tpk_plan_field_offset gives the byte offset of a field inside
  * the image so callers can pass e.g. depth or token_index to the kernels. */
 #define TPK_FIELD_DEPTH        0   /* int32 [F] */
 #define TPK_FIELD_TOKEN_INDEX  1   /* int32 [R] */

@@ -130,7 +130,21 @@ int tpk_plan_upload(const tpk_plan* plan, void* dev_image, void* stream) {
   if (reinterpret_cast<uintptr_t>(dev_image) % 256) return TPK_E_ARG;
   const auto& img = plan->p.image;
   if (img.empty()) return TPK_OK;
-  cudaError_t e = cudaMemcpyAsync(dev_image, img.data(), img.size(), cudaMemcpyHostToDevice,
+  const void* src = img.data();
+  {
+    std::lock_guard<std::mutex> lock(plan->pinned_mu);
+    if (!plan->pinned) {
+      void* h = nullptr;
+      if (cudaMallocHost(&h, img.size()) == cudaSuccess) {
+        std::memcpy(h, img.data(), img.size());
+        plan->pinned = h;
+      } else {
+        (void)cudaGetLastError();   // no page-locked memory: copy from the pageable image
+      }
+    }
+    if (plan->pinned) src = plan->pinned;
+  }
+  cudaError_t e = cudaMemcpyAsync(dev_image, src, img.size(), cudaMemcpyHostToDevice,
                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TPK_OK : TPK_E_CUDA;
 }
