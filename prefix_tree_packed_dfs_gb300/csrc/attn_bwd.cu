@@ -62,24 +62,34 @@ struct BwdParams {
 };
 
 // ----------------------------------------------------------------- pass 1
+// D[h, f] = dO[f, h, :] . O[f, h, :] in fp32.  A row of D bf16 is D/8
+// 16-byte chunks; that many lanes share a row (two rows per warp at D = 128,
+// four at D = 64) and add their partial dots with shuffles inside the group.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dout,
                                                        float* __restrict__ dsum, int64_t F, int Hq, int D) {
   const int lane = threadIdx.x & 31;
+  const int lpr = D / 8;            // lanes per row
+  const int rpw = 32 / lpr;         // rows per warp step
+  const int sub = lane / lpr, cl = lane % lpr;
   const int64_t n = F * Hq;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < n; w += nwarps) {
-    const int64_t f = w / Hq, h = w % Hq;
-    const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(o + w * D);
-    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(dout + w * D);
+  for (int64_t w0 = (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * rpw; w0 < n;
+       w0 += nwarps * rpw) {
+    const int64_t w = w0 + sub;
     float acc = 0.f;
-    for (int c = lane; c < D / 2; c += 32) {
-      const float2 x = __bfloat1622float2(a[c]), y = __bfloat1622float2(b[c]);
-      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
-    }
+    if (w < n) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + w * D) + cl);
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(dout + w * D) + cl);
+      const uint32_t x[4] = {a.x, a.y, a.z, a.w}, y[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) dsum[h * F + f] = acc;
+      for (int j = 0; j < 4; ++j) {
+        acc = fmaf(__uint_as_float(x[j] << 16), __uint_as_float(y[j] << 16), acc);
+        acc = fmaf(__uint_as_float(x[j] & 0xFFFF0000u), __uint_as_float(y[j] & 0xFFFF0000u), acc);
+      }
+    }
+    for (int off = lpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (cl == 0 && w < n) dsum[(w % Hq) * F + w / Hq] = acc;
   }
 }
 
@@ -783,8 +793,8 @@ extern "C" int tpk_tree_attn_bwd_phase(int32_t phase, const tpk_plan* plan, cons
   if (st != TPK_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (phase == TPK_BWD_PREP) {
-    const int64_t warps = P.F * Hq;
-    int64_t blocks = (warps + 7) / 8;
+    const int64_t rows_per_block = 8 * (32 / (d / 8));   // 8 warps, 32/(d/8) rows each
+    int64_t blocks = (P.F * Hq + rows_per_block - 1) / rows_per_block;
     const int64_t cap = int64_t{num_sms()} * 32;
     if (blocks > cap) blocks = cap;
     bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
