@@ -173,8 +173,10 @@ int tpk_plan_raw_of_forwarded(const tpk_plan* plan, int32_t* fwd_raw_begin, int3
  * tpk_plan_upload (async on `stream`; the plan keeps the host image alive until
  * destroyed, so keep the plan until the copy has completed).  The first upload
  * copies the image once into page-locked host memory owned by the plan, so
- * every upload is an asynchronous DMA; tpk_plan_destroy frees it (and may
- * wait for the device to do so).  If page-locked memory cannot be had, the
+ * every upload is an asynchronous DMA.  tpk_plan_destroy hands that buffer
+ * to the next plan's upload instead of freeing it (the library keeps at most
+ * two such buffers per process: allocating and freeing page-locked memory
+ * costs more than the copy).  If page-locked memory cannot be had, the
  * upload copies from pageable memory (same bytes, not asynchronous).
  * tpk_plan_field_offset gives the byte offset of a field inside
  * the image so callers can pass e.g. depth or token_index to the kernels. */

@@ -3,11 +3,53 @@
 
 #include <cstring>
 #include <new>
+#include <utility>
+#include <vector>
 
 #include "plan_handle.h"
 #include "tpk.h"
 
 namespace {
+// Page-locked buffers of destroyed plans, kept for the next plans' uploads:
+// allocating and freeing page-locked memory costs far more than the copy, and
+// callers that plan every step would pay it every step.  At most two are kept.
+std::mutex g_pinned_mu;
+std::vector<std::pair<void*, size_t>> g_pinned_free;
+constexpr size_t kMaxFreePinned = 2;
+
+void* take_pinned(size_t bytes, size_t* got) {
+  std::lock_guard<std::mutex> lock(g_pinned_mu);
+  size_t best = g_pinned_free.size();
+  for (size_t i = 0; i < g_pinned_free.size(); ++i)
+    if (g_pinned_free[i].second >= bytes && (best == g_pinned_free.size() || g_pinned_free[i].second < g_pinned_free[best].second))
+      best = i;
+  if (best == g_pinned_free.size()) return nullptr;
+  void* p = g_pinned_free[best].first;
+  *got = g_pinned_free[best].second;
+  g_pinned_free.erase(g_pinned_free.begin() + static_cast<std::ptrdiff_t>(best));
+  return p;
+}
+
+void give_pinned(void* p, size_t bytes) {
+  void* drop = p;
+  {
+    std::lock_guard<std::mutex> lock(g_pinned_mu);
+    if (g_pinned_free.size() < kMaxFreePinned) {
+      g_pinned_free.push_back({p, bytes});
+      return;
+    }
+    // full: keep the larger buffers
+    size_t smallest = 0;
+    for (size_t i = 1; i < g_pinned_free.size(); ++i)
+      if (g_pinned_free[i].second < g_pinned_free[smallest].second) smallest = i;
+    if (g_pinned_free[smallest].second < bytes) {
+      drop = g_pinned_free[smallest].first;
+      g_pinned_free[smallest] = {p, bytes};
+    }
+  }
+  cudaFreeHost(drop);
+}
+
 template <typename T, typename U>
 void copy_out(T* dst, const std::vector<U>& v) {
   if (dst)
@@ -134,12 +176,20 @@ int tpk_plan_upload(const tpk_plan* plan, void* dev_image, void* stream) {
   {
     std::lock_guard<std::mutex> lock(plan->pinned_mu);
     if (!plan->pinned) {
-      void* h = nullptr;
-      if (cudaMallocHost(&h, img.size()) == cudaSuccess) {
+      size_t got = 0;
+      void* h = take_pinned(img.size(), &got);
+      if (!h) {
+        if (cudaMallocHost(&h, img.size()) == cudaSuccess) {
+          got = img.size();
+        } else {
+          h = nullptr;
+          (void)cudaGetLastError();   // no page-locked memory: copy from the pageable image
+        }
+      }
+      if (h) {
         std::memcpy(h, img.data(), img.size());
         plan->pinned = h;
-      } else {
-        (void)cudaGetLastError();   // no page-locked memory: copy from the pageable image
+        plan->pinned_bytes = got;
       }
     }
     if (plan->pinned) src = plan->pinned;
@@ -149,7 +199,14 @@ int tpk_plan_upload(const tpk_plan* plan, void* dev_image, void* stream) {
   return e == cudaSuccess ? TPK_OK : TPK_E_CUDA;
 }
 
-void tpk_plan_destroy(tpk_plan* plan) { delete plan; }
+void tpk_plan_destroy(tpk_plan* plan) {
+  if (!plan) return;
+  if (plan->pinned) {
+    give_pinned(plan->pinned, plan->pinned_bytes);
+    plan->pinned = nullptr;
+  }
+  delete plan;
+}
 
 const char* tpk_status_string(int status) {
   switch (status) {

@@ -12,6 +12,7 @@ struct tpk_plan {
   // every upload is an asynchronous DMA instead of a copy staged through
   // pageable memory (which queues behind other host-to-device traffic).
   mutable void* pinned = nullptr;
+  mutable size_t pinned_bytes = 0;
   mutable std::mutex pinned_mu;
 
   tpk_plan() = default;
