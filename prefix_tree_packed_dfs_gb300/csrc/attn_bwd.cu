@@ -110,7 +110,10 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
 //   MMA order per step n:  S/dP(n, half 0) | dV/dK(n-1, half 1) | S/dP(n, half 1) | dV/dK(n, half 0)
 // TMEM: slot h at [128h, 128h+128): S^T (64 cols) then dP^T (64 cols);
 // dV at [256, 256+D), dK at [256+D, 256+2D).  P^T and dS^T (bf16) overwrite
-// the first 32 columns of S^T and dP^T of their slot.
+// the first 32 columns of S^T and dP^T of their slot, in two 32-query parts
+// that the softmax releases one after the other (p_part, p_full) so the
+// first part's dV/dK products start early.  S^T and dP^T read K and V from
+// shared memory: the two slots and dK, dV fill TMEM.
 // Warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 2 loads LSE*log2(e) and D
 // of each step's 128 queries into shared memory, 4-7 softmax of half 0,
 // 8-11 softmax of half 1.
@@ -454,10 +457,12 @@ __global__ void __launch_bounds__(384, 1)
 // boxes), each released as soon as its half's dQ product is issued.
 // TMEM: slot h at [128h, 128h+128): S (64 cols) then dP (64 cols); dQ at
 // [256, 256+D); the query tile's Q and dO (bf16, D/2 cols each) after it.
-// dS (bf16) overwrites the first 32 columns of S of its slot.  Q and dO are
-// the A operands of the S and dP products straight from TMEM: shared memory
-// then only feeds the 64-key K / V halves (an A tile from shared memory as
-// well would need 6 KB per 32-cycle N=64 product, above the port's rate).
+// dS (bf16) overwrites the first 32 columns of S of its slot, released to
+// the dQ products in two 32-key parts (p_part, p_full).  Q and dO are the A
+// operands of the S and dP products straight from TMEM, so shared memory only
+// feeds the 64-key K / V halves: on this part an M=128, N=64 product took
+// about 75 cycles with its A tile in shared memory and 32-42 with it in TMEM
+// (the A tile read does not overlap the product).
 // Warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 4-7 softmax of half 0,
 // 8-11 softmax of half 1 (thread t owns query row t).
 template <int D, int NH>

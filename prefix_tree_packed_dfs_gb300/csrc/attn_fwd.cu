@@ -23,9 +23,12 @@
 //   warps 4..   one softmax warpgroup per head slot; thread t owns query row t
 // TMEM (512 columns): S_h at [128h, 128h+128) fp32, O_h at [128*HPC + D*h, +D).
 // P_h (bf16) is written over the first 64 columns of S_h and fed to the PV MMA
-// straight from TMEM.  The MMA thread interleaves the two head slots
+// straight from TMEM, in two 64-key halves: the softmax releases the first
+// half (p_half) before computing the second (p_full), so the first half's PV
+// products run meanwhile.  The MMA thread interleaves the two head slots
 // (PV_0(i-1), S_0(i), PV_1(i-1), S_1(i)) so one slot's softmax overlaps the
-// other slot's matrix products.
+// other slot's matrix products.  QK^T reads Q from shared memory: the four
+// S and O accumulators fill TMEM.
 // Online softmax with a lazily raised running maximum: O and the row sum are
 // rescaled only when the block maximum exceeds the one in use by more than
 // 2^8, which keeps exponentials <= 256 and skips almost every rescale.
