@@ -53,16 +53,21 @@ TRAFFIC = {"digest": "5e73321511a2481178556a853a594f42051a838efd665ebfccb441fca3
 
 
 def source_digest():
-    """sha256 over the library's sources (csrc/ and include/), in name order."""
+    """sha256 over the library's sources (csrc/ and include/), in name order,
+    with comments and whitespace removed: edits to comments leave it alone."""
     import hashlib
+    import re
     h = hashlib.sha256()
     dirs = [os.path.join(ROOT, "prefix_tree_packed_dfs_gb300", "csrc"), os.path.join(ROOT, "include")]
     for d in dirs:
         for name in sorted(os.listdir(d)):
             if name.endswith((".cu", ".cuh", ".cpp", ".h")):
+                with open(os.path.join(d, name)) as f:
+                    code = f.read()
+                code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
+                code = re.sub(r"//[^\n]*", " ", code)
                 h.update(name.encode())
-                with open(os.path.join(d, name), "rb") as f:
-                    h.update(f.read())
+                h.update(" ".join(code.split()).encode())
     return h.hexdigest()
 
 

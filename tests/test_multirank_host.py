@@ -57,3 +57,19 @@ def test_recorded_traffic_only_for_the_sources_it_was_taken_on(monkeypatch):
     assert bench.recorded_traffic("fwd", "deep_small") is None          # another workload
     monkeypatch.setattr(bench, "TRAFFIC", {"digest": "0" * 64, "fwd": 123, "bwd_dkdv": 456, "bwd_dq": 7})
     assert bench.recorded_traffic("bwd_dkdv", bench.WORKLOAD) is None   # sources changed since
+
+
+def test_source_digest_ignores_comments(tmp_path, monkeypatch):
+    import shutil
+    import bench
+    root = tmp_path / "r"
+    shutil.copytree(os.path.join(bench.ROOT, "prefix_tree_packed_dfs_gb300", "csrc"),
+                    root / "prefix_tree_packed_dfs_gb300" / "csrc")
+    shutil.copytree(os.path.join(bench.ROOT, "include"), root / "include")
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    d0 = bench.source_digest()
+    f = root / "prefix_tree_packed_dfs_gb300" / "csrc" / "scatter.cu"
+    f.write_text("// a new comment line\n" + f.read_text().replace("{", "{ /* inline */", 1))
+    assert bench.source_digest() == d0
+    f.write_text(f.read_text().replace("kThreads = 256", "kThreads = 128"))
+    assert bench.source_digest() != d0
