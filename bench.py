@@ -87,6 +87,8 @@ def _args():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--planner", action="store_true",
+                    help="host planner of the library vs the oracle's planner on every workload (no GPU)")
     ap.add_argument("--layout", action="store_true",
                     help="raw order <-> packed layout kernels (materialisation gather, sum of raw-order rows) "
                          "on --workload; one line")
@@ -617,9 +619,38 @@ def run_layout(a):
                       "l2": "flushed (256 MiB write) before every timed launch"}), flush=True)
 
 
+def run_planner(a):
+    """Host planner of the library against the oracle's planner, every
+    workload: median of three library builds, one oracle build.  No GPU."""
+    import workloads
+    from oracle import planner as op
+    from prefix_tree_packed_dfs_gb300 import ops
+    cores = _cpu_threads()
+    for name in workloads.ALL:
+        w = workloads.get(name)
+        times = []
+        for _ in range(3):
+            t0 = time.perf_counter()
+            plan = ops.Plan.from_sequences(w.sequences, group_ids=w.group_ids, row_capacity=w.row_capacity,
+                                           min_shared=w.min_shared)
+            times.append(time.perf_counter() - t0)
+        t0 = time.perf_counter()
+        op.plan(w.sequences, group_ids=w.group_ids, min_shared=w.min_shared, row_capacity=w.row_capacity)
+        t_or = time.perf_counter() - t0
+        info = plan.info
+        ms = 1e3 * statistics.median(times)
+        print(json.dumps({"mode": "planner", "workload": name, "raw_tokens": info["n_raw"],
+                          "forwarded_tokens": info["n_fwd"], "rows": info["n_rows"],
+                          "library_ms": ms, "oracle_ms": 1e3 * t_or, "oracle_over_library": t_or * 1e3 / ms,
+                          "library_raw_tokens_per_s": info["n_raw"] / ms * 1e3, "host_threads": cores,
+                          "library_threads": 1}), flush=True)
+
+
 def main():
     a = _args()
-    if a.sweep:
+    if a.planner:
+        run_planner(a)
+    elif a.sweep:
         run_sweep(a)
     elif a.layout:
         run_layout(a)
