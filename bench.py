@@ -389,19 +389,22 @@ def run_ours(a):
 
         copy_stream = torch.cuda.Stream(dev)
 
-        def e2e_step():
+        def build_plan():
+            return ops.Plan(tokens, offs, group_ids=w.group_ids, row_capacity=w.row_capacity,
+                            min_shared=w.min_shared)
+
+        def e2e_step(p2, held):
             # this step's inputs go up on a copy stream in the order the
             # kernels first read them (Q, K and the plan image for RoPE, V for
-            # the forward, dO for the backward); the host builds the plan while
-            # Q and K are in flight; each kernel waits only for what it reads,
-            # and the raw-order LSE comes back on the copy stream while the
-            # backward runs
+            # the forward, dO for the backward); each kernel waits only for
+            # what it reads, and the raw-order LSE comes back on the copy
+            # stream while the backward runs.  While the GPU works, the host
+            # builds the next step's plan and releases the previous step's,
+            # as a training loop prepares its next batch.
             ready = {k: torch.cuda.Event() for k in ("qk", "v", "do", "out")}
             with torch.cuda.stream(copy_stream):
                 Q.copy_(hQ, non_blocking=True)
                 K.copy_(hK, non_blocking=True)
-            p2 = ops.Plan(tokens, offs, group_ids=w.group_ids, row_capacity=w.row_capacity, min_shared=w.min_shared)
-            with torch.cuda.stream(copy_stream):
                 d2 = p2.to_device(dev)   # the plan image right behind Q, K on the copy stream
                 ready["qk"].record()
                 V.copy_(hV, non_blocking=True)
@@ -412,28 +415,32 @@ def run_ours(a):
             with torch.cuda.stream(copy_stream):
                 copy_stream.wait_event(ready["out"])
                 hLSE.copy_(LSE_raw, non_blocking=True)
+            nxt = build_plan()
+            held.clear()             # the previous step's plan and device image
             torch.cuda.synchronize()
-            return p2, d2
-        e2e_step()
+            held.append((p2, d2))
+            return nxt
+        held = []
+        nxt = e2e_step(build_plan(), held)
         barrier()
         per_step = []
         for _ in range(a.e2e_steps):
             t0 = time.perf_counter()
-            keep = e2e_step()
+            nxt = e2e_step(nxt, held)
             per_step.append(time.perf_counter() - t0)
         # the median step: host-to-device copies share the host with other
         # jobs on the machine, so single steps can be slow for reasons
         # outside this process
         dt = statistics.median(per_step)
-        del keep
+        del held, nxt
         dt = max_over_ranks(dt, dev, world)
         e2e = {"value": job_value(world, R, dt), "unit": "raw tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": 1e3 * dt,
                "ms_each_step": [round(1e3 * x, 1) for x in per_step], "statistic": "median over steps",
-               "includes": "plan build on host, plan image + Q/K/V + raw-order dO host->device, full step, "
-                           "raw-order LSE device->host; uploads on a copy stream in first-use order, "
-                           "overlapping the host plan build and the forward; one step at a time "
-                           "(synchronised at the end of every step)"}
+               "includes": "one plan build on the host per step (the next step's, while the GPU runs this "
+                           "one), plan image + Q/K/V + raw-order dO host->device, full step, raw-order LSE "
+                           "device->host; uploads on a copy stream in first-use order; synchronised at the "
+                           "end of every step"}
         del hQ, hK, hV, hdO
 
     # ---- CPU baseline (oracle), rank 0 only ----------------------------------
