@@ -21,7 +21,11 @@
 //               NS-stage ring (K and V have separate full/empty barriers)
 //   warp 1      MMA issuer (one thread) and TMEM owner
 //   warps 4..   one softmax warpgroup per head slot; thread t owns query row t
-// TMEM (512 columns): S_h at [128h, 128h+128) fp32, O_h at [128*HPC + D*h, +D).
+// With a GQA group of one (or an odd size) a CTA takes a single head and its
+// two slots take alternate key blocks of that head's list instead: each slot
+// keeps its own O, running maximum and row sum, merged once at the end
+// (split over keys inside the CTA), so the ping-pong below still applies.
+// TMEM (512 columns): S_h at [128h, 128h+128) fp32, O_h at [256 + D*h, +D).
 // P_h (bf16) is written over the first 64 columns of S_h and fed to the PV MMA
 // straight from TMEM, in two 64-key halves: the softmax releases the first
 // half (p_half) before computing the second (p_full), so the first half's PV
@@ -45,7 +49,7 @@ constexpr int BM = 128;          // query rows per tile
 constexpr int BN = 128;          // keys per block
 constexpr int kBox = BM * 128;   // bytes of one 128-row x 64-element swizzled box
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
-// Register split of the two-slot kernel (384 threads): the producer / MMA
+// Register split (384 threads): the producer / MMA
 // warpgroup gives registers up to the two softmax warpgroups, which hold a
 // whole 128-column score row per thread.
 constexpr uint32_t kRegsCtl = 56;
@@ -73,7 +77,9 @@ struct FwdSmem {
   uint8_t v[NS][D / 64][kBox];
   uint64_t q_full;
   uint64_t k_full[NS], v_full[NS], k_empty[NS], v_empty[NS];
-  uint64_t s_full[HPC], p_half[HPC], p_full[HPC], o_done[HPC];
+  uint64_t s_full[2], p_half[2], p_full[2], o_done[2];
+  uint64_t mrg_bar;          // single-head CTAs: the two slots swap (max, sum) per row
+  float mrg[2][2][BM];       // [slot][max, sum][row]
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -85,7 +91,7 @@ constexpr size_t fwd_smem_bytes() {
 }
 
 template <int D, int HPC, int NS>
-__global__ void __launch_bounds__(128 * (1 + HPC), 1)
+__global__ void __launch_bounds__(384, 1)
     tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using Smem = FwdSmem<D, HPC, NS>;
@@ -111,7 +117,8 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
       ptx::mbar_init(&S.k_empty[s], 1);
       ptx::mbar_init(&S.v_empty[s], 1);
     }
-    for (int h = 0; h < HPC; ++h) {
+    ptx::mbar_init(&S.mrg_bar, 256);
+    for (int h = 0; h < 2; ++h) {
       ptx::mbar_init(&S.s_full[h], 1);
       ptx::mbar_init(&S.p_half[h], 128);   // P of keys 0..63 stored
       ptx::mbar_init(&S.p_full[h], 128);
@@ -131,7 +138,7 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
   const uint32_t tmem = S.tmem_base;
 
   if (warp < 4) {
-  if constexpr (HPC == 2) ptx::regs_dec<kRegsCtl>();
+  ptx::regs_dec<kRegsCtl>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (ptx::elect_one()) {
@@ -177,19 +184,20 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
       const uint32_t q_base[2] = {ptx::smem_addr(S.q[0][0]), ptx::smem_addr(S.q[HPC - 1][0])};
       // PV of one key half (keys 64*part ..), so the first half's products
       // run while the softmax still computes the second half's P
-      auto issue_pv = [&](int s, int blk, int part) {
+      auto issue_pv = [&](int s, int blk, int part, bool first) {
         const int st = blk % NS;
         const uint32_t v_base = ptx::smem_addr(S.v[st][0]);
-        const uint32_t o_col = tmem + BM * HPC + D * s;
+        const uint32_t o_col = tmem + 2 * BM + D * s;
         const uint32_t p_col = tmem + BM * s;
 #pragma unroll
         for (int kk = part * (BN / 32); kk < (part + 1) * (BN / 32); ++kk) {
           // V block as the MN-major B operand: N = head dim (64-wide column
           // groups one box apart), K = 16 keys = 2 KB further per step
           const uint64_t bdesc = ptx::desc_add(ptx::sw128_desc(v_base, kBox, 1024), kk * 2048);
-          ptx::mma_ts(o_col, p_col + kk * 8, bdesc, idesc_pv, (blk > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_ts(o_col, p_col + kk * 8, bdesc, idesc_pv, (!first || kk > 0) ? 1u : 0u);
         }
       };
+      if constexpr (HPC == 2) {
       for (int i = 0; ok && i < n_blocks; ++i) {
         const int st = i % NS;
         const uint32_t use = i / NS;
@@ -205,10 +213,10 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
             }
             if (!ptx::mbar_wait(&S.p_half[s], (i - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
             ptx::tc_fence_after();
-            issue_pv(s, i - 1, 0);
+            issue_pv(s, i - 1, 0, i == 1);
             if (!ptx::mbar_wait(&S.p_full[s], (i - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
             ptx::tc_fence_after();
-            issue_pv(s, i - 1, 1);
+            issue_pv(s, i - 1, 1, i == 1);
           }
           const uint32_t s_col = tmem + BM * s;
 #pragma unroll
@@ -232,13 +240,58 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
           for (int s = 0; s < HPC; ++s) {
             if (!ptx::mbar_wait(&S.p_half[s], last & 1, abort_flag, kWaitLimitNs)) break;
             ptx::tc_fence_after();
-            issue_pv(s, last, 0);
+            issue_pv(s, last, 0, last == 0);
             if (!ptx::mbar_wait(&S.p_full[s], last & 1, abort_flag, kWaitLimitNs)) break;
             ptx::tc_fence_after();
-            issue_pv(s, last, 1);
+            issue_pv(s, last, 1, last == 0);
             ptx::mma_commit(&S.o_done[s]);
           }
         }
+      }
+      } else {
+      // one head: slot s takes blocks s, s+2, ...; the PV of a slot's block
+      // is issued one pair later, once its P is stored
+      const int n_pairs = (n_blocks + 1) / 2;
+      auto finish_pv = [&](int s, int pb, int local) {   // block pb is slot s's local-th
+        if (!ptx::mbar_wait(&S.v_full[pb % NS], (pb / NS) & 1, abort_flag, kWaitLimitNs)) return false;
+        if (!ptx::mbar_wait(&S.p_half[s], local & 1, abort_flag, kWaitLimitNs)) return false;
+        ptx::tc_fence_after();
+        issue_pv(s, pb, 0, local == 0);
+        if (!ptx::mbar_wait(&S.p_full[s], local & 1, abort_flag, kWaitLimitNs)) return false;
+        ptx::tc_fence_after();
+        issue_pv(s, pb, 1, local == 0);
+        ptx::mma_commit(&S.v_empty[pb % NS]);
+        return true;
+      };
+      for (int j = 0; ok && j < n_pairs; ++j) {
+        for (int s = 0; s < 2; ++s) {
+          const int b = 2 * j + s;
+          if (j > 0 && !finish_pv(s, b - 2, j - 1)) { ok = false; break; }
+          if (b >= n_blocks) continue;
+          const int st = b % NS;
+          if (!ptx::mbar_wait(&S.k_full[st], (b / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t k_base = ptx::smem_addr(S.k[st][0]);
+          uint32_t qb0 = q_base[0];
+          asm volatile("" : "+r"(qb0));
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
+            const uint64_t adesc = ptx::desc_add(ptx::sw128_desc(qb0, 16, 1024), koff);
+            const uint64_t bdesc = ptx::desc_add(ptx::sw128_desc(k_base, 16, 1024), koff);
+            ptx::mma_ss(tmem + BM * s, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&S.s_full[s]);
+          ptx::mma_commit(&S.k_empty[st]);
+        }
+      }
+      if (ok) {
+        for (int s = 0; s < 2; ++s) {
+          const int n_s = (n_blocks - s + 1) / 2;   // blocks of slot s; the last one's PV
+          if (n_s > 0 && n_s == n_pairs && !finish_pv(s, 2 * (n_s - 1) + s, n_s - 1)) break;   // is still due
+          ptx::mma_commit(&S.o_done[s]);
+        }
+      }
       }
       // drain: every MMA issued above has completed before TMEM is released
       ptx::mma_commit(&S.drain);
@@ -247,20 +300,24 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
   }
   } else {
     // ------------------------------------------------------------ softmax
-    if constexpr (HPC == 2) ptx::regs_inc<kRegsSoftmax>();
+    ptx::regs_inc<kRegsSoftmax>();
     const int slot = (warp - 4) >> 2;
     const int wq = warp & 3;                 // TMEM lane quarter of this warp
     const int r = wq * 32 + (threadIdx.x & 31);
     const int qi = q0 + r;                   // this thread's query (forwarded index)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t s_tm = tmem + lane_off + BM * slot;
-    const uint32_t o_tm = tmem + lane_off + BM * HPC + D * slot;
+    const uint32_t o_tm = tmem + lane_off + 2 * BM + D * slot;
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY;   // running maximum in use (log2 units)
     float l = 0.f;              // running row sum (relative to m_used)
     bool ok = true;
-    for (int i = 0; i < n_blocks; ++i) {
-      ok = ptx::mbar_wait(&S.s_full[slot], i & 1, abort_flag, kWaitLimitNs);
+    // two heads: every block; one head: this slot's blocks slot, slot+2, ...
+    constexpr bool kSplit = HPC == 1;
+    const int n_mine = kSplit ? (n_blocks - slot + 1) / 2 : n_blocks;
+    for (int jj = 0; jj < n_mine; ++jj) {
+      const int i = kSplit ? 2 * jj + slot : jj;
+      ok = ptx::mbar_wait(&S.s_full[slot], jj & 1, abort_flag, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
@@ -300,7 +357,7 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
         alpha = ptx::ex2(m_used - m_blk);   // 0 when m_used = -inf
         m_used = m_blk;
       }
-      if (i > 0 && __any_sync(0xffffffffu, raise)) {
+      if (jj > 0 && __any_sync(0xffffffffu, raise)) {
         // O accumulated through block i-1 is complete: the S(i) commit this
         // warp waited on tracks every earlier MMA, including PV(i-1).  It is
         // rescaled before any P of block i is released to the PV products.
@@ -341,6 +398,52 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
       const float sum = (s0 + s1) + (s2 + s3);
       l = l * alpha + sum;
     }
+    if constexpr (kSplit) {
+      // one head: merge the two slots' partial results row by row
+      if (ok) {
+        S.mrg[slot][0][r] = m_used;
+        S.mrg[slot][1][r] = l;
+        ptx::mbar_arrive(&S.mrg_bar);
+        ok = ptx::mbar_wait(&S.mrg_bar, 0, abort_flag, kWaitLimitNs) &&
+             ptx::mbar_wait(&S.o_done[0], 0, abort_flag, kWaitLimitNs) &&
+             ptx::mbar_wait(&S.o_done[1], 0, abort_flag, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok) {
+        ptx::tc_fence_after();
+        const float m0 = S.mrg[0][0][r], l0 = S.mrg[0][1][r], m1 = S.mrg[1][0][r], l1 = S.mrg[1][1][r];
+        const float m = fmaxf(m0, m1);
+        const float c0 = m0 == -INFINITY ? 0.f : ptx::ex2(m0 - m);
+        const float c1 = m1 == -INFINITY ? 0.f : ptx::ex2(m1 - m);
+        const float lt = l0 * c0 + l1 * c1;
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        const float w0 = c0 * inv, w1 = c1 * inv;
+        // this warpgroup writes half of the head dimension from both O
+        const uint32_t oa = tmem + lane_off + 2 * BM + (D / 2) * slot, ob = oa + D;
+        __nv_bfloat16* orow = p.o + (static_cast<int64_t>(qi) * p.Hq + h0) * D + (D / 2) * slot;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t ua[32], ub[32];
+          ptx::tmem_ld32(oa + c * 32, ua);
+          ptx::tmem_ld32(ob + c * 32, ub);
+          ptx::tmem_wait_ld();
+          if (r < nq) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[j] = ptx::pack_bf16x2(__uint_as_float(ua[2 * j]) * w0 + __uint_as_float(ub[2 * j]) * w1,
+                                       __uint_as_float(ua[2 * j + 1]) * w0 + __uint_as_float(ub[2 * j + 1]) * w1);
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          }
+        }
+        if (r < nq && slot == 0) {
+          const float lse = lt > 0.f ? (m + log2f(lt)) * 0.69314718055994530942f : -INFINITY;
+          p.lse[static_cast<int64_t>(h0) * p.F + qi] = lse;
+        }
+      }
+    } else {
     if (ok) {
       ok = ptx::mbar_wait(&S.o_done[slot], 0, abort_flag, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
@@ -370,6 +473,7 @@ __global__ void __launch_bounds__(128 * (1 + HPC), 1)
         p.lse[static_cast<int64_t>(h) * p.F + qi] = lse;
       }
     }
+    }
   }
 
   ptx::tc_fence_before();
@@ -392,17 +496,17 @@ int launch(const FwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, c
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
       return TPK_E_CUDA;
-    if constexpr (HPC == 2) {
+    {
       // the warpgroups' register shares must fit in what the CTA launches with
       cudaFuncAttributes fa;
       if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return TPK_E_CUDA;
-      if (fa.numRegs * 128 * (1 + HPC) < kRegsNeeded) return TPK_E_UNSUPPORTED;
+      if (fa.numRegs * 384 < kRegsNeeded) return TPK_E_UNSUPPORTED;
     }
     configured = true;
   }
   if (items <= 0) return TPK_OK;
   if (items > 0x7fffffff) return TPK_E_OVERFLOW;
-  kern<<<static_cast<unsigned>(items), 128 * (1 + HPC), smem, stream>>>(tq, tk, tv, prm);
+  kern<<<static_cast<unsigned>(items), 384, smem, stream>>>(tq, tk, tv, prm);
   return cuda_status(cudaGetLastError());
 }
 
