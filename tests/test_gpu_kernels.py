@@ -239,12 +239,22 @@ def _sample_raw(case, n, seed):
     return sorted(picks)
 
 
-FULL = ["grpo", "agentic"] + ["sweep_%.2f" % r for r in workloads.SWEEP_RHOS] + ["deep"]
+FULL = ["grpo", "agentic"] + ["sweep_%.2f" % r for r in workloads.SWEEP_RHOS] + ["deep", "sweep_3.56_mha"]
+
+
+def _full_workload(name):
+    # "<name>_mha": the same workload with one KV head per query head, which
+    # takes the forward's single-head (split over keys) path
+    if name.endswith("_mha"):
+        import dataclasses
+        w = workloads.get(name[:-4])
+        return dataclasses.replace(w, n_heads_kv=w.n_heads_q)
+    return workloads.get(name)
 
 
 @pytest.mark.parametrize("name", FULL)
 def test_forward_full_size_sampled(ops, name):
-    case = Case(ops, workloads.get(name))
+    case = Case(ops, _full_workload(name))
     Q, K, V, _ = case.inputs("cuda")
     _, _, o, lse, o_raw, lse_raw = gpu_forward(ops, case, Q, K, V)
     del Q, K, V
