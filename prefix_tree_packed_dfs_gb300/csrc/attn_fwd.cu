@@ -17,22 +17,27 @@
 //
 // One CTA = one (query tile, pair of query heads sharing a KV head).  Both
 // heads use the same K/V blocks, loaded once.  Warp roles:
-//   warp 0      TMA producer: Q tiles once, then K and V blocks through an
-//               NS-stage ring (K and V have separate full/empty barriers)
+//   warp 0      TMA producer: Q tiles once, then K and V blocks of 128 keys
+//               through an NS-stage ring (separate full/empty barriers)
 //   warp 1      MMA issuer (one thread) and TMEM owner
 //   warps 4..   one softmax warpgroup per head slot; thread t owns query row t
-// With a GQA group of one (or an odd size) a CTA takes a single head and its
-// two slots take alternate key blocks of that head's list instead: each slot
-// keeps its own O, running maximum and row sum, merged once at the end
-// (split over keys inside the CTA), so the ping-pong below still applies.
-// TMEM (512 columns): S_h at [128h, 128h+128) fp32, O_h at [256 + D*h, +D).
-// P_h (bf16) is written over the first 64 columns of S_h and fed to the PV MMA
-// straight from TMEM, in two 64-key halves: the softmax releases the first
-// half (p_half) before computing the second (p_full), so the first half's PV
+// TMEM (512 columns): S_s at [128s, 128s+128) fp32 and O_s at [256 + D*s, +D)
+// fp32, which fills it: QK^T reads Q from shared memory.  P_s (bf16) is
+// written over the first 64 columns of S_s and fed to the PV product straight
+// from TMEM, in two parts of half the keys: the softmax releases the first
+// part (p_half) before computing the second (p_full), so the first part's PV
 // products run meanwhile.  The MMA thread interleaves the two head slots
 // (PV_0(i-1), S_0(i), PV_1(i-1), S_1(i)) so one slot's softmax overlaps the
-// other slot's matrix products.  QK^T reads Q from shared memory: the four
-// S and O accumulators fill TMEM.
+// other slot's matrix products.
+// With a GQA group of one (or an odd size) a CTA takes a single head and its
+// two slots take the two 64-key halves of every block instead (split over
+// keys inside the CTA): each slot keeps its own O, running maximum and row
+// sum, merged once at the end.  S_s then needs 64 columns, which leaves room
+// for the Q tile in TMEM ([128 + 2D, +D/2), copied there by the softmax warps
+// once), so QK^T takes its A operand from TMEM -- measured 1.06-1.15x faster
+// than whole blocks per slot with Q in shared memory.  With two heads the
+// same 64-key form measured 1.16-1.24x slower than the layout above: its
+// shorter products no longer cover the softmax of the other slot.
 // Online softmax with a lazily raised running maximum: O and the row sum are
 // rescaled only when the block maximum exceeds the one in use by more than
 // 2^8, which keeps exponentials <= 256 and skips almost every rescale.
@@ -46,12 +51,12 @@ namespace tpk {
 namespace {
 
 constexpr int BM = 128;          // query rows per tile
-constexpr int BN = 128;          // keys per block
+constexpr int kBlock = 128;      // keys per block (one K/V stage)
 constexpr int kBox = BM * 128;   // bytes of one 128-row x 64-element swizzled box
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 // Register split (384 threads): the producer / MMA
 // warpgroup gives registers up to the two softmax warpgroups, which hold a
-// whole 128-column score row per thread.
+// 64-column score row per thread.
 constexpr uint32_t kRegsCtl = 56;
 constexpr uint32_t kRegsSoftmax = 216;
 constexpr int kRegsNeeded = 128 * kRegsCtl + 256 * kRegsSoftmax;
@@ -75,7 +80,7 @@ struct FwdSmem {
   uint8_t q[HPC][D / 64][kBox];
   uint8_t k[NS][D / 64][kBox];
   uint8_t v[NS][D / 64][kBox];
-  uint64_t q_full;
+  uint64_t q_full, qt_full;
   uint64_t k_full[NS], v_full[NS], k_empty[NS], v_empty[NS];
   uint64_t s_full[2], p_half[2], p_full[2], o_done[2];
   uint64_t mrg_bar;          // single-head CTAs: the two slots swap (max, sum) per row
@@ -99,6 +104,13 @@ __global__ void __launch_bounds__(384, 1)
   Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   volatile int* abort_flag = &S.abort_flag;
+  constexpr bool kSplit = HPC == 1;
+  // keys per S accumulator: a whole block (two heads) or one half (one head)
+  constexpr int kCols = kSplit ? kBlock / 2 : kBlock;
+  // TMEM columns: S_s at kCols*s (fp32), O_s at cO0 + D*s (fp32), and with
+  // one head its Q tile at cQ0 (bf16 pairs)
+  constexpr uint32_t cO0 = 2 * kCols, cQ0 = 2 * kCols + 2 * D;
+  static_assert(cQ0 + (kSplit ? D / 2 : 0) <= 512, "TMEM columns");
 
   const int item = blockIdx.x;
   const int tile = __ldg(p.qt_order + item / p.n_hgroups);
@@ -111,6 +123,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&S.q_full, 1);
+    ptx::mbar_init(&S.qt_full, 256);   // one head: every softmax thread, after its rows of Q are in TMEM
     for (int s = 0; s < NS; ++s) {
       ptx::mbar_init(&S.k_full[s], 1);
       ptx::mbar_init(&S.v_full[s], 1);
@@ -120,7 +133,7 @@ __global__ void __launch_bounds__(384, 1)
     ptx::mbar_init(&S.mrg_bar, 256);
     for (int h = 0; h < 2; ++h) {
       ptx::mbar_init(&S.s_full[h], 1);
-      ptx::mbar_init(&S.p_half[h], 128);   // P of keys 0..63 stored
+      ptx::mbar_init(&S.p_half[h], 128);   // P of the first half of the S columns stored
       ptx::mbar_init(&S.p_full[h], 128);
       ptx::mbar_init(&S.o_done[h], 1);
     }
@@ -177,121 +190,101 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (ptx::elect_one()) {
-      constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, BN, false, false);
+      constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(BM, kCols, false, false);
       constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(BM, D, false, true);
-      bool ok = ptx::mbar_wait(&S.q_full, 0, abort_flag, kWaitLimitNs);
+      bool ok = ptx::mbar_wait(kSplit ? &S.qt_full : &S.q_full, 0, abort_flag, kWaitLimitNs);
       ptx::tc_fence_after();
-      const uint32_t q_base[2] = {ptx::smem_addr(S.q[0][0]), ptx::smem_addr(S.q[HPC - 1][0])};
-      // PV of one key half (keys 64*part ..), so the first half's products
-      // run while the softmax still computes the second half's P
-      auto issue_pv = [&](int s, int blk, int part, bool first) {
-        const int st = blk % NS;
-        const uint32_t v_base = ptx::smem_addr(S.v[st][0]);
-        const uint32_t o_col = tmem + 2 * BM + D * s;
-        const uint32_t p_col = tmem + BM * s;
+      // PV of one part (half the keys of S_s) of the keys kCols*hf.. of block
+      // blk, so the first part's products run while the softmax still
+      // computes the second part's P
+      auto issue_pv = [&](int s, int blk, int hf, int part, bool first) {
+        const uint32_t v_base = ptx::smem_addr(S.v[blk % NS][0]);
+        const uint32_t o_col = tmem + cO0 + D * s;
+        const uint32_t p_col = tmem + kCols * s;
+        constexpr int kSteps = kCols / 32;   // 16-key steps per part
 #pragma unroll
-        for (int kk = part * (BN / 32); kk < (part + 1) * (BN / 32); ++kk) {
+        for (int kk = part * kSteps; kk < (part + 1) * kSteps; ++kk) {
           // V block as the MN-major B operand: N = head dim (64-wide column
           // groups one box apart), K = 16 keys = 2 KB further per step
-          const uint64_t bdesc = ptx::desc_add(ptx::sw128_desc(v_base, kBox, 1024), kk * 2048);
+          const uint64_t bdesc =
+              ptx::desc_add(ptx::sw128_desc(v_base, kBox, 1024), (kCols / 16 * hf + kk) * 2048);
           ptx::mma_ts(o_col, p_col + kk * 8, bdesc, idesc_pv, (!first || kk > 0) ? 1u : 0u);
         }
       };
-      if constexpr (HPC == 2) {
-      for (int i = 0; ok && i < n_blocks; ++i) {
-        const int st = i % NS;
-        const uint32_t use = i / NS;
-        if (!ptx::mbar_wait(&S.k_full[st], use & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+      // PV of slot s's n-th S (block blk, keys kCols*hf..), once both parts of its P are stored
+      auto finish_pv = [&](int s, int blk, int hf, int n) {
+        if (!ptx::mbar_wait(&S.p_half[s], n & 1, abort_flag, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
-        const uint32_t k_base = ptx::smem_addr(S.k[st][0]);
-        for (int s = 0; s < HPC; ++s) {
-          if (i > 0) {
-            const int pst = (i - 1) % NS;
-            if (s == 0 && !ptx::mbar_wait(&S.v_full[pst], ((i - 1) / NS) & 1, abort_flag, kWaitLimitNs)) {
-              ok = false;
-              break;
-            }
-            if (!ptx::mbar_wait(&S.p_half[s], (i - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-            ptx::tc_fence_after();
-            issue_pv(s, i - 1, 0, i == 1);
-            if (!ptx::mbar_wait(&S.p_full[s], (i - 1) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
-            ptx::tc_fence_after();
-            issue_pv(s, i - 1, 1, i == 1);
-          }
-          const uint32_t s_col = tmem + BM * s;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            // Q and K as K-major operands: 16 elements = 32 bytes per step
-            // inside a 64-element box, next box after 4 steps
-            const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
-            const uint64_t adesc = ptx::desc_add(ptx::sw128_desc(q_base[s], 16, 1024), koff);
-            const uint64_t bdesc = ptx::desc_add(ptx::sw128_desc(k_base, 16, 1024), koff);
-            ptx::mma_ss(s_col, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          ptx::mma_commit(&S.s_full[s]);
-        }
-        if (!ok) break;
-        ptx::mma_commit(&S.k_empty[st]);
-        if (i > 0) ptx::mma_commit(&S.v_empty[(i - 1) % NS]);
-      }
-      if (ok && n_blocks > 0) {
-        const int last = n_blocks - 1;
-        if (ptx::mbar_wait(&S.v_full[last % NS], (last / NS) & 1, abort_flag, kWaitLimitNs)) {
-          for (int s = 0; s < HPC; ++s) {
-            if (!ptx::mbar_wait(&S.p_half[s], last & 1, abort_flag, kWaitLimitNs)) break;
-            ptx::tc_fence_after();
-            issue_pv(s, last, 0, last == 0);
-            if (!ptx::mbar_wait(&S.p_full[s], last & 1, abort_flag, kWaitLimitNs)) break;
-            ptx::tc_fence_after();
-            issue_pv(s, last, 1, last == 0);
-            ptx::mma_commit(&S.o_done[s]);
-          }
-        }
-      }
-      } else {
-      // one head: slot s takes blocks s, s+2, ...; the PV of a slot's block
-      // is issued one pair later, once its P is stored
-      const int n_pairs = (n_blocks + 1) / 2;
-      auto finish_pv = [&](int s, int pb, int local) {   // block pb is slot s's local-th
-        if (!ptx::mbar_wait(&S.v_full[pb % NS], (pb / NS) & 1, abort_flag, kWaitLimitNs)) return false;
-        if (!ptx::mbar_wait(&S.p_half[s], local & 1, abort_flag, kWaitLimitNs)) return false;
+        issue_pv(s, blk, hf, 0, n == 0);
+        if (!ptx::mbar_wait(&S.p_full[s], n & 1, abort_flag, kWaitLimitNs)) return false;
         ptx::tc_fence_after();
-        issue_pv(s, pb, 0, local == 0);
-        if (!ptx::mbar_wait(&S.p_full[s], local & 1, abort_flag, kWaitLimitNs)) return false;
-        ptx::tc_fence_after();
-        issue_pv(s, pb, 1, local == 0);
-        ptx::mma_commit(&S.v_empty[pb % NS]);
+        issue_pv(s, blk, hf, 1, n == 0);
         return true;
       };
-      for (int j = 0; ok && j < n_pairs; ++j) {
-        for (int s = 0; s < 2; ++s) {
-          const int b = 2 * j + s;
-          if (j > 0 && !finish_pv(s, b - 2, j - 1)) { ok = false; break; }
-          if (b >= n_blocks) continue;
-          const int st = b % NS;
-          if (!ptx::mbar_wait(&S.k_full[st], (b / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+      auto wait_v = [&](int blk) {
+        return ptx::mbar_wait(&S.v_full[blk % NS], (blk / NS) & 1, abort_flag, kWaitLimitNs);
+      };
+      if constexpr (!kSplit) {
+        // two heads: PV_0(i-1), S_0(i), PV_1(i-1), S_1(i); QK^T reads Q from
+        // shared memory (TMEM holds the two S and two O accumulators)
+        const uint32_t q_base[2] = {ptx::smem_addr(S.q[0][0]), ptx::smem_addr(S.q[HPC - 1][0])};
+        for (int i = 0; ok && i < n_blocks; ++i) {
+          const int st = i % NS;
+          if (!ptx::mbar_wait(&S.k_full[st], (i / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t k_base = ptx::smem_addr(S.k[st][0]);
-          uint32_t qb0 = q_base[0];
-          asm volatile("" : "+r"(qb0));
+          for (int s = 0; s < 2; ++s) {
+            if (i > 0) {
+              if (s == 0 && !wait_v(i - 1)) { ok = false; break; }
+              if (!finish_pv(s, i - 1, 0, i - 1)) { ok = false; break; }
+            }
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
-            const uint64_t adesc = ptx::desc_add(ptx::sw128_desc(qb0, 16, 1024), koff);
-            const uint64_t bdesc = ptx::desc_add(ptx::sw128_desc(k_base, 16, 1024), koff);
-            ptx::mma_ss(tmem + BM * s, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              // Q and K as K-major operands: 16 elements = 32 bytes per step
+              // inside a 64-element box, next box after 4 steps
+              const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
+              const uint64_t adesc = ptx::desc_add(ptx::sw128_desc(q_base[s], 16, 1024), koff);
+              const uint64_t bdesc = ptx::desc_add(ptx::sw128_desc(k_base, 16, 1024), koff);
+              ptx::mma_ss(tmem + kCols * s, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(&S.s_full[s]);
           }
-          ptx::mma_commit(&S.s_full[s]);
+          if (!ok) break;
           ptx::mma_commit(&S.k_empty[st]);
+          if (i > 0) ptx::mma_commit(&S.v_empty[(i - 1) % NS]);
+        }
+      } else {
+        // one head: slot s takes keys 64s.. of every block; QK^T reads Q from
+        // TMEM; a slot's PV is issued one block later, once its P is stored
+        for (int i = 0; ok && i < n_blocks; ++i) {
+          const int st = i % NS;
+          if (!ptx::mbar_wait(&S.k_full[st], (i / NS) & 1, abort_flag, kWaitLimitNs)) { ok = false; break; }
+          ptx::tc_fence_after();
+          for (int s = 0; s < 2; ++s) {
+            if (i > 0) {
+              if (s == 0 && !wait_v(i - 1)) { ok = false; break; }
+              if (!finish_pv(s, i - 1, s, i - 1)) { ok = false; break; }
+            }
+            const uint32_t k_base = ptx::smem_addr(S.k[st][0]) + s * (kBox / 2);   // key rows 64s..
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = (kk >> 2) * kBox + (kk & 3) * 32;
+              const uint64_t bdesc = ptx::desc_add(ptx::sw128_desc(k_base, 16, 1024), koff);
+              ptx::mma_ts(tmem + kCols * s, tmem + cQ0 + kk * 8, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(&S.s_full[s]);
+          }
+          if (!ok) break;
+          ptx::mma_commit(&S.k_empty[st]);
+          if (i > 0) ptx::mma_commit(&S.v_empty[(i - 1) % NS]);
         }
       }
-      if (ok) {
+      // the last block's PV products are still due
+      if (ok && n_blocks > 0 && wait_v(n_blocks - 1)) {
         for (int s = 0; s < 2; ++s) {
-          const int n_s = (n_blocks - s + 1) / 2;   // blocks of slot s; the last one's PV
-          if (n_s > 0 && n_s == n_pairs && !finish_pv(s, 2 * (n_s - 1) + s, n_s - 1)) break;   // is still due
+          if (!finish_pv(s, n_blocks - 1, kSplit ? s : 0, n_blocks - 1)) break;
           ptx::mma_commit(&S.o_done[s]);
         }
-      }
       }
       // drain: every MMA issued above has completed before TMEM is released
       ptx::mma_commit(&S.drain);
@@ -306,37 +299,63 @@ __global__ void __launch_bounds__(384, 1)
     const int r = wq * 32 + (threadIdx.x & 31);
     const int qi = q0 + r;                   // this thread's query (forwarded index)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t s_tm = tmem + lane_off + BM * slot;
-    const uint32_t o_tm = tmem + lane_off + 2 * BM + D * slot;
+    const uint32_t s_tm = tmem + lane_off + kCols * slot;
+    const uint32_t o_tm = tmem + lane_off + cO0 + D * slot;
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY;   // running maximum in use (log2 units)
     float l = 0.f;              // running row sum (relative to m_used)
     bool ok = true;
-    // two heads: every block; one head: this slot's blocks slot, slot+2, ...
-    constexpr bool kSplit = HPC == 1;
-    const int n_mine = kSplit ? (n_blocks - slot + 1) / 2 : n_blocks;
-    for (int jj = 0; jj < n_mine; ++jj) {
-      const int i = kSplit ? 2 * jj + slot : jj;
+    if constexpr (kSplit) {
+      // row r of the Q tile into TMEM lane r (the A operand of QK^T).  The
+      // tile sits in shared memory as 128-byte-swizzled boxes of 64 elements
+      // (16-byte chunk c of row r at chunk c ^ (r % 8)); TMEM column w holds
+      // elements 2w, 2w+1.  The two warpgroups take alternate boxes.
+      ok = ptx::mbar_wait(&S.q_full, 0, abort_flag, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b) {
+          if ((b & 1) != slot) continue;
+          uint32_t w[32];
+          const uint8_t* row = S.q[0][b] + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
+            w[4 * c] = v.x;
+            w[4 * c + 1] = v.y;
+            w[4 * c + 2] = v.z;
+            w[4 * c + 3] = v.w;
+          }
+          ptx::tmem_st32(tmem + lane_off + cQ0 + b * 32, w);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&S.qt_full);
+      }
+    }
+    // two heads: every block, all its keys; one head: keys 64*slot.. of every block
+    const int hf = kSplit ? slot : 0;
+    for (int jj = 0; ok && jj < n_blocks; ++jj) {
       ok = ptx::mbar_wait(&S.s_full[slot], jj & 1, abort_flag, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
-      const int2 blk = __ldg(&p.kb[kb_begin + i]);
-      const int k0 = blk.x, nk = blk.y & 0xFFFF;
+      const int2 blk = __ldg(&p.kb[kb_begin + jj]);
+      const int k0 = blk.x + kCols * hf, nk = (blk.y & 0xFFFF) - kCols * hf;
       const bool full = (blk.y >> 16) & 1;
-      float sv[BN];
+      float sv[kCols];
       {
-        uint32_t u[BN];
+        uint32_t u[kCols];
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c)
+        for (int c = 0; c < kCols / 32; ++c)
           ptx::tmem_ld32(s_tm + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < BN; ++j) sv[j] = __uint_as_float(u[j]);
+        for (int j = 0; j < kCols; ++j) sv[j] = __uint_as_float(u[j]);
       }
       if (!full) {
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
+        for (int c = 0; c < kCols; ++c) {
           const int j = k0 + c;
           const bool vis = (c < nk) && (j <= qi) && (qi < __ldg(p.subtree_end + j));
           if (!vis) sv[c] = -INFINITY;
@@ -345,7 +364,7 @@ __global__ void __launch_bounds__(384, 1)
       // row maximum: 3-input max, four independent chains
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < BN; c += 8) {   // columns c .. c+7, exactly 0 .. BN-1
+      for (int c = 0; c < kCols; c += 8) {   // columns c .. c+7, exactly 0 .. kCols-1
 #pragma unroll
         for (int x = 0; x < 4; ++x) m4[x] = ptx::max3(m4[x], sv[c + 2 * x], sv[c + 2 * x + 1]);
       }
@@ -358,9 +377,10 @@ __global__ void __launch_bounds__(384, 1)
         m_used = m_blk;
       }
       if (jj > 0 && __any_sync(0xffffffffu, raise)) {
-        // O accumulated through block i-1 is complete: the S(i) commit this
-        // warp waited on tracks every earlier MMA, including PV(i-1).  It is
-        // rescaled before any P of block i is released to the PV products.
+        // O accumulated through this slot's previous block is complete: the
+        // S commit this warp waited on tracks every earlier MMA, including
+        // that block's PV.  It is rescaled before any P of this block is
+        // released to the PV products.
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t u[32];
@@ -372,22 +392,27 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
-      // exponent arguments and the row sum on packed fp32 pairs; P of keys
-      // 0..63 is released (p_half) before the second half is computed
+      // exponent arguments and the row sum on packed fp32 pairs; P of the
+      // first half of the keys is released (p_half) before the second half
+      // is computed
       const uint64_t sl2x2 = ptx::f2(sl2, sl2), negm = ptx::f2(-m_sub, -m_sub);
       uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
-      for (int c = 0; c < BN / 64; ++c) {
-        uint32_t pk[32];
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[kCols / 4];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < kCols / 4; ++j) {
           float a0, a1;
-          ptx::unf2(ptx::fma2(ptx::f2(sv[c * 64 + 2 * j], sv[c * 64 + 2 * j + 1]), sl2x2, negm), a0, a1);
+          ptx::unf2(ptx::fma2(ptx::f2(sv[c * (kCols / 2) + 2 * j], sv[c * (kCols / 2) + 2 * j + 1]), sl2x2, negm),
+                    a0, a1);
           const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
           sum2[j & 1] = ptx::add2(sum2[j & 1], ptx::f2(p0, p1));
           pk[j] = ptx::pack_bf16x2(p0, p1);
         }
-        ptx::tmem_st32(s_tm + c * 32, pk);
+        if constexpr (kCols == 128)
+          ptx::tmem_st32(s_tm + c * 32, pk);
+        else
+          ptx::tmem_st16(s_tm + c * 16, pk);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(c == 0 ? &S.p_half[slot] : &S.p_full[slot]);
@@ -419,7 +444,7 @@ __global__ void __launch_bounds__(384, 1)
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
         const float w0 = c0 * inv, w1 = c1 * inv;
         // this warpgroup writes half of the head dimension from both O
-        const uint32_t oa = tmem + lane_off + 2 * BM + (D / 2) * slot, ob = oa + D;
+        const uint32_t oa = tmem + lane_off + cO0 + (D / 2) * slot, ob = oa + D;
         __nv_bfloat16* orow = p.o + (static_cast<int64_t>(qi) * p.Hq + h0) * D + (D / 2) * slot;
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
