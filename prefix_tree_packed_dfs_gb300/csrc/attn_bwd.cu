@@ -127,8 +127,8 @@ struct KVSmem {
   uint8_t v[D / 64][kBox];
   uint8_t q[NH][D / 64][kHalfBox];
   uint8_t dO[NH][D / 64][kHalfBox];
-  float lse2[kStat][BT];   // -LSE * log2(e) of the step's queries (-inf past the block)
-  float dsum[kStat][BT];   // -D = -(dO . O)
+  alignas(16) float lse2[kStat][BT];   // -LSE * log2(e) of the step's queries (-inf past the block); 16-byte loads
+  alignas(16) float dsum[kStat][BT];   // -D = -(dO . O); 16-byte loads
   int2 blk[kStat];         // the step's query block (first query, count | full << 16)
   uint64_t kv_full, q_full[NH], q_empty[NH], stat_full[kStat], stat_empty[kStat], s_full[2], p_part[2], p_full[2], acc_done,
       drain;
@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(384, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
   using Smem = KVSmem<D, NH>;
+  static_assert(offsetof(Smem, lse2) % 16 == 0 && offsetof(Smem, dsum) % 16 == 0, "16-byte shared loads");
   extern __shared__ uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -472,6 +473,8 @@ struct QSmem {
   uint8_t k[NH][D / 64][kHalfBox];
   uint8_t v[NH][D / 64][kHalfBox];
   uint64_t q_full, qt_full, kv_full[NH], kv_empty[NH], s_full[2], p_part[2], p_full[2], acc_done, drain;
+  alignas(16) int se[2][2][kHalf];    // [half][buffer][key]: subtree_end of a masked block's keys (16-byte loads)
+  uint64_t se_bar[2];        // per half: its warpgroup has staged se
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -482,6 +485,7 @@ __global__ void __launch_bounds__(384, 1)
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                  const BwdParams p) {
   using Smem = QSmem<D, NH>;
+  static_assert(offsetof(Smem, se) % 16 == 0, "16-byte shared loads of se");
   extern __shared__ uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -509,6 +513,7 @@ __global__ void __launch_bounds__(384, 1)
       ptx::mbar_init(&S.s_full[x], 1);
       ptx::mbar_init(&S.p_part[x], 128);   // dS of the half's first 32 keys stored
       ptx::mbar_init(&S.p_full[x], 128);
+      ptx::mbar_init(&S.se_bar[x], 128);
     }
     ptx::mbar_init(&S.acc_done, 1);
     ptx::mbar_init(&S.drain, 1);
@@ -653,6 +658,7 @@ __global__ void __launch_bounds__(384, 1)
       ptx::mbar_arrive(&S.qt_full);
     }
     int2 next = n_blocks > 0 ? __ldg(&p.kb[kb_begin]) : make_int2(0, 0);
+    int n_masked = 0;   // masked blocks so far (selects the subtree_end buffer)
     for (int b = 0; ok && b < n_blocks; ++b) {
       const int2 blk = next;   // fetched one block ahead
       if (b + 1 < n_blocks) next = __ldg(&p.kb[kb_begin + b + 1]);
@@ -663,6 +669,21 @@ __global__ void __launch_bounds__(384, 1)
       const int kb0 = blk.x, nkb = blk.y & 0xFFFF;
       const bool full = (blk.y >> 16) & 1;
       const int base = kb0 + half * kHalf;     // first key of this half
+      const int* se = S.se[half][n_masked & 1];
+      if (!full) {
+        // key j = base + col is visible to query i iff j <= i < subtree_end[j]:
+        // the warpgroup stages the half's subtree_end in shared memory (one
+        // load per thread; 0 past the block's end, which hides the column)
+        // and meets at its se_bar (bounded wait); two buffers by the parity of
+        // the masked-block count, as in the forward
+        if (t < kHalf) S.se[half][n_masked & 1][t] = half * kHalf + t < nkb ? __ldg(p.subtree_end + base + t) : 0;
+        ptx::mbar_arrive(&S.se_bar[half]);
+        ok = ptx::mbar_wait(&S.se_bar[half], n_masked & 1, abort_flag, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        ++n_masked;
+        if (!ok) break;
+      }
+      const int cmax = i - base;               // columns <= cmax hold keys j <= i
 #pragma unroll
       for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t us[32], ud[32];
@@ -674,16 +695,19 @@ __global__ void __launch_bounds__(384, 1)
         for (int e = 0; e < 32; e += 2)
           ptx::unf2(ptx::fma2(ptx::f2(__uint_as_float(us[e]), __uint_as_float(us[e + 1])), sl2x2, nl2x2), arg[e],
                     arg[e + 1]);
-        if (!(full && row_ok)) {
-          // partial block: key j visible iff j < block end, j <= i < subtree_end[j]
+        if (!full) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int col = half * kHalf + c * 32 + e;
-            const int jj = base + c * 32 + e;
-            bool vis = row_ok && col < nkb && jj <= i;
-            if (vis) vis = i < __ldg(p.subtree_end + jj);
-            arg[e] = vis ? arg[e] : -INFINITY;
+          for (int e = 0; e < 32; e += 4) {
+            const int4 v = ptx::lds128i(se + c * 32 + e);
+            const int cc = c * 32 + e;
+            if (!(row_ok && cc <= cmax && i < v.x)) arg[e] = -INFINITY;
+            if (!(row_ok && cc + 1 <= cmax && i < v.y)) arg[e + 1] = -INFINITY;
+            if (!(row_ok && cc + 2 <= cmax && i < v.z)) arg[e + 2] = -INFINITY;
+            if (!(row_ok && cc + 3 <= cmax && i < v.w)) arg[e + 3] = -INFINITY;
           }
+        } else if (!row_ok) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) arg[e] = -INFINITY;
         }
         uint32_t pd[16];
 #pragma unroll

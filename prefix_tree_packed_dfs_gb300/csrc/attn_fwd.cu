@@ -85,6 +85,8 @@ struct FwdSmem {
   uint64_t s_full[2], p_half[2], p_full[2], o_done[2];
   uint64_t mrg_bar;          // single-head CTAs: the two slots swap (max, sum) per row
   float mrg[2][2][BM];       // [slot][max, sum][row]
+  alignas(16) int se[2][2][kBlock];   // [slot][buffer][key]: subtree_end of a masked block's keys (16-byte loads)
+  uint64_t se_bar[2];        // per slot: its warpgroup has staged se
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -100,6 +102,7 @@ __global__ void __launch_bounds__(384, 1)
     tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using Smem = FwdSmem<D, HPC, NS>;
+  static_assert(offsetof(Smem, se) % 16 == 0, "16-byte shared loads of se");
   extern __shared__ uint8_t smem_raw[];
   Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     ptx::mbar_init(&S.mrg_bar, 256);
     for (int h = 0; h < 2; ++h) {
+      ptx::mbar_init(&S.se_bar[h], 128);
       ptx::mbar_init(&S.s_full[h], 1);
       ptx::mbar_init(&S.p_half[h], 128);   // P of the first half of the S columns stored
       ptx::mbar_init(&S.p_full[h], 128);
@@ -335,6 +339,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     // two heads: every block, all its keys; one head: keys 64*slot.. of every block
     const int hf = kSplit ? slot : 0;
+    int n_masked = 0;   // masked blocks so far (selects the subtree_end buffer)
     for (int jj = 0; ok && jj < n_blocks; ++jj) {
       ok = ptx::mbar_wait(&S.s_full[slot], jj & 1, abort_flag, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
@@ -354,11 +359,29 @@ __global__ void __launch_bounds__(384, 1)
         for (int j = 0; j < kCols; ++j) sv[j] = __uint_as_float(u[j]);
       }
       if (!full) {
+        // key j = k0 + c is visible to query qi iff j <= qi < subtree_end[j].
+        // The warpgroup stages the keys' subtree_end in shared memory (one
+        // load per thread; 0 past the block's end, which hides the column),
+        // meets at its se_bar (a bounded wait, like every wait here), then
+        // every row tests all columns from there.  Two buffers by the parity
+        // of the masked-block count: a buffer is rewritten only after every
+        // thread of the warpgroup has arrived for the next masked block, i.e.
+        // has finished reading it.
+        int* se = S.se[slot][n_masked & 1];
+        if (r < kCols) se[r] = r < nk ? __ldg(p.subtree_end + k0 + r) : 0;
+        ptx::mbar_arrive(&S.se_bar[slot]);
+        ok = ptx::mbar_wait(&S.se_bar[slot], n_masked & 1, abort_flag, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        ++n_masked;
+        if (!ok) break;
+        const int cmax = qi - k0;   // columns c <= cmax hold keys j <= qi
 #pragma unroll
-        for (int c = 0; c < kCols; ++c) {
-          const int j = k0 + c;
-          const bool vis = (c < nk) && (j <= qi) && (qi < __ldg(p.subtree_end + j));
-          if (!vis) sv[c] = -INFINITY;
+        for (int c = 0; c < kCols; c += 4) {
+          const int4 e = ptx::lds128i(se + c);
+          if (!(c <= cmax && qi < e.x)) sv[c] = -INFINITY;
+          if (!(c + 1 <= cmax && qi < e.y)) sv[c + 1] = -INFINITY;
+          if (!(c + 2 <= cmax && qi < e.z)) sv[c + 2] = -INFINITY;
+          if (!(c + 3 <= cmax && qi < e.w)) sv[c + 3] = -INFINITY;
         }
       }
       // row maximum: 3-input max, four independent chains

@@ -242,6 +242,15 @@ __device__ __forceinline__ float4 lds128(const void* p) {
   return v;
 }
 
+// 16-byte shared-memory load of four int32.
+__device__ __forceinline__ int4 lds128i(const void* p) {
+  int4 v;
+  asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+
 // ---- packed fp32 pairs (sm_100 family): two lanes per instruction ---------
 __device__ __forceinline__ uint64_t f2(float lo, float hi) {
   uint64_t r;

@@ -166,6 +166,10 @@ SMALL = {
     "ragged_d128_h1": lambda: _ragged(1, 3, 3, 128),
     "ragged_d64_gqa2": lambda: _ragged(2, 4, 2, 64),
     "ragged_d128_gqa4": lambda: _ragged(3, 8, 2, 128, cap=1024),
+    # odd GQA group (3 query heads per KV head) and MHA at d=64: the
+    # forward's single-head path (each slot one 64-key half of every block)
+    "ragged_d128_gqa3": lambda: _ragged(4, 6, 2, 128),
+    "ragged_d64_h1": lambda: _ragged(5, 2, 2, 64, n_leaves=12),
 }
 
 
@@ -273,7 +277,8 @@ def test_forward_full_size_sampled(ops, name):
 
 
 # --------------------------------------------------------------- backward
-@pytest.mark.parametrize("name", ["tiny", "deep_small", "ragged_d128_h1", "ragged_d64_gqa2", "ragged_d128_gqa4"])
+@pytest.mark.parametrize("name", ["tiny", "deep_small", "ragged_d128_h1", "ragged_d64_gqa2", "ragged_d128_gqa4",
+                                  "ragged_d128_gqa3"])
 def test_backward_full_parity(ops, name):
     case = Case(ops, SMALL[name]())
     Q, K, V, dO = case.inputs("cpu", backward=True)
