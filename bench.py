@@ -49,8 +49,8 @@ LAUNCHES_PER_STEP = 9   # rope, fwd, scatter rows, scatter lse, dO sum, bwd prep
 # (first launch of each kernel; the summary is in profiles/), tagged with a
 # digest of the library sources they were built from.  Once the sources
 # differ the figure no longer describes the kernel and is reported as null.
-TRAFFIC = {"digest": "318627fd7fca3c8373390c8316f28c1cc72ef76af2791e471cd49c6552be373f",
-           "fwd": 152339315712, "bwd_dkdv": 473889441792, "bwd_dq": 249086969344}
+TRAFFIC = {"digest": "f066e32a89fa112925c6b7553780947f70795981f954fa3f501c6ce3957bedc5",
+           "fwd": 173898329856, "bwd_dkdv": 475493116928, "bwd_dq": 261452960768}
 
 
 def source_digest():
@@ -85,7 +85,7 @@ def _args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--planner", action="store_true",
