@@ -47,22 +47,25 @@ LAUNCHES_PER_STEP = 9   # rope, fwd, scatter rows, scatter lse, dO sum, bwd prep
 # attention kernels on the deep-tree workload, from one ncu capture of
 #   bench.py --steps 1 --warmup 1 --e2e-steps 0 --no-cpu-baseline
 # (first launch of each kernel; the summary is in profiles/), tagged with a
-# digest of the library sources they were built from.  Once the sources
+# digest of the kernel and planner sources they were built from.  Once those
 # differ the figure no longer describes the kernel and is reported as null.
-TRAFFIC = {"digest": "f066e32a89fa112925c6b7553780947f70795981f954fa3f501c6ce3957bedc5",
+TRAFFIC = {"digest": "53984cdfbfa968722824226d117ca2e66edee8d4b60a62d5a8db493986750b13",
            "fwd": 173898329856, "bwd_dkdv": 475493116928, "bwd_dq": 261452960768}
 
 
 def source_digest():
-    """sha256 over the library's sources (csrc/ and include/), in name order,
-    with comments and whitespace removed: edits to comments leave it alone."""
+    """sha256 over the sources that decide the kernels' memory traffic -- the
+    device code (csrc/*.cu, *.cuh) and the planner that orders their work
+    (csrc/planner.*, plan_handle.h) -- in name order, with comments and
+    whitespace removed: edits to comments, or to host-side API code, leave
+    it alone."""
     import hashlib
     import re
     h = hashlib.sha256()
-    dirs = [os.path.join(ROOT, "prefix_tree_packed_dfs_gb300", "csrc"), os.path.join(ROOT, "include")]
+    dirs = [os.path.join(ROOT, "prefix_tree_packed_dfs_gb300", "csrc")]
     for d in dirs:
         for name in sorted(os.listdir(d)):
-            if name.endswith((".cu", ".cuh", ".cpp", ".h")):
+            if name.endswith((".cu", ".cuh")) or name in ("planner.cpp", "planner.h", "plan_handle.h"):
                 with open(os.path.join(d, name)) as f:
                     code = f.read()
                 code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
@@ -86,6 +89,9 @@ def _args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--shard-rows", action="store_true",
+                    help="with several ranks: split one batch across them by whole rows (strong scaling) "
+                         "instead of one batch of the same shape per rank")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--planner", action="store_true",
@@ -288,13 +294,25 @@ def run_ours(a):
         dist.init_process_group("nccl")
     peaks = _peaks()
     w = workloads.get(a.workload)
-    # weak scaling: every rank owns one batch of the same shape (rows are
-    # independent; no data crosses ranks)
+    # rows are independent, so no data crosses ranks.  Weak scaling (default):
+    # every rank owns one batch of the same shape.  --shard-rows: one batch,
+    # its rows dealt to the ranks longest first; each rank plans its rows'
+    # sequences with their row as the group, which rebuilds exactly those rows.
+    sharded = a.shard_rows and world > 1
     t0 = time.perf_counter()
-    plan = ops.Plan.from_sequences(w.sequences, group_ids=w.group_ids, row_capacity=w.row_capacity,
+    full = ops.Plan.from_sequences(w.sequences, group_ids=w.group_ids, row_capacity=w.row_capacity,
                                    min_shared=w.min_shared)
+    if sharded:
+        rank_of_row, _ = full.shard_rows(world)
+        plan, my_seqs = full.rank_plan(w.sequences, rank_of_row, rank, w.row_capacity, w.min_shared)
+        my_groups = full.export()["row_of_seq"][my_seqs]
+    else:
+        plan, my_seqs, my_groups = full, np.arange(len(w.sequences)), w.group_ids
     plan_s = time.perf_counter() - t0
     info = plan.info
+    # raw / forwarded tokens per second of the whole job
+    job_rate = ((lambda n_rank, n_full, secs: n_full / secs) if sharded
+                else (lambda n_rank, n_full, secs: job_value(world, n_rank, secs)))
     F, R, d, Hq, Hkv = info["n_fwd"], info["n_raw"], w.head_dim, w.n_heads_q, w.n_heads_kv
     pairs = info["useful_pairs"]
     dp = plan.to_device()
@@ -391,8 +409,9 @@ def run_ours(a):
     # ---- end to end through the public API, host buffers -----------------
     e2e = None
     if a.e2e_steps > 0:
-        tokens = np.concatenate(w.sequences).astype(np.int32)
-        offs = w.seq_offsets()
+        tokens = np.concatenate([w.sequences[i] for i in my_seqs]).astype(np.int32)
+        offs = np.zeros(len(my_seqs) + 1, np.int64)
+        offs[1:] = np.cumsum([len(w.sequences[i]) for i in my_seqs])
         hQ, hK, hV, hdO = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (Q, K, V, dO_raw))
         for h, x in zip((hQ, hK, hV, hdO), (Q, K, V, dO_raw)):
             h.copy_(x)
@@ -407,8 +426,8 @@ def run_ours(a):
         copy_stream = torch.cuda.Stream(dev)
 
         def build_plan():
-            return ops.Plan(tokens, offs, group_ids=w.group_ids, row_capacity=w.row_capacity,
-                            min_shared=w.min_shared)
+            return ops.Plan(tokens, offs, group_ids=my_groups, row_capacity=w.row_capacity,
+                            min_shared=w.min_shared, placement="groups" if sharded else "bfd")
 
         def events(*keys, timing=False):
             return {k: torch.cuda.Event(enable_timing=timing) for k in keys}
@@ -496,7 +515,7 @@ def run_ours(a):
         run_e2e(2)                        # warm-up: allocations, page-locked staging
         dt, gaps, first = run_e2e(a.e2e_steps)
         dt = max_over_ranks(dt / a.e2e_steps, dev, world)
-        e2e = {"value": job_value(world, R, dt), "unit": "raw tokens/s", "h2d_bytes_per_step": int(h2d),
+        e2e = {"value": job_rate(R, full.info["n_raw"], dt), "unit": "raw tokens/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": 1e3 * dt, "steps": a.e2e_steps,
                "ms_between_step_ends": [round(x, 1) for x in gaps], "first_step_ms": first,
                "statistic": "wall time of all steps / steps",
@@ -550,18 +569,19 @@ def run_ours(a):
 
     useful_tflops = (fwd_flop + bwd_flop) / (ms / 1e3) / 1e12
     out = {
-        "metric": METRIC, "value": job_value(world, R, ms / 1e3), "unit": "raw tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": job_rate(R, full.info["n_raw"], ms / 1e3), "unit": "raw tokens/s", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "strong" if sharded else "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC, "raw_tokens": R, "forwarded_tokens": F, "rows": info["n_rows"],
                    "packing_ratio": info["packing_ratio"], "useful_pairs": pairs,
                    "visited_pairs_fwd": info["visited_pairs"], "Hq": Hq, "Hkv": Hkv, "head_dim": d,
                    "row_capacity": w.row_capacity, "l2": "inputs larger than L2 (Q alone %.1f GB)" % (F * Hq * d * 2 / 1e9),
-                   "parallelism": "rows per rank, no collective" if world > 1 else "single GPU"},
+                   "parallelism": ("one batch, whole rows per rank (longest first), no collective" if sharded
+                                   else "one batch per rank, no collective" if world > 1 else "single GPU")},
         "useful_tflops": useful_tflops,
         "pct_of_peak": 100.0 * useful_tflops / peaks["bf16_tflops_sustained"],
         "pct_of_burst_peak": 100.0 * useful_tflops / peaks["bf16_tflops"],
-        "forwarded_tokens_per_s": world * F / (ms / 1e3),
+        "forwarded_tokens_per_s": job_rate(F, full.info["n_fwd"], ms / 1e3),
         "fwd_tflops": fwd_flop / (per["fwd"] / 1e3) / 1e12,
         "bwd_tflops": bwd_flop / ((per["bwd_prep"] + per["bwd_dkdv"] + per["bwd_dq"]) / 1e3) / 1e12,
         "kernels": kernels,

@@ -66,6 +66,12 @@ extern "C" {
                                    over marginal cost (the default) */
 #define TPK_PLACE_NEXT_FIT  1   /* [ART] "One tree, not one per group": fill rows in
                                    order, open a new row when the next leaf does not fit */
+#define TPK_PLACE_GROUPS    2   /* no counterpart on the pages: one row per placement
+                                   group, rows in increasing group id (a rank that owns
+                                   rows of a larger batch, see tpk_plan_shard_rows, plans
+                                   its sequences with their global row as the group and
+                                   gets those rows back); a group that does not fit in
+                                   one row gives TPK_E_SEQ_TOO_LONG */
 
 typedef struct tpk_plan tpk_plan;   /* opaque, host memory */
 
@@ -74,7 +80,7 @@ typedef struct {
                               memory; [TRL] token_budget counts forwarded tokens) */
     int32_t min_shared;    /* minimum shared-segment length ([ART] "The tree": shorter
                               shared runs are copied into each branch); <=1 disables */
-    int32_t placement;     /* TPK_PLACE_BFD or TPK_PLACE_NEXT_FIT */
+    int32_t placement;     /* TPK_PLACE_BFD, TPK_PLACE_NEXT_FIT or TPK_PLACE_GROUPS */
 } tpk_plan_opts;
 
 typedef struct {
@@ -167,6 +173,24 @@ int tpk_plan_worklists(const tpk_plan* plan, int32_t* qt_q0, int32_t* qt_nq,
  * arrays (TPK_FIELD_FWD_RAW_BEGIN, TPK_FIELD_FWD_RAW) for
  * tpk_gather_to_forwarded and tpk_sum_to_forwarded. */
 int tpk_plan_raw_of_forwarded(const tpk_plan* plan, int32_t* fwd_raw_begin, int32_t* fwd_raw);
+
+/* Rows across ranks (no counterpart on the pages, which run one GPU per
+ * row batch): the mask never crosses a row ("Prefix Tree Packing in ART",
+ * section "Token-mixing layers": a token sees only its own root-to-leaf
+ * path), so rows are independent units of work and data-parallel ranks can
+ * take whole rows with nothing exchanged.  A row's work is its useful
+ * (query, key) pairs, the sum of depth + 1 over its forwarded positions.
+ * Rows are assigned longest first, each to the rank with the least work so
+ * far (ties: lower row index first, then the lower rank), which keeps every
+ * rank's total within one row's work of the lightest rank's.
+ *   rank_of_row: host int32 [n_rows], written (rank 0 .. world-1 per row);
+ *   rank_pairs:  host int64 [world], each rank's total pairs (may be NULL).
+ * A rank runs the sequences whose row it owns (row_of_seq of
+ * tpk_plan_export), planned as a batch of their own with their global row
+ * as the group and TPK_PLACE_GROUPS, which gives back exactly those rows.
+ * Returns TPK_E_ARG for
+ * a NULL plan or rank_of_row, or world <= 0. */
+int tpk_plan_shard_rows(const tpk_plan* plan, int32_t world, int32_t* rank_of_row, int64_t* rank_pairs);
 
 /* Device image of the plan.  The caller allocates tpk_plan_device_bytes()
  * bytes of device memory (256-byte aligned) and uploads the image with

@@ -233,6 +233,23 @@ def place_next_fit(groups, capacity):
     return rows
 
 
+def place_one_row_per_group(groups, keys, capacity):
+    """One row per placement group, rows in increasing group id (no
+    counterpart on the pages: it lets a data-parallel rank that owns some
+    rows of a larger batch plan its sequences with their global row index as
+    the group and get exactly those rows back).  A group that does not fit in
+    one row is an error."""
+    rows = []
+    for g in sorted(range(len(groups)), key=lambda g: keys[g]):
+        row = _Row()
+        for leaf in groups[g]:
+            row.take(leaf)
+        if row.load > capacity:
+            raise PlanError("group larger than a row")
+        rows.append(row)
+    return rows
+
+
 # --------------------------------------------------------------------------
 # 4. layout
 # --------------------------------------------------------------------------
@@ -265,12 +282,13 @@ def plan(sequences, trained=None, group_ids=None, min_shared=64,
             return int(group_ids[leaf.representative])
         return leaf.path[0][0]
     leaves_in_input_order = sorted(leaves, key=lambda lf: lf.representative)
-    groups, index = [], {}
+    groups, index, keys = [], {}, []
     for leaf in leaves_in_input_order:
         g = group_of(leaf)
         if g not in index:
             index[g] = len(groups)
             groups.append([])
+            keys.append(g)
         groups[index[g]].append(leaf)
 
     for leaf in leaves:
@@ -280,6 +298,8 @@ def plan(sequences, trained=None, group_ids=None, min_shared=64,
         rows = place_best_fit_decreasing(groups, row_capacity)
     elif placement == "next_fit":
         rows = place_next_fit(groups, row_capacity)
+    elif placement == "groups":
+        rows = place_one_row_per_group(groups, keys, row_capacity)
     else:
         raise PlanError("unknown placement")
 

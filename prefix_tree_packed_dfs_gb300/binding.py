@@ -18,12 +18,14 @@ STATUS = {
 BWD_PREP, BWD_DKDV, BWD_DQ = 0, 1, 2
 PLACE_BFD = 0
 PLACE_NEXT_FIT = 1
+PLACE_GROUPS = 2
 FIELD_DEPTH, FIELD_TOKEN_INDEX, FIELD_SUBTREE_END, FIELD_PARENT = 0, 1, 2, 3
 FIELD_FWD_RAW_BEGIN, FIELD_FWD_RAW = 4, 5
 
 # every symbol include/tpk.h declares
 EXPORTS = [
     "tpk_plan_build", "tpk_plan_info_get", "tpk_plan_export", "tpk_plan_worklists", "tpk_plan_raw_of_forwarded",
+    "tpk_plan_shard_rows",
     "tpk_plan_device_bytes", "tpk_plan_field_offset", "tpk_plan_upload", "tpk_plan_destroy",
     "tpk_rope_by_depth", "tpk_attn_workspace_bytes", "tpk_tree_attn_fwd", "tpk_tree_attn_bwd",
     "tpk_tree_attn_bwd_phase", "tpk_tree_attn_bwd_noalloc", "tpk_selftest_wait_timeout",
@@ -67,6 +69,7 @@ def _sig(lib):
     lib.tpk_plan_raw_of_forwarded.argtypes = [P, P, P]
     lib.tpk_plan_device_bytes.argtypes = [P]
     lib.tpk_plan_device_bytes.restype = SZ
+    lib.tpk_plan_shard_rows.argtypes = [P, I32, P, P]
     lib.tpk_plan_field_offset.argtypes = [P, I32, ctypes.POINTER(SZ)]
     lib.tpk_plan_upload.argtypes = [P, P, P]
     lib.tpk_plan_destroy.argtypes = [P]

@@ -1,8 +1,10 @@
 // C ABI: planner entry points, device image upload, status strings.
 #include <cuda_runtime_api.h>
 
+#include <algorithm>
 #include <cstring>
 #include <new>
+#include <numeric>
 #include <utility>
 #include <vector>
 
@@ -149,6 +151,31 @@ int tpk_plan_raw_of_forwarded(const tpk_plan* plan, int32_t* fwd_raw_begin, int3
   if (!plan) return TPK_E_ARG;
   copy_out(fwd_raw_begin, plan->p.fwd_raw_begin);
   copy_out(fwd_raw, plan->p.fwd_raw);
+  return TPK_OK;
+}
+
+int tpk_plan_shard_rows(const tpk_plan* plan, int32_t world, int32_t* rank_of_row, int64_t* rank_pairs) {
+  if (!plan || world <= 0 || !rank_of_row) return TPK_E_ARG;
+  const tpk::Plan& P = plan->p;
+  const size_t rows = P.row_loads.size();
+  // a row's work: its useful (query, key) pairs, sum of depth + 1 over its positions
+  std::vector<int64_t> pairs(rows, 0);
+  for (size_t r = 0; r < rows; ++r)
+    for (int64_t f = P.row_offsets[r]; f < P.row_offsets[r + 1]; ++f) pairs[r] += static_cast<int64_t>(P.depth[f]) + 1;
+  // longest processing time first: heaviest row to the least loaded rank
+  // (ties: the lower row, the lower rank), so the assignment is reproducible
+  std::vector<int32_t> order(rows);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return pairs[a] > pairs[b]; });
+  std::vector<int64_t> load(static_cast<size_t>(world), 0);
+  for (const int32_t r : order) {
+    size_t k = 0;
+    for (size_t j = 1; j < load.size(); ++j)
+      if (load[j] < load[k]) k = j;
+    rank_of_row[r] = static_cast<int32_t>(k);
+    load[k] += pairs[r];
+  }
+  if (rank_pairs) std::copy(load.begin(), load.end(), rank_pairs);
   return TPK_OK;
 }
 

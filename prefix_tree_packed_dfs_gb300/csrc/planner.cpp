@@ -105,7 +105,8 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
                const PlanOptions& opts, Plan* out) {
   if (!tokens || !seq_offsets || !out || n_seqs <= 0) return TPK_E_ARG;
   if (opts.row_capacity <= 0) return TPK_E_ARG;
-  if (opts.placement != TPK_PLACE_BFD && opts.placement != TPK_PLACE_NEXT_FIT) return TPK_E_ARG;
+  if (opts.placement != TPK_PLACE_BFD && opts.placement != TPK_PLACE_NEXT_FIT && opts.placement != TPK_PLACE_GROUPS)
+    return TPK_E_ARG;
   if (seq_offsets[0] != 0) return TPK_E_ARG;
   for (int32_t s = 0; s < n_seqs; ++s)
     if (seq_offsets[s + 1] <= seq_offsets[s]) return TPK_E_ARG;
@@ -210,12 +211,17 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   std::sort(by_input.begin(), by_input.end(),
             [&](int32_t a, int32_t b) { return leaves[a].rep() < leaves[b].rep(); });
   std::vector<std::vector<int32_t>> groups;   // in first-appearance order
+  std::vector<int64_t> group_key;             // the id of each group
   {
     std::unordered_map<int64_t, size_t> index;
     for (int32_t li : by_input) {
       const int64_t g = group_ids ? group_ids[leaves[li].rep()] : leaves[li].path.front();
       auto it = index.find(g);
-      if (it == index.end()) { it = index.emplace(g, groups.size()).first; groups.emplace_back(); }
+      if (it == index.end()) {
+        it = index.emplace(g, groups.size()).first;
+        groups.emplace_back();
+        group_key.push_back(g);
+      }
       groups[it->second].push_back(li);
     }
   }
@@ -240,6 +246,16 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
         if (best < 0) best = static_cast<int64_t>(new_bin());
         take(bins[best], li, leaves[li], segs);
       }
+    }
+  } else if (opts.placement == TPK_PLACE_GROUPS) {
+    // one row per group, rows in increasing group id
+    std::vector<int32_t> gorder(groups.size());
+    std::iota(gorder.begin(), gorder.end(), 0);
+    std::sort(gorder.begin(), gorder.end(), [&](int32_t a, int32_t b) { return group_key[a] < group_key[b]; });
+    for (int32_t g : gorder) {
+      const size_t b = new_bin();
+      for (int32_t li : groups[g]) take(bins[b], li, leaves[li], segs);
+      if (bins[b].load > C) return TPK_E_SEQ_TOO_LONG;
     }
   } else {
     for (auto& g : groups)

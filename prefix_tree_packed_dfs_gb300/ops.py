@@ -51,7 +51,7 @@ class Plan:
         if gr is not None and len(gr) != n:
             raise ValueError("group_ids must have one id per sequence")
         opts = B.PlanOpts(int(row_capacity), int(min_shared),
-                          B.PLACE_BFD if placement == "bfd" else B.PLACE_NEXT_FIT)
+                          {"bfd": B.PLACE_BFD, "next_fit": B.PLACE_NEXT_FIT, "groups": B.PLACE_GROUPS}[placement])
         h = ctypes.c_void_p()
         st = lib.tpk_plan_build(tokens.ctypes.data, offs.ctypes.data, n,
                                 None if tr is None else tr.ctypes.data,
@@ -117,6 +117,33 @@ class Plan:
         B.check(self._lib.tpk_plan_raw_of_forwarded(self._h, begin.ctypes.data, raw.ctypes.data),
                 "tpk_plan_raw_of_forwarded")
         return begin, raw
+
+    def shard_rows(self, world):
+        """Whole rows to `world` data-parallel ranks, heaviest row first to the
+        least-loaded rank (work = useful pairs).  Returns (rank_of_row int32
+        [n_rows], rank_pairs int64 [world])."""
+        rows = self.info["n_rows"]
+        rank_of_row, rank_pairs = np.zeros(rows, np.int32), np.zeros(world, np.int64)
+        B.check(self._lib.tpk_plan_shard_rows(self._h, int(world), rank_of_row.ctypes.data, rank_pairs.ctypes.data),
+                "tpk_plan_shard_rows")
+        return rank_of_row, rank_pairs
+
+    def sequences_of_rank(self, rank_of_row, rank):
+        """Indices (input order) of the sequences whose row `rank` owns."""
+        return np.flatnonzero(np.asarray(rank_of_row)[self.export()["row_of_seq"]] == rank)
+
+    def rank_plan(self, sequences, rank_of_row, rank, row_capacity, min_shared=64, trained=None):
+        """The plan of rank `rank`'s rows (``shard_rows``): its sequences,
+        planned with their row in this plan as the group and one row per
+        group, i.e. exactly those rows.  Returns (plan, sequence indices);
+        ``sequences`` / ``trained`` are the inputs this plan was built from."""
+        idx = self.sequences_of_rank(rank_of_row, rank)
+        rows = self.export()["row_of_seq"][idx]
+        sub = Plan.from_sequences([sequences[i] for i in idx],
+                                  trained=None if trained is None else [trained[i] for i in idx],
+                                  group_ids=rows, row_capacity=row_capacity, min_shared=min_shared,
+                                  placement="groups")
+        return sub, idx
 
     def device_bytes(self):
         return int(self._lib.tpk_plan_device_bytes(self._h))

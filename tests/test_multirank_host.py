@@ -1,10 +1,12 @@
-"""The bench's multi-rank host logic on CPU with two gloo ranks.
+"""Multi-rank host logic on CPU with gloo ranks.
 
-Rows are independent, so N GPUs run N batches of the same shape (weak
-scaling) with no collective on the data path.  The only cross-rank steps
-are the timing barrier and the max-over-ranks reduction of the step time;
-here two CPU processes check them: distinct per-rank batches, the slowest
-rank's time on every rank, and the whole-job value from it.
+Rows are independent, so data-parallel ranks need no collective on the data
+path.  bench.py runs N batches of the same shape (weak scaling); the only
+cross-rank steps are the timing barrier and the max-over-ranks reduction of
+the step time.  A single batch splits across ranks by whole rows
+(tpk_plan_shard_rows, longest first to the least-loaded rank), each rank
+planning its rows' sequences as a batch of its own that reproduces exactly
+those rows.
 """
 import os
 import socket
@@ -73,3 +75,119 @@ def test_source_digest_ignores_comments(tmp_path, monkeypatch):
     assert bench.source_digest() == d0
     f.write_text(f.read_text().replace("kThreads = 256", "kThreads = 128"))
     assert bench.source_digest() != d0
+    # host-side API code does not change what the kernels move
+    d1 = bench.source_digest()
+    api = root / "prefix_tree_packed_dfs_gb300" / "csrc" / "api.cpp"
+    api.write_text(api.read_text() + "\nint tpk_unused_probe() { return 0; }\n")
+    assert bench.source_digest() == d1
+    pl = root / "prefix_tree_packed_dfs_gb300" / "csrc" / "planner.cpp"
+    pl.write_text(pl.read_text().replace("kOrderChunk = 128", "kOrderChunk = 64"))
+    assert bench.source_digest() != d1          # the launch order does
+
+
+# ---------------------------------------------------------------- rows across ranks
+def _plan(name):
+    import workloads
+    from prefix_tree_packed_dfs_gb300 import ops
+    w = workloads.get(name)
+    return w, ops.Plan.from_sequences(w.sequences, group_ids=w.group_ids, row_capacity=w.row_capacity,
+                                      min_shared=w.min_shared)
+
+
+def _row_pairs(plan):
+    """Useful pairs per row from the exported layout: sum of depth + 1."""
+    import numpy as np
+    ex = plan.export()
+    off, depth = ex["row_offsets"], ex["depth"].astype(np.int64)
+    return np.array([int((depth[off[r]:off[r + 1]] + 1).sum()) for r in range(len(off) - 1)], np.int64)
+
+
+@pytest.mark.parametrize("name", ["grpo", "agentic", "deep_small", "tiny"])
+@pytest.mark.parametrize("world", [1, 2, 3, 4, 8])
+def test_shard_rows_is_a_balanced_partition(name, world):
+    import numpy as np
+    w, plan = _plan(name)
+    pairs = _row_pairs(plan)
+    rank_of_row, rank_pairs = plan.shard_rows(world)
+    assert rank_of_row.min() >= 0 and rank_of_row.max() < world
+    for k in range(world):
+        assert rank_pairs[k] == pairs[rank_of_row == k].sum()
+    assert rank_pairs.sum() == plan.info["useful_pairs"]
+    # greedy least-loaded assignment: no rank ends more than one row above the lightest
+    assert rank_pairs.max() - rank_pairs.min() <= pairs.max()
+    if world >= len(pairs):
+        assert np.bincount(rank_of_row, minlength=world).max() == 1
+    again, _ = plan.shard_rows(world)
+    assert np.array_equal(again, rank_of_row)          # reproducible
+    # every sequence belongs to exactly one rank
+    seqs = [plan.sequences_of_rank(rank_of_row, k) for k in range(world)]
+    allseq = np.sort(np.concatenate(seqs))
+    assert np.array_equal(allseq, np.arange(len(w.sequences)))
+
+
+def test_shard_rows_within_grahams_bound_of_the_optimum():
+    """Longest-processing-time-first list scheduling is within
+    4/3 - 1/(3m) of the best makespan (Graham 1969); the optimum here is by
+    brute force over every assignment of the GRPO batch's 7 rows."""
+    import itertools
+    w, plan = _plan("grpo")
+    pairs = _row_pairs(plan)
+    for m in (2, 3):
+        best = min(max(sum(int(pairs[r]) for r in range(len(pairs)) if a[r] == k) for k in range(m))
+                   for a in itertools.product(range(m), repeat=len(pairs)))
+        _, rank_pairs = plan.shard_rows(m)
+        assert best <= rank_pairs.max() <= (4 / 3 - 1 / (3 * m)) * best
+
+
+def test_shard_rows_rejects_bad_arguments():
+    from prefix_tree_packed_dfs_gb300 import binding
+    lib = binding.load()
+    import ctypes
+    assert lib.tpk_plan_shard_rows(None, 2, ctypes.c_void_p(16), None) == -1
+    _, plan = _plan("tiny")
+    assert lib.tpk_plan_shard_rows(plan.handle, 0, ctypes.c_void_p(16), None) == -1
+    assert lib.tpk_plan_shard_rows(plan.handle, 2, None, None) == -1
+
+
+def _shard_worker(rank, world, port, out):
+    import numpy as np
+    import torch.distributed as dist
+    import workloads
+    from prefix_tree_packed_dfs_gb300 import ops
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # every rank plans the whole batch on its host, takes its rows' sequences
+        # and plans them as its own batch: nothing but this listing crosses ranks
+        w = workloads.get("grpo")
+        full = ops.Plan.from_sequences(w.sequences, group_ids=w.group_ids, row_capacity=w.row_capacity,
+                                       min_shared=w.min_shared)
+        rank_of_row, rank_pairs = full.shard_rows(world)
+        sub, mine = full.rank_plan(w.sequences, rank_of_row, rank, w.row_capacity, w.min_shared)
+        # the rank's plan is its rows of the whole batch's plan, row for row
+        ex_full, ex_sub = full.export(), sub.export()
+        rows = np.flatnonzero(rank_of_row == rank)
+        same = [np.array_equal(ex_full[k][ex_full["row_offsets"][r]:ex_full["row_offsets"][r + 1]],
+                               ex_sub[k][ex_sub["row_offsets"][j]:ex_sub["row_offsets"][j + 1]])
+                for j, r in enumerate(rows) for k in ("fwd_token", "depth")]
+        got = [None] * world
+        dist.all_gather_object(got, (mine.tolist(), sub.info["n_raw"], sub.info["useful_pairs"]))
+        out[rank] = (got, int(rank_pairs[rank]), full.info["n_raw"], len(w.sequences), all(same),
+                     sub.info["n_rows"] == len(rows))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_split_one_batch_by_rows():
+    world, port = 2, _free_port()
+    out = mp.get_context("spawn").Manager().dict()
+    mp.start_processes(_shard_worker, args=(world, port, out), nprocs=world, join=True, start_method="spawn")
+    got0, pairs0, n_raw, n_seq, same0, nrows0 = out[0]
+    got1, pairs1, _, _, same1, nrows1 = out[1]
+    assert got0 == got1                                   # both ranks see the same split
+    seqs = sorted(got0[0][0] + got0[1][0])
+    assert seqs == list(range(n_seq))                     # each sequence on exactly one rank
+    assert got0[0][1] + got0[1][1] == n_raw               # raw tokens add up
+    # each rank's plan holds exactly its rows: same tokens and depths, same work
+    assert same0 and same1 and nrows0 and nrows1
+    assert got0[0][2] == pairs0 and got0[1][2] == pairs1

@@ -215,3 +215,41 @@ def test_raw_of_forwarded_is_token_index_inverted(lib, name):
     assert np.array_equal(begin, exp_begin)
     assert np.array_equal(raw, exp_raw)
     assert np.array_equal(raw[begin[:-1]], np.asarray(ref["fwd_src"]))
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_one_row_per_group_bit_exact(lib, seed):
+    """Placement "groups": one row per group id, rows in increasing id --
+    library and oracle agree bit for bit, and every row holds exactly one
+    group's sequences."""
+    rng = np.random.Generator(np.random.PCG64(500 + seed))
+    seqs = _random_case(rng, int(rng.integers(2, 6)), 12, 24)
+    groups = (rng.integers(0, 4, size=len(seqs)) * 3 + 7).astype(np.int32)     # sparse, unordered ids
+    _, got = _compare(seqs, None, groups, int(rng.choice([0, 2, 5])), 1 << 20, "groups")
+    # identical sequences are one leaf, placed with the group of the lowest-index copy
+    first = {}
+    eff = np.array([groups[first.setdefault(tuple(x.tolist()), i)] for i, x in enumerate(seqs)])
+    ids = sorted(set(eff.tolist()))
+    assert got.info["n_rows"] == len(ids)
+    assert np.array_equal(got.export()["row_of_seq"], np.searchsorted(ids, eff))
+
+
+def test_one_row_per_group_rebuilds_the_rows_of_a_plan(lib):
+    """A BFD plan's rows, planned again with each sequence's row as its group,
+    come back identical (the per-rank plan of a row-sharded batch)."""
+    w = workloads.get("grpo")
+    full = _cpp_plan(w.sequences, None, w.group_ids, w.min_shared, w.row_capacity)
+    rows = full.export()["row_of_seq"]
+    _, again = _compare(w.sequences, None, rows, w.min_shared, w.row_capacity, "groups")
+    a, b = full.export(), again.export()
+    for k in ("row_offsets", "fwd_token", "depth", "parent", "subtree_end", "token_index", "row_of_seq"):
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_one_row_per_group_rejects_an_oversized_group(lib):
+    from prefix_tree_packed_dfs_gb300 import binding as B
+    seqs = [np.arange(40, dtype=np.int32) + 100 * i for i in range(3)]
+    with pytest.raises(B.TpkError):
+        _cpp_plan(seqs, None, np.zeros(3, np.int32), 4, 100, "groups")
+    with pytest.raises(op.PlanError):
+        op.plan(seqs, group_ids=np.zeros(3, np.int32), row_capacity=100, min_shared=4, placement="groups")
