@@ -734,6 +734,31 @@ def run_planner(a):
                           "library_ms": ms, "oracle_ms": 1e3 * t_or, "oracle_over_library": t_or * 1e3 / ms,
                           "library_raw_tokens_per_s": info["n_raw"] / ms * 1e3, "host_threads": cores,
                           "library_threads": 1}), flush=True)
+    # scaling with the number of leaves, on stand-ins for the multi-task
+    # batches of "Prefix Tree Packing in ART" (section "Bin packing, with a
+    # twist"), whose table gives tree walk / bin packing ms and rows for the
+    # same group and completion counts (another machine, another language:
+    # context only)
+    pages = {12: (0.9, 1.4, 15), 48: (9.6, 4.2, 61), 192: (42.0, 48.7, 227), 768: (291.2, 743.5, 918)}
+    for g, n_comp in workloads.CURRICULUM.items():
+        w = workloads.get("curriculum_%d" % g)
+        times = []
+        for _ in range(3):
+            t0 = time.perf_counter()
+            plan = ops.Plan.from_sequences(w.sequences, group_ids=w.group_ids, row_capacity=w.row_capacity,
+                                           min_shared=w.min_shared)
+            times.append(time.perf_counter() - t0)
+        t0 = time.perf_counter()
+        op.plan(w.sequences, group_ids=w.group_ids, min_shared=w.min_shared, row_capacity=w.row_capacity)
+        t_or = time.perf_counter() - t0
+        info = plan.info
+        ms = 1e3 * statistics.median(times)
+        walk, pack, rows = pages[g]
+        print(json.dumps({"mode": "planner_scaling", "workload": w.name, "groups": g, "completions": n_comp,
+                          "raw_tokens": info["n_raw"], "forwarded_tokens": info["n_fwd"], "rows": info["n_rows"],
+                          "library_ms": ms, "oracle_ms": 1e3 * t_or, "host_threads": cores, "library_threads": 1,
+                          "pages_context": {"tree_walk_ms": walk, "bin_packing_ms": pack, "rows": rows,
+                                            "batch_shape": "not given on the page"}}), flush=True)
 
 
 def main():

@@ -43,6 +43,14 @@ def test_workloads_bit_exact(lib, name):
     _compare(w.sequences, None, w.group_ids, w.min_shared, w.row_capacity)
 
 
+@pytest.mark.parametrize("name", ["curriculum_12", "curriculum_48"])
+def test_curriculum_batches_bit_exact(lib, name):
+    """The planner-scaling stand-ins (many groups under shared task prompts)."""
+    w = workloads.get(name)
+    ref, got = _compare(w.sequences, None, w.group_ids, w.min_shared, w.row_capacity)
+    assert got.info["n_leaves"] == workloads.CURRICULUM[int(name.split("_")[1])]
+
+
 @pytest.mark.slow
 def test_deep_workload_bit_exact(lib):
     w = workloads.get("deep")

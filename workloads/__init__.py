@@ -215,6 +215,36 @@ def deep_small():
                     6000, backward=True)
 
 
+# Planner-scaling batches.  "Prefix Tree Packing in ART" (section "Bin
+# packing, with a twist") times its tree walk and bin packing on a
+# "multi-task curriculum" batch of 12 / 48 / 192 / 768 groups with 105 / 450 /
+# 1,668 / 6,686 completions, without giving the batch's shape.  These stand
+# in for it with the same counts: tasks whose system prompt is shared by
+# several groups (so one tree spans groups), a prompt per group, completions
+# of 256-3072 tokens, rows of 16,384.
+CURRICULUM = {12: 105, 48: 450, 192: 1668, 768: 6686}
+
+
+def curriculum(n_groups):
+    n_comp = CURRICULUM[n_groups]
+    tk = _Tokens(7000 + n_groups)
+    n_tasks = max(2, n_groups // 6)
+    systems = tk.siblings([int(x) for x in tk.rng.integers(200, 801, size=n_tasks)])
+    base, extra = divmod(n_comp, n_groups)
+    counts = [base + (1 if g < extra else 0) for g in range(n_groups)]
+    first_of_prompts = [set() for _ in range(n_tasks)]   # a task's prompts are siblings
+    seqs, groups = [], []
+    for g in range(n_groups):
+        t = g % n_tasks
+        prompt = tk.draw(int(tk.rng.integers(100, 501)), avoid_first=first_of_prompts[t])
+        first_of_prompts[t].add(int(prompt[0]))
+        for comp in tk.siblings([int(x) for x in tk.rng.integers(256, 3073, size=counts[g])]):
+            seqs.append(np.concatenate([systems[t], prompt, comp]))
+            groups.append(g)
+    return Workload("curriculum_%d" % n_groups, seqs, np.asarray(groups, np.int32), None, 64, 16384,
+                    16, 8, 128, 1e6, 7000 + n_groups)
+
+
 def get(name):
     if name == "tiny":
         return tiny(512)
@@ -228,6 +258,8 @@ def get(name):
         return deep()
     if name == "deep_small":
         return deep_small()
+    if name.startswith("curriculum_"):
+        return curriculum(int(name.split("_")[1]))
     if name.startswith("sweep_"):
         parts = name.split("_")
         return sweep(float(parts[1]), seqpack=len(parts) > 2 and parts[2] == "seqpack")
