@@ -293,21 +293,24 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
       for (int32_t s : leaf.path) {
         if (placed[s] < 0) {
           const int32_t f0 = static_cast<int32_t>(P.depth.size());
+          const int32_t L = segs[s].end - segs[s].start;
           placed[s] = f0;
           placed_inst[s] = static_cast<int32_t>(inst_start.size());
           touched.push_back(s);
           inst_start.push_back(f0);
-          inst_len.push_back(segs[s].end - segs[s].start);
+          inst_len.push_back(L);
           inst_parent.push_back(prev >= 0 ? placed_inst[prev] : -1);
-          for (int32_t p = segs[s].start; p < segs[s].end; ++p) {
-            const int32_t f = static_cast<int32_t>(P.depth.size());
-            P.depth.push_back(p);
-            P.fwd_token.push_back(tokens[rep_off + p]);
-            if (p > segs[s].start) P.parent.push_back(f - 1);
-            else if (prev >= 0) P.parent.push_back(placed[prev] + (segs[prev].end - 1 - segs[prev].start));
-            else P.parent.push_back(-1);
-            inst_of[f] = placed_inst[s];
-          }
+          // one segment = a chain: depths segs[s].start.., tokens copied,
+          // each position's parent the one before it (the first one's: the
+          // last position of the parent segment, or none at a root)
+          P.depth.resize(f0 + L);
+          P.fwd_token.resize(f0 + L);
+          P.parent.resize(f0 + L);
+          std::iota(P.depth.begin() + f0, P.depth.end(), segs[s].start);
+          std::memcpy(P.fwd_token.data() + f0, tokens + rep_off + segs[s].start, sizeof(int32_t) * L);
+          P.parent[f0] = prev >= 0 ? placed[prev] + (segs[prev].end - 1 - segs[prev].start) : -1;
+          std::iota(P.parent.begin() + f0 + 1, P.parent.end(), f0);
+          std::fill(inst_of.begin() + f0, inst_of.begin() + f0 + L, placed_inst[s]);
         }
         prev = s;
       }
@@ -456,9 +459,13 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   place(P.off_kt_qb_begin, 4 * P.kt_qb_begin.size());
   place(P.off_qb, 4 * P.qb.size());
   place(P.off_kt_order, 4 * P.kt_order.size());
-  P.image.assign(off, 0);
+  // every byte is written once: the sections by copy, the padding after
+  // each section (up to the next 256-byte boundary) with zeros
+  P.image.resize(off);
   auto put = [&](size_t field, const std::vector<int32_t>& v) {
     if (!v.empty()) std::memcpy(P.image.data() + field, v.data(), 4 * v.size());
+    const size_t end = field + 4 * v.size();
+    std::memset(P.image.data() + end, 0, std::min(align256(end), off) - end);
   };
   put(P.off_depth, P.depth);
   put(P.off_token_index, P.token_index);

@@ -5,9 +5,33 @@
 #pragma once
 #include <cstdint>
 #include <cstddef>
+#include <memory>
+#include <new>
+#include <utility>
 #include <vector>
 
 namespace tpk {
+
+// Allocator whose resize() leaves new elements uninitialised: for a buffer
+// that is written in full right after it is sized (the device image).
+template <typename T>
+struct UninitAllocator : std::allocator<T> {
+  template <typename U>
+  struct rebind {
+    using other = UninitAllocator<U>;
+  };
+  UninitAllocator() noexcept = default;
+  template <typename U>
+  UninitAllocator(const UninitAllocator<U>&) noexcept {}
+  template <typename U>
+  void construct(U* p) noexcept {
+    ::new (static_cast<void*>(p)) U;
+  }
+  template <typename U, typename... A>
+  void construct(U* p, A&&... a) {
+    ::new (static_cast<void*>(p)) U(std::forward<A>(a)...);
+  }
+};
 
 constexpr int kTile = 128;   // query / key tile height of the attention kernels
 
@@ -37,7 +61,7 @@ struct Plan {
   std::vector<int32_t> kt_k0, kt_nk, kt_qb_begin, qb, kt_order;
 
   // device image: every array above that a kernel reads, 256-byte aligned sections
-  std::vector<uint8_t> image;
+  std::vector<uint8_t, UninitAllocator<uint8_t>> image;
   size_t off_depth = 0, off_token_index = 0, off_subtree_end = 0, off_parent = 0;
   size_t off_fwd_raw_begin = 0, off_fwd_raw = 0;
   size_t off_qt_q0 = 0, off_qt_nq = 0, off_qt_kb_begin = 0, off_kb = 0, off_qt_order = 0;
