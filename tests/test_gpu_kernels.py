@@ -243,7 +243,8 @@ def _sample_raw(case, n, seed):
     return sorted(picks)
 
 
-FULL = ["grpo", "agentic"] + ["sweep_%.2f" % r for r in workloads.SWEEP_RHOS] + ["deep", "sweep_3.56_mha"]
+FULL = (["grpo", "agentic"] + ["sweep_%.2f" % r for r in workloads.SWEEP_RHOS] + ["deep", "sweep_3.56_mha"]
+        + ["curriculum_12"])   # system prompts shared across groups, 105 short leaves
 
 
 def _full_workload(name):
