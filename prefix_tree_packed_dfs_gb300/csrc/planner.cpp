@@ -35,9 +35,11 @@
 #include "planner.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <limits>
 #include <numeric>
+#include <thread>
 #include <unordered_map>
 
 #include "tpk.h"
@@ -98,6 +100,27 @@ void take(Bin& b, int32_t leaf_id, const Leaf& leaf, const std::vector<Segment>&
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// fn(i) for i in [0, n) on up to 16 host threads; every i writes only its own
+// outputs, so the result does not depend on the schedule
+template <typename Fn>
+void parallel_for(int64_t n, Fn fn) {
+  const int64_t hw = std::max<int64_t>(1, std::thread::hardware_concurrency());
+  const int64_t nt = std::min<int64_t>({hw, 16, n});
+  if (nt <= 1) {
+    for (int64_t i = 0; i < n; ++i) fn(i);
+    return;
+  }
+  std::atomic<int64_t> next{0};
+  auto worker = [&]() {
+    for (int64_t i; (i = next.fetch_add(1, std::memory_order_relaxed)) < n;) fn(i);
+  };
+  std::vector<std::thread> pool;
+  pool.reserve(static_cast<size_t>(nt - 1));
+  for (int64_t t = 1; t < nt; ++t) pool.emplace_back(worker);
+  worker();
+  for (auto& th : pool) th.join();
+}
+
 }  // namespace
 
 int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs,
@@ -126,7 +149,8 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
 
   // ---- 1. symbols --------------------------------------------------------
   std::vector<uint64_t> sym(R);
-  for (int32_t s = 0; s < n_seqs; ++s) {
+  parallel_for(n_seqs, [&](int64_t si) {
+    const int32_t s = static_cast<int32_t>(si);
     const int64_t o = seq_offsets[s];
     const int32_t L = len(s);
     for (int32_t p = 0; p < L; ++p) {
@@ -135,7 +159,7 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
       if (flag || p == L - 1) target = (p + 1 < L) ? tokens[o + p + 1] : kEos;
       sym[o + p] = pack_symbol(tokens[o + p], flag, target);
     }
-  }
+  });
 
   // ---- 2. tree -----------------------------------------------------------
   std::vector<int32_t> order(n_seqs);
@@ -267,50 +291,60 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   P.n_rows = static_cast<int64_t>(bins.size());
 
   // ---- 4. layout ----------------------------------------------------------
-  int64_t F = 0;
-  for (auto& b : bins) F += b.load;
+  // Rows are laid out independently: row b fills the forwarded positions
+  // [fbase[b], fbase[b+1]) (its load) and the segment instances (a segment
+  // placed in one row) [ibase[b], ibase[b+1]) (its distinct segments), in
+  // the same order as one sequential pass over the rows would.
+  const size_t nb = bins.size();
+  std::vector<int64_t> fbase(nb + 1, 0), ibase(nb + 1, 0);
+  for (size_t b = 0; b < nb; ++b) {
+    int64_t distinct = 0;
+    for (const uint64_t w : bins[b].held) distinct += __builtin_popcountll(w);
+    fbase[b + 1] = fbase[b] + bins[b].load;
+    ibase[b + 1] = ibase[b] + distinct;
+  }
+  const int64_t F = fbase[nb];
   if (F >= (int64_t{1} << 31)) return TPK_E_OVERFLOW;
   P.F = F;
-  P.depth.reserve(F);
-  P.fwd_token.reserve(F);
-  P.parent.reserve(F);
+  P.depth.resize(F);
+  P.fwd_token.resize(F);
+  P.parent.resize(F);
   P.token_index.assign(R, -1);
   P.row_of_seq.assign(n_seqs, -1);
-  P.row_offsets.push_back(0);
-  // segment instances (a segment placed in one row)
-  std::vector<int32_t> inst_start, inst_len, inst_parent;
+  P.row_offsets.assign(fbase.begin(), fbase.end());
+  P.row_loads.resize(nb);
+  for (size_t b = 0; b < nb; ++b) P.row_loads[b] = bins[b].load;
+  std::vector<int32_t> inst_start(ibase[nb]), inst_len(ibase[nb]), inst_parent(ibase[nb]);
   std::vector<int32_t> inst_of(F);
-  std::vector<int32_t> placed(segs.size(), -1), placed_inst(segs.size(), -1);
-  for (size_t b = 0; b < bins.size(); ++b) {
+  parallel_for(static_cast<int64_t>(nb), [&](int64_t bi) {
+    const size_t b = static_cast<size_t>(bi);
+    std::vector<int32_t> placed(segs.size(), -1), placed_inst(segs.size(), -1);
     std::vector<int32_t> row_leaves = bins[b].leaves;
     std::sort(row_leaves.begin(), row_leaves.end(),
               [&](int32_t x, int32_t y) { return leaves[x].rank < leaves[y].rank; });
-    std::vector<int32_t> touched;
+    int32_t f = static_cast<int32_t>(fbase[b]), inst = static_cast<int32_t>(ibase[b]);
     for (int32_t li : row_leaves) {
       const Leaf& leaf = leaves[li];
       const int64_t rep_off = seq_offsets[leaf.rep()];
       int32_t prev = -1;
       for (int32_t s : leaf.path) {
         if (placed[s] < 0) {
-          const int32_t f0 = static_cast<int32_t>(P.depth.size());
           const int32_t L = segs[s].end - segs[s].start;
-          placed[s] = f0;
-          placed_inst[s] = static_cast<int32_t>(inst_start.size());
-          touched.push_back(s);
-          inst_start.push_back(f0);
-          inst_len.push_back(L);
-          inst_parent.push_back(prev >= 0 ? placed_inst[prev] : -1);
+          placed[s] = f;
+          placed_inst[s] = inst;
+          inst_start[inst] = f;
+          inst_len[inst] = L;
+          inst_parent[inst] = prev >= 0 ? placed_inst[prev] : -1;
           // one segment = a chain: depths segs[s].start.., tokens copied,
           // each position's parent the one before it (the first one's: the
           // last position of the parent segment, or none at a root)
-          P.depth.resize(f0 + L);
-          P.fwd_token.resize(f0 + L);
-          P.parent.resize(f0 + L);
-          std::iota(P.depth.begin() + f0, P.depth.end(), segs[s].start);
-          std::memcpy(P.fwd_token.data() + f0, tokens + rep_off + segs[s].start, sizeof(int32_t) * L);
-          P.parent[f0] = prev >= 0 ? placed[prev] + (segs[prev].end - 1 - segs[prev].start) : -1;
-          std::iota(P.parent.begin() + f0 + 1, P.parent.end(), f0);
-          std::fill(inst_of.begin() + f0, inst_of.begin() + f0 + L, placed_inst[s]);
+          std::iota(P.depth.begin() + f, P.depth.begin() + f + L, segs[s].start);
+          std::memcpy(P.fwd_token.data() + f, tokens + rep_off + segs[s].start, sizeof(int32_t) * L);
+          P.parent[f] = prev >= 0 ? placed[prev] + (segs[prev].end - 1 - segs[prev].start) : -1;
+          std::iota(P.parent.begin() + f + 1, P.parent.begin() + f + L, f);
+          std::fill(inst_of.begin() + f, inst_of.begin() + f + L, inst);
+          f += L;
+          ++inst;
         }
         prev = s;
       }
@@ -322,19 +356,19 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
             P.token_index[o + p] = placed[s] + (p - segs[s].start);
       }
     }
-    for (int32_t s : touched) { placed[s] = -1; placed_inst[s] = -1; }
-    P.row_offsets.push_back(static_cast<int64_t>(P.depth.size()));
-    P.row_loads.push_back(bins[b].load);
-  }
+  });
   P.fwd_src.assign(F, -1);
   for (int64_t r = 0; r < R; ++r)
     if (P.fwd_src[P.token_index[r]] < 0) P.fwd_src[P.token_index[r]] = static_cast<int32_t>(r);
+  // subtree ends, row by row (a parent always lies in its child's row, before it)
   P.subtree_end.resize(F);
-  for (int64_t f = 0; f < F; ++f) P.subtree_end[f] = static_cast<int32_t>(f + 1);
-  for (int64_t f = F - 1; f >= 0; --f) {
-    const int32_t p = P.parent[f];
-    if (p >= 0 && P.subtree_end[f] > P.subtree_end[p]) P.subtree_end[p] = P.subtree_end[f];
-  }
+  parallel_for(static_cast<int64_t>(nb), [&](int64_t b) {
+    for (int64_t f = fbase[b]; f < fbase[b + 1]; ++f) P.subtree_end[f] = static_cast<int32_t>(f + 1);
+    for (int64_t f = fbase[b + 1] - 1; f >= fbase[b]; --f) {
+      const int32_t p = P.parent[f];
+      if (p >= 0 && P.subtree_end[f] > P.subtree_end[p]) P.subtree_end[p] = P.subtree_end[f];
+    }
+  });
   int64_t forks = 0;
   for (auto& s : segs) forks += (s.n_children >= 2);
   P.useful_pairs = 0;
@@ -460,12 +494,18 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   place(P.off_qb, 4 * P.qb.size());
   place(P.off_kt_order, 4 * P.kt_order.size());
   // every byte is written once: the sections by copy, the padding after
-  // each section (up to the next 256-byte boundary) with zeros
+  // each section (up to the next 256-byte boundary) with zeros; copied in
+  // pieces of up to 4 MB on the host threads
   P.image.resize(off);
+  struct Piece { size_t dst; const uint8_t* src; size_t bytes; };
+  std::vector<Piece> pieces;
   auto put = [&](size_t field, const std::vector<int32_t>& v) {
-    if (!v.empty()) std::memcpy(P.image.data() + field, v.data(), 4 * v.size());
-    const size_t end = field + 4 * v.size();
-    std::memset(P.image.data() + end, 0, std::min(align256(end), off) - end);
+    constexpr size_t kPiece = size_t{4} << 20;
+    const auto* src = reinterpret_cast<const uint8_t*>(v.data());
+    const size_t bytes = 4 * v.size();
+    for (size_t b = 0; b < bytes; b += kPiece) pieces.push_back({field + b, src + b, std::min(kPiece, bytes - b)});
+    const size_t end = field + bytes;
+    pieces.push_back({end, nullptr, std::min(align256(end), off) - end});   // zeros
   };
   put(P.off_depth, P.depth);
   put(P.off_token_index, P.token_index);
@@ -483,6 +523,12 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   put(P.off_kt_qb_begin, P.kt_qb_begin);
   put(P.off_qb, P.qb);
   put(P.off_kt_order, P.kt_order);
+  parallel_for(static_cast<int64_t>(pieces.size()), [&](int64_t i) {
+    const Piece& pc = pieces[static_cast<size_t>(i)];
+    if (pc.bytes == 0) return;
+    if (pc.src) std::memcpy(P.image.data() + pc.dst, pc.src, pc.bytes);
+    else std::memset(P.image.data() + pc.dst, 0, pc.bytes);
+  });
   return TPK_OK;
 }
 
