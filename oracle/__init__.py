@@ -15,7 +15,8 @@ Contents
                "The walk"), best-fit-decreasing over marginal cost ("Prefix Tree
                Packing in ART", section "Bin packing, with a twist"), the
                in-order fill ("Prefix Tree Packing in ART", sections "One tree,
-               not one per group" and "Does it actually help?") and the
+               not one per group" and "Does it actually help?"), one row per
+               placement group (no counterpart on the pages) and the
                depth-first layout with depth positions and token_index ("DAG
                packing", sections "The walk" and "Positions"; "TRL Tree Packing
                for AsyncGRPO", section "How tree packing works").

@@ -26,7 +26,11 @@ Steps and the passages they follow
    length of the path segments the row does not hold yet; groups ordered by
    their most expensive leaf; each leaf to the row it leaves least room in),
    and the in-order fill of sections "One tree, not one per group" and "Does
-   it actually help?".
+   it actually help?".  ``place_one_row_per_group`` has no counterpart on the
+   pages: one row per placement group, rows in increasing group id (how a
+   data-parallel rank rebuilds the rows it owns of a larger batch); pinned by
+   replanning a best-fit-decreasing plan with each sequence's row as its group,
+   which must give back the same rows.
 4. ``layout_rows``        -- depth-first layout ("DAG packing", section "The
    walk"; "TRL Tree Packing for AsyncGRPO", section "How tree packing
    works"), positions = tree depth ("DAG packing", section "Positions"),
