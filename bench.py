@@ -49,7 +49,7 @@ LAUNCHES_PER_STEP = 9   # rope, fwd, scatter rows, scatter lse, dO sum, bwd prep
 # (first launch of each kernel; the summary is in profiles/), tagged with a
 # digest of the kernel and planner sources they were built from.  Once those
 # differ the figure no longer describes the kernel and is reported as null.
-TRAFFIC = {"digest": "2d246e4a7659fc59837f558e9b7e61560fa2f0bfbe661b03324a158c568d82ce",
+TRAFFIC = {"digest": "a67187d5be4d584b5484e12cb8c571f1fb7c51f7a43fe4c78ebd2c0017d346bd",
            "fwd": 173898329856, "bwd_dkdv": 475493116928, "bwd_dq": 261452960768}
 
 

@@ -213,6 +213,11 @@ int tpk_plan_shard_rows(const tpk_plan* plan, int32_t world, int32_t* rank_of_ro
 size_t tpk_plan_device_bytes(const tpk_plan* plan);
 int tpk_plan_field_offset(const tpk_plan* plan, int32_t field, size_t* offset);
 int tpk_plan_upload(const tpk_plan* plan, void* dev_image, void* stream);
+
+/* Frees the plan.  The library keeps the host arrays of the last destroyed
+ * plan (at most one plan's worth) and builds the next tpk_plan_build into
+ * them, so a loop that plans one batch per step writes into memory that is
+ * already mapped.  NULL is ignored. */
 void tpk_plan_destroy(tpk_plan* plan);
 
 /* ---- GPU kernels (sm_103a) ---------------------------------------------- */

@@ -3,6 +3,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <numeric>
 #include <utility>
@@ -57,6 +58,28 @@ void copy_out(T* dst, const std::vector<U>& v) {
   if (dst)
     for (size_t i = 0; i < v.size(); ++i) dst[i] = static_cast<T>(v[i]);
 }
+// The arrays of the last destroyed plan, kept for the next build: a training
+// loop plans one batch per step, and building into memory that is already
+// mapped skips the page faults of fresh allocations (most of what the
+// planner spends on a large batch after its parallel passes).  At most one
+// plan's storage is kept.
+std::mutex g_plan_mu;
+tpk::Plan g_plan_free;
+bool g_plan_free_held = false;
+
+void take_plan_storage(tpk::Plan* p) {
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  if (!g_plan_free_held) return;
+  std::swap(*p, g_plan_free);
+  g_plan_free_held = false;
+}
+
+void give_plan_storage(tpk::Plan* p) {
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  std::swap(*p, g_plan_free);   // the previous spare, if any, is freed with the handle
+  g_plan_free_held = true;
+}
+
 }  // namespace
 
 extern "C" {
@@ -74,6 +97,7 @@ int tpk_plan_build(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_
   }
   tpk_plan* h = new (std::nothrow) tpk_plan();
   if (!h) return TPK_E_ARG;
+  take_plan_storage(&h->p);
   int st;
   try {
     st = tpk::build_plan(tokens, seq_offsets, n_seqs, trained, group_ids, o, &h->p);
@@ -232,6 +256,7 @@ void tpk_plan_destroy(tpk_plan* plan) {
     give_pinned(plan->pinned, plan->pinned_bytes);
     plan->pinned = nullptr;
   }
+  give_plan_storage(&plan->p);
   delete plan;
 }
 

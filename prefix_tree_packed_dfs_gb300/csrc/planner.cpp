@@ -141,7 +141,7 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
     if (seq_offsets[s + 1] - seq_offsets[s] > opts.row_capacity) return TPK_E_SEQ_TOO_LONG;
 
   Plan& P = *out;
-  P = Plan();
+  P.reset_keep_capacity();
   P.n_seqs = n_seqs;
   P.R = R;
   P.row_capacity = opts.row_capacity;

@@ -66,6 +66,27 @@ struct Plan {
   size_t off_fwd_raw_begin = 0, off_fwd_raw = 0;
   size_t off_qt_q0 = 0, off_qt_nq = 0, off_qt_kb_begin = 0, off_kb = 0, off_qt_order = 0;
   size_t off_kt_k0 = 0, off_kt_nk = 0, off_kt_qb_begin = 0, off_qb = 0, off_kt_order = 0;
+
+  // Back to an empty plan, keeping every array's allocation: a plan built
+  // into recycled storage writes into memory that is already mapped.  Every
+  // member above is reset here.
+  void reset_keep_capacity() {
+    n_seqs = R = F = n_rows = n_segments = n_leaves = 0;
+    useful_pairs = visited_pairs = max_depth = 0;
+    packing_ratio = row_fill_frac = fork_frac = 0;
+    row_capacity = 0;
+    row_offsets.clear();
+    row_loads.clear();
+    for (std::vector<int32_t>* v : {&row_of_seq, &fwd_token, &fwd_src, &parent, &depth, &token_index, &subtree_end,
+                                    &fwd_raw_begin, &fwd_raw, &qt_q0, &qt_nq, &qt_kb_begin, &kb, &qt_order, &kt_k0,
+                                    &kt_nk, &kt_qb_begin, &qb, &kt_order})
+      v->clear();
+    image.clear();
+    off_depth = off_token_index = off_subtree_end = off_parent = 0;
+    off_fwd_raw_begin = off_fwd_raw = 0;
+    off_qt_q0 = off_qt_nq = off_qt_kb_begin = off_kb = off_qt_order = 0;
+    off_kt_k0 = off_kt_nk = off_kt_qb_begin = off_qb = off_kt_order = 0;
+  }
 };
 
 // Returns a TPK_* status; on success fills *out.
