@@ -357,9 +357,6 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
       }
     }
   });
-  P.fwd_src.assign(F, -1);
-  for (int64_t r = 0; r < R; ++r)
-    if (P.fwd_src[P.token_index[r]] < 0) P.fwd_src[P.token_index[r]] = static_cast<int32_t>(r);
   // subtree ends, row by row (a parent always lies in its child's row, before it)
   P.subtree_end.resize(F);
   parallel_for(static_cast<int64_t>(nb), [&](int64_t b) {
@@ -465,13 +462,45 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   P.kt_order = launch_order(P.kt_qb_begin);
 
   // ---- raw tokens of each forwarded position (counting sort of token_index) --
-  P.fwd_raw_begin.assign(static_cast<size_t>(P.F) + 1, 0);
-  for (int32_t f : P.token_index) ++P.fwd_raw_begin[static_cast<size_t>(f) + 1];
-  for (int64_t f = 0; f < P.F; ++f) P.fwd_raw_begin[f + 1] += P.fwd_raw_begin[f];
-  P.fwd_raw.assign(P.token_index.size(), 0);
+  // A row's positions hold exactly the raw tokens of the row's sequences, so
+  // each row sorts its own: its sequences in increasing index, their tokens
+  // in order, keep every position's list ascending in raw index.  fwd_src,
+  // the owner of a position, is the first of its list.
   {
-    std::vector<int32_t> fill(P.fwd_raw_begin.begin(), P.fwd_raw_begin.end() - 1);
-    for (size_t r = 0; r < P.token_index.size(); ++r) P.fwd_raw[fill[P.token_index[r]]++] = static_cast<int32_t>(r);
+    std::vector<int64_t> seq_begin(nb + 1, 0), raw_base(nb + 1, 0);
+    for (int32_t q = 0; q < n_seqs; ++q) {
+      ++seq_begin[P.row_of_seq[q] + 1];
+      raw_base[P.row_of_seq[q] + 1] += len(q);
+    }
+    for (size_t b = 0; b < nb; ++b) {
+      seq_begin[b + 1] += seq_begin[b];
+      raw_base[b + 1] += raw_base[b];
+    }
+    std::vector<int32_t> row_seqs(static_cast<size_t>(n_seqs));
+    {
+      std::vector<int64_t> at(seq_begin.begin(), seq_begin.end() - 1);
+      for (int32_t q = 0; q < n_seqs; ++q) row_seqs[at[P.row_of_seq[q]]++] = q;
+    }
+    P.fwd_raw_begin.resize(static_cast<size_t>(F) + 1);
+    P.fwd_raw.resize(static_cast<size_t>(R));
+    P.fwd_src.resize(static_cast<size_t>(F));
+    parallel_for(static_cast<int64_t>(nb), [&](int64_t b) {
+      const int64_t f0 = fbase[b], nf = fbase[b + 1] - fbase[b];
+      std::vector<int64_t> at(static_cast<size_t>(nf) + 1, 0);
+      for (int64_t k = seq_begin[b]; k < seq_begin[b + 1]; ++k) {
+        const int32_t q = row_seqs[k];
+        for (int64_t r = seq_offsets[q]; r < seq_offsets[q + 1]; ++r) ++at[P.token_index[r] - f0 + 1];
+      }
+      for (int64_t i = 0; i < nf; ++i) at[i + 1] += at[i];
+      for (int64_t i = 0; i < nf; ++i) P.fwd_raw_begin[f0 + i] = static_cast<int32_t>(raw_base[b] + at[i]);
+      for (int64_t k = seq_begin[b]; k < seq_begin[b + 1]; ++k) {
+        const int32_t q = row_seqs[k];
+        for (int64_t r = seq_offsets[q]; r < seq_offsets[q + 1]; ++r)
+          P.fwd_raw[raw_base[b] + at[P.token_index[r] - f0]++] = static_cast<int32_t>(r);
+      }
+      for (int64_t i = 0; i < nf; ++i) P.fwd_src[f0 + i] = P.fwd_raw[P.fwd_raw_begin[f0 + i]];
+    });
+    P.fwd_raw_begin[F] = static_cast<int32_t>(R);
   }
 
   // ---- device image -------------------------------------------------------
