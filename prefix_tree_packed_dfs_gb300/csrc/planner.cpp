@@ -379,25 +379,33 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   P.fork_frac = static_cast<double>(forks) / static_cast<double>(segs.size());
 
   // ---- 5. work lists ------------------------------------------------------
-  std::vector<int32_t> chain;
-  std::vector<std::pair<int32_t, int32_t>> ivals;
-  P.visited_pairs = 0;
-  for (int64_t row = 0; row < P.n_rows; ++row) {
-    const int32_t rs = static_cast<int32_t>(P.row_offsets[row]);
-    const int32_t re = static_cast<int32_t>(P.row_offsets[row + 1]);
+  // Tiles sit on a per-row grid and read only their row, so every row builds
+  // its own lists (begin offsets local to the row); they are then joined in
+  // row order.
+  struct RowLists {
+    std::vector<int32_t> qt_q0, qt_nq, qt_kb_begin, kb, kt_k0, kt_nk, kt_qb_begin, qb;
+    int64_t visited = 0;
+  };
+  std::vector<RowLists> lists(nb);
+  parallel_for(static_cast<int64_t>(nb), [&](int64_t row) {
+    RowLists& L = lists[static_cast<size_t>(row)];
+    std::vector<int32_t> chain;
+    std::vector<std::pair<int32_t, int32_t>> ivals;
+    const int32_t rs = static_cast<int32_t>(fbase[row]);
+    const int32_t re = static_cast<int32_t>(fbase[row + 1]);
     for (int32_t q0 = rs; q0 < re; q0 += kTile) {
       const int32_t q1 = std::min(q0 + kTile, re);
-      P.qt_q0.push_back(q0);
-      P.qt_nq.push_back(q1 - q0);
-      P.qt_kb_begin.push_back(static_cast<int32_t>(P.kb.size() / 2));
+      L.qt_q0.push_back(q0);
+      L.qt_nq.push_back(q1 - q0);
+      L.qt_kb_begin.push_back(static_cast<int32_t>(L.kb.size() / 2));
       // ancestor chain of q0: proper ancestor instances, then q0's own prefix
       chain.clear();
       for (int32_t i = inst_parent[inst_of[q0]]; i >= 0; i = inst_parent[i]) chain.push_back(i);
       ivals.clear();
       for (size_t c = chain.size(); c-- > 0;) {
-        const int32_t a = inst_start[chain[c]], e = a + inst_len[chain[c]];
-        if (!ivals.empty() && ivals.back().second == a) ivals.back().second = e;
-        else ivals.push_back({a, e});
+        const int32_t a0 = inst_start[chain[c]], e = a0 + inst_len[chain[c]];
+        if (!ivals.empty() && ivals.back().second == a0) ivals.back().second = e;
+        else ivals.push_back({a0, e});
       }
       const int32_t own = inst_start[inst_of[q0]];
       if (own < q0) {
@@ -413,9 +421,9 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
           // Along an ancestor chain subtree ends do not increase, so the last
           // key of the block has the smallest one.
           const bool full = nk == kTile && (k0 + nk - 1 <= q0) && (P.subtree_end[k0 + nk - 1] >= q1);
-          P.kb.push_back(k0);
-          P.kb.push_back(nk | (full ? (1 << 16) : 0));
-          P.visited_pairs += int64_t{kTile} * kTile;
+          L.kb.push_back(k0);
+          L.kb.push_back(nk | (full ? (1 << 16) : 0));
+          L.visited += int64_t{kTile} * kTile;
         }
       }
     }
@@ -426,16 +434,31 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
         qend = std::max(qend, P.subtree_end[j]);
         min_se = std::min(min_se, P.subtree_end[j]);
       }
-      P.kt_k0.push_back(k0);
-      P.kt_nk.push_back(k1 - k0);
-      P.kt_qb_begin.push_back(static_cast<int32_t>(P.qb.size() / 2));
+      L.kt_k0.push_back(k0);
+      L.kt_nk.push_back(k1 - k0);
+      L.kt_qb_begin.push_back(static_cast<int32_t>(L.qb.size() / 2));
       for (int32_t qs = k0; qs < qend; qs += kTile) {
         const int32_t qe = std::min(qs + kTile, qend);
         const bool full = (qe - qs == kTile) && (k1 - 1 <= qs) && (min_se >= qe);
-        P.qb.push_back(qs);
-        P.qb.push_back((qe - qs) | (full ? (1 << 16) : 0));
+        L.qb.push_back(qs);
+        L.qb.push_back((qe - qs) | (full ? (1 << 16) : 0));
       }
     }
+  });
+  P.visited_pairs = 0;
+  for (const RowLists& L : lists) {
+    const size_t kb0 = P.kb.size() / 2, qb0 = P.qb.size() / 2;
+    if (kb0 + L.kb.size() / 2 >= (size_t{1} << 31) || qb0 + L.qb.size() / 2 >= (size_t{1} << 31))
+      return TPK_E_OVERFLOW;
+    P.qt_q0.insert(P.qt_q0.end(), L.qt_q0.begin(), L.qt_q0.end());
+    P.qt_nq.insert(P.qt_nq.end(), L.qt_nq.begin(), L.qt_nq.end());
+    for (const int32_t x : L.qt_kb_begin) P.qt_kb_begin.push_back(static_cast<int32_t>(kb0) + x);
+    P.kb.insert(P.kb.end(), L.kb.begin(), L.kb.end());
+    P.kt_k0.insert(P.kt_k0.end(), L.kt_k0.begin(), L.kt_k0.end());
+    P.kt_nk.insert(P.kt_nk.end(), L.kt_nk.begin(), L.kt_nk.end());
+    for (const int32_t x : L.kt_qb_begin) P.kt_qb_begin.push_back(static_cast<int32_t>(qb0) + x);
+    P.qb.insert(P.qb.end(), L.qb.begin(), L.qb.end());
+    P.visited_pairs += L.visited;
   }
   if (P.kb.size() / 2 >= (size_t{1} << 31) || P.qb.size() / 2 >= (size_t{1} << 31)) return TPK_E_OVERFLOW;
   P.qt_kb_begin.push_back(static_cast<int32_t>(P.kb.size() / 2));
