@@ -49,7 +49,7 @@ LAUNCHES_PER_STEP = 9   # rope, fwd, scatter rows, scatter lse, dO sum, bwd prep
 # (first launch of each kernel; the summary is in profiles/), tagged with a
 # digest of the kernel and planner sources they were built from.  Once those
 # differ the figure no longer describes the kernel and is reported as null.
-TRAFFIC = {"digest": "f37951deb7d9cb90e8a9170565d154c70ce3110f3653a46404f7365d24a871af",
+TRAFFIC = {"digest": "14dbfda3ba6c2d57325fbd48b4040bf4a719361e6dcba7848bee5df9f25d89d3",
            "fwd": 173898329856, "bwd_dkdv": 475493116928, "bwd_dq": 261452960768}
 
 

@@ -121,6 +121,34 @@ void parallel_for(int64_t n, Fn fn) {
   for (auto& th : pool) th.join();
 }
 
+// std::stable_sort of v by comp, on up to 16 host threads: contiguous chunks
+// are sorted stably in parallel, then neighbours are merged stably in rounds
+// (the left range's elements first among equals), which gives exactly the
+// permutation a single stable sort gives.
+template <typename Comp>
+void parallel_stable_sort(std::vector<int32_t>& v, Comp comp) {
+  const int64_t n = static_cast<int64_t>(v.size());
+  const int64_t hw = std::max<int64_t>(1, std::thread::hardware_concurrency());
+  int64_t chunks = std::min<int64_t>({hw, 16, n / 64});
+  if (chunks <= 1) {
+    std::stable_sort(v.begin(), v.end(), comp);
+    return;
+  }
+  std::vector<int64_t> cut(static_cast<size_t>(chunks) + 1);
+  for (int64_t c = 0; c <= chunks; ++c) cut[c] = n * c / chunks;
+  parallel_for(chunks, [&](int64_t c) { std::stable_sort(v.begin() + cut[c], v.begin() + cut[c + 1], comp); });
+  while (cut.size() > 2) {
+    const int64_t pairs = static_cast<int64_t>(cut.size() - 1) / 2;
+    parallel_for(pairs, [&](int64_t i) {
+      std::inplace_merge(v.begin() + cut[2 * i], v.begin() + cut[2 * i + 1], v.begin() + cut[2 * i + 2], comp);
+    });
+    std::vector<int64_t> next;
+    for (size_t i = 0; i < cut.size(); i += 2) next.push_back(cut[i]);
+    if (next.back() != cut.back()) next.push_back(cut.back());
+    cut.swap(next);
+  }
+}
+
 }  // namespace
 
 int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs,
@@ -164,7 +192,7 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   // ---- 2. tree -----------------------------------------------------------
   std::vector<int32_t> order(n_seqs);
   std::iota(order.begin(), order.end(), 0);
-  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
+  parallel_stable_sort(order, [&](int32_t a, int32_t b) {
     return std::lexicographical_compare(sym.begin() + seq_offsets[a], sym.begin() + seq_offsets[a + 1],
                                         sym.begin() + seq_offsets[b], sym.begin() + seq_offsets[b + 1]);
   });
