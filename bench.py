@@ -49,7 +49,7 @@ LAUNCHES_PER_STEP = 9   # rope, fwd, scatter rows, scatter lse, dO sum, bwd prep
 # (first launch of each kernel; the summary is in profiles/), tagged with a
 # digest of the kernel and planner sources they were built from.  Once those
 # differ the figure no longer describes the kernel and is reported as null.
-TRAFFIC = {"digest": "14dbfda3ba6c2d57325fbd48b4040bf4a719361e6dcba7848bee5df9f25d89d3",
+TRAFFIC = {"digest": "4a139e48410d90aa268ade1d0972dfd0011c10f8534963217d8489cb4eb558dc",
            "fwd": 173898329856, "bwd_dkdv": 475493116928, "bwd_dq": 261452960768}
 
 

@@ -176,7 +176,7 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   auto len = [&](int32_t s) { return static_cast<int32_t>(seq_offsets[s + 1] - seq_offsets[s]); };
 
   // ---- 1. symbols --------------------------------------------------------
-  std::vector<uint64_t> sym(R);
+  std::vector<uint64_t, UninitAllocator<uint64_t>> sym(R);   // every element written below
   parallel_for(n_seqs, [&](int64_t si) {
     const int32_t s = static_cast<int32_t>(si);
     const int64_t o = seq_offsets[s];
@@ -343,7 +343,7 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   P.row_loads.resize(nb);
   for (size_t b = 0; b < nb; ++b) P.row_loads[b] = bins[b].load;
   std::vector<int32_t> inst_start(ibase[nb]), inst_len(ibase[nb]), inst_parent(ibase[nb]);
-  std::vector<int32_t> inst_of(F);
+  std::vector<int32_t, UninitAllocator<int32_t>> inst_of(F);   // every position written by its row
   parallel_for(static_cast<int64_t>(nb), [&](int64_t bi) {
     const size_t b = static_cast<size_t>(bi);
     std::vector<int32_t> placed(segs.size(), -1), placed_inst(segs.size(), -1);
