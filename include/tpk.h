@@ -119,6 +119,9 @@ typedef struct {
  *               family (root segment) of each sequence.
  *   opts        see tpk_plan_opts (NULL = capacity 65536, min_shared 64, BFD)
  *   out         receives the new plan; free with tpk_plan_destroy.
+ * The planner uses up to 16 host threads (the environment variable
+ * TPK_PLANNER_THREADS sets another limit, >= 1); its result does not
+ * depend on the number.
  * Errors: TPK_E_ARG (bad offsets / negative token / NULL), TPK_E_SEQ_TOO_LONG,
  *         TPK_E_OVERFLOW (F or R >= 2^31).  Inputs are copied; the caller
  *         keeps ownership of its buffers. */

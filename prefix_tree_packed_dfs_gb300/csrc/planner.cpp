@@ -36,6 +36,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <limits>
 #include <numeric>
@@ -100,12 +101,19 @@ void take(Bin& b, int32_t leaf_id, const Leaf& leaf, const std::vector<Segment>&
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// fn(i) for i in [0, n) on up to 16 host threads; every i writes only its own
-// outputs, so the result does not depend on the schedule
+// Host threads the planner may use: TPK_PLANNER_THREADS if set (>= 1), else
+// the hardware's, at most 16.
+int64_t planner_threads() {
+  const char* env = std::getenv("TPK_PLANNER_THREADS");
+  if (env && std::atoll(env) >= 1) return std::min<int64_t>(std::atoll(env), 16);
+  return std::min<int64_t>(std::max<int64_t>(1, std::thread::hardware_concurrency()), 16);
+}
+
+// fn(i) for i in [0, n) on the planner's host threads; every i writes only
+// its own outputs, so the result does not depend on the schedule
 template <typename Fn>
 void parallel_for(int64_t n, Fn fn) {
-  const int64_t hw = std::max<int64_t>(1, std::thread::hardware_concurrency());
-  const int64_t nt = std::min<int64_t>({hw, 16, n});
+  const int64_t nt = std::min<int64_t>(planner_threads(), n);
   if (nt <= 1) {
     for (int64_t i = 0; i < n; ++i) fn(i);
     return;
@@ -128,8 +136,7 @@ void parallel_for(int64_t n, Fn fn) {
 template <typename Comp>
 void parallel_stable_sort(std::vector<int32_t>& v, Comp comp) {
   const int64_t n = static_cast<int64_t>(v.size());
-  const int64_t hw = std::max<int64_t>(1, std::thread::hardware_concurrency());
-  int64_t chunks = std::min<int64_t>({hw, 16, n / 64});
+  const int64_t chunks = std::min<int64_t>(planner_threads(), n / 64);
   if (chunks <= 1) {
     std::stable_sort(v.begin(), v.end(), comp);
     return;

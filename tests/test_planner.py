@@ -261,3 +261,23 @@ def test_one_row_per_group_rejects_an_oversized_group(lib):
         _cpp_plan(seqs, None, np.zeros(3, np.int32), 4, 100, "groups")
     with pytest.raises(op.PlanError):
         op.plan(seqs, group_ids=np.zeros(3, np.int32), row_capacity=100, min_shared=4, placement="groups")
+
+
+@pytest.mark.parametrize("name", ["curriculum_48", "curriculum_192", "deep_small", "grpo", "agentic"])
+def test_plan_does_not_depend_on_the_thread_count(lib, monkeypatch, name):
+    """The planner's parallel passes (symbols per sequence, sort in chunks,
+    layout / work lists / raw-token lists per row, image in pieces) give the
+    same plan on 1, 3 and 16 host threads."""
+    w = workloads.get(name)
+    outs = []
+    for threads in ("1", "3", "16"):
+        monkeypatch.setenv("TPK_PLANNER_THREADS", threads)
+        p = _cpp_plan(w.sequences, None, w.group_ids, w.min_shared, w.row_capacity)
+        outs.append((p.export(), p.worklists(), p.raw_of_forwarded(), dict(p.info), p.device_bytes()))
+        p.close()
+    e0, w0, r0, i0, d0 = outs[0]
+    for e, wl, r, i, d in outs[1:]:
+        assert all(np.array_equal(e0[k], e[k]) for k in e0)
+        assert all(np.array_equal(w0[k], wl[k]) for k in w0)
+        assert all(np.array_equal(a, b) for a, b in zip(r0, r))
+        assert i == i0 and d == d0
