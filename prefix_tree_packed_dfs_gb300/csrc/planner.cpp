@@ -16,10 +16,11 @@
 //     Shared runs shorter than min_shared are not emitted; their positions
 //     are carried into each child ([ART] "The tree", first refinement);
 //  3. placement of leaves into rows: best-fit decreasing over marginal cost
-//     ([ART] "Bin packing, with a twist") or next-fit ([ART] "One tree, not one
-//     per group"); a row's segment set is closed under ancestors, so a leaf's
-//     marginal cost is the length of its path below the deepest segment the
-//     row already holds;
+//     ([ART] "Bin packing, with a twist"), next-fit ([ART] "One tree, not one
+//     per group") or one row per placement group (no counterpart on the pages:
+//     a data-parallel rank rebuilding the rows it owns); a row's segment set
+//     is closed under ancestors, so a leaf's marginal cost is the length of
+//     its path below the deepest segment the row already holds;
 //  4. depth-first layout of each row (leaves in symbol order, each segment
 //     emitted once, parents first; [DAG] "The walk", [TRL] "How tree packing
 //     works"), depth positions ([DAG] "Positions"), token_index, subtree ends
@@ -32,6 +33,13 @@
 //     CTAs resident at the same time then read the same ancestor K/V blocks
 //     (query tiles) or descendant Q/dO blocks (key tiles) and share them in
 //     L2, while long work still starts before short work.
+// Host threads: symbols per sequence, the symbol-string sort in chunks
+// (merged stably), and layout, subtree ends, work lists and raw-token lists
+// per row -- once rows are placed, each row's forwarded range and instance
+// range are fixed, tiles read only their row and a row holds only its own
+// sequences' raw tokens -- each write only their own outputs, so the plan
+// does not depend on the thread count.  The caller may hand in the storage
+// of an earlier plan (Plan::reset_keep_capacity) to skip fresh allocations.
 #include "planner.h"
 
 #include <algorithm>
