@@ -5,10 +5,15 @@ One step = the whole path over one batch of the deep-tree workload (root of
 4096 tokens, branching factor 1-3 every 256-1024 tokens down to depth 24000,
 128 leaves, rows of 65536 forwarded tokens, 32 query / 8 KV heads, head_dim
 128, bf16):
-    RoPE at depth (Q, K)  ->  tree attention forward (O, LSE)
+    RoPE at depth (Q, K, in place)  ->  tree attention forward (O, LSE)
     ->  scatter to raw-token order (O, LSE)  ->  raw-order dO summed into the
     packed layout (the scatter's transpose)  ->  tree attention backward
-    (prep, dK/dV pass, dQ pass)  ->  inverse RoPE on dQ, dK.
+    (prep, dK/dV pass, dQ pass; the inverse RoPE of dQ, dK inside the
+    passes' epilogues).
+The same step is also timed in the precise mode (P and dS as hi + lo bf16
+pairs, the forward's O residual), and the forward alone on the other
+workloads (tiny, GRPO, agentic, the packing-ratio sweep with its
+sequence-packing twins) under ``configs``.
 The plan (host) is built once for ``value``; the ``e2e`` leg rebuilds it
 every step and moves inputs from pinned host memory and the raw-order LSE
 back, through the same public API, preparing step i+1 (plan build, uploads)
@@ -41,7 +46,7 @@ WORKLOAD = "deep"
 WORKLOAD_DESC = ("deep random tree: root 4096, branching {1,2,3} every 256-1024 tokens to depth 24000, "
                  "128 leaves, rows 65536, Hq 32 / Hkv 8 / d 128, fwd+bwd")
 METRIC = "tree-attn raw tokens/s, useful TFLOP/s and % of GB300 bf16 dense peak"
-LAUNCHES_PER_STEP = 9   # rope, fwd, scatter rows, scatter lse, dO sum, bwd prep, bwd dK/dV, bwd dQ, rope inverse
+LAUNCHES_PER_STEP = 8   # rope, fwd, scatter rows, scatter lse, dO sum, bwd prep, bwd dK/dV, bwd dQ
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # attention kernels on the deep-tree workload, from one ncu capture of
@@ -94,6 +99,8 @@ def _args():
                          "instead of one batch of the same shape per rank")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bound on the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-precise", action="store_true", help="skip the precise-mode step")
+    ap.add_argument("--no-configs", action="store_true", help="skip the forward on the other workloads")
     ap.add_argument("--planner", action="store_true",
                     help="host planner of the library vs the oracle's planner on every workload (no GPU)")
     ap.add_argument("--layout", action="store_true",
@@ -279,6 +286,80 @@ def run_reference(a):
     }), flush=True)
 
 
+def _time_launches(fn, flush, min_s=0.5, min_n=10, warmup=3):
+    """Median CUDA-event time (ms) of fn() on the current stream, L2 flushed
+    (a write larger than L2) before each launch; repeated until ``min_s`` of
+    device time and ``min_n`` launches, so a clock sample spans it."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    times = []
+    while len(times) < min_n or sum(times) < 1e3 * min_s:
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+        if len(times) >= 2000:
+            break
+    return statistics.median(times), len(times)
+
+
+CONFIG_WORKLOADS = (["tiny", "grpo", "agentic"] + ["sweep_%.2f" % r for r in (1.00, 1.45, 2.0, 2.8, 3.56)]
+                    + ["sweep_%.2f_seqpack" % r for r in (1.45, 2.0, 2.8, 3.56)])
+
+
+def run_configs(peaks, local, warmup):
+    """Forward on every other workload: one launch timed at a time (L2
+    flushed before each, median), with its own clock sample."""
+    import torch
+    import workloads
+    from prefix_tree_packed_dfs_gb300 import ops
+    from workloads import rng as wrng
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    out = {}
+    for name in CONFIG_WORKLOADS:
+        w = workloads.get(name)
+        plan = ops.Plan.from_sequences(w.sequences, group_ids=w.group_ids, row_capacity=w.row_capacity,
+                                       min_shared=w.min_shared)
+        dp = plan.to_device()
+        info = plan.info
+        F, Hq, Hkv, d = info["n_fwd"], w.n_heads_q, w.n_heads_kv, w.head_dim
+        q = wrng.normal_bf16(w.seeds["q"], (F, Hq, d), "cuda")
+        k = wrng.normal_bf16(w.seeds["k"], (F, Hkv, d), "cuda")
+        v = wrng.normal_bf16(w.seeds["v"], (F, Hkv, d), "cuda")
+        ops.rope_by_depth(q, k, dp.depth, w.rope_base)
+        o = torch.empty_like(q)
+        lse = torch.empty((Hq, F), dtype=torch.float32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        clocks = Clocks(local)
+        torch.cuda.synchronize()
+        clocks.start()
+        ms, n = _time_launches(lambda: ops.tree_attn_fwd(dp, q, k, v, out=o, lse=lse, dev_err=err), flush,
+                               warmup=max(3, warmup))
+        clk = clocks.stop()
+        if int(err.item()) != 0:
+            raise SystemExit("device wait timed out (TPK_E_TIMEOUT) on %s" % name)
+        flops = 4.0 * d * Hq * info["useful_pairs"]
+        tfl = flops / ms / 1e9
+        out[name] = {"raw_tokens": info["n_raw"], "forwarded_tokens": F, "rows": info["n_rows"],
+                     "packing_ratio": info["packing_ratio"], "useful_pairs": info["useful_pairs"],
+                     "Hq": Hq, "Hkv": Hkv, "head_dim": d, "ms": ms, "launches_timed": n,
+                     "raw_tokens_per_s": info["n_raw"] / ms * 1e3, "forwarded_tokens_per_s": F / ms * 1e3,
+                     "useful_tflops": tfl, "frac_of_burst_peak": tfl / peaks["bf16_tflops"], "clocks": clk}
+        del q, k, v, o, lse, dp, plan
+        torch.cuda.empty_cache()
+    for rho in (1.45, 2.0, 2.8, 3.56):
+        tree, seq = out["sweep_%.2f" % rho], out["sweep_%.2f_seqpack" % rho]
+        tree["speedup_vs_sequence_packing"] = seq["ms"] / tree["ms"]
+    return {"what": "forward only, one launch timed at a time: L2 flushed (256 MiB write) before each, median "
+                    "of >= 10 launches and >= 0.5 s; frac against the burst bf16 peak (%s); "
+                    "sweep_<rho>_seqpack = the same raw tokens without sharing" % peaks["source"],
+            "peak_tflops": peaks["bf16_tflops"], "workloads": out}
+
+
 def run_ours(a):
     import torch
     import workloads
@@ -325,7 +406,6 @@ def run_ours(a):
     # summed into the packed layout inside the step (transpose of the scatter)
     dO_raw = wrng.normal_bf16(s["do"], (R, Hq, d), dev)
     dO = torch.empty((F, Hq, d), dtype=torch.bfloat16, device=dev)
-    qr, kr = torch.empty_like(Q), torch.empty_like(K)
     O = torch.empty_like(Q)
     LSE = torch.empty((Hq, F), dtype=torch.float32, device=dev)
     O_raw = torch.empty((R, Hq, d), dtype=torch.bfloat16, device=dev)
@@ -333,28 +413,29 @@ def run_ours(a):
     dq, dk, dv = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     ws = torch.empty(max(ops.attn_workspace_bytes(dp, Hq, Hkv, d, True), 256), dtype=torch.uint8, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    names = ["rope", "fwd", "scatter", "dO_sum", "bwd_prep", "bwd_dkdv", "bwd_dq", "rope_inv"]
+    names = ["rope", "fwd", "scatter", "dO_sum", "bwd_prep", "bwd_dkdv", "bwd_dq"]
 
-    def step(dplan, ev=None, ready=None, sig=None, v=None):
-        """One pass of the path.  End to end only: ``ready`` holds events of
-        the input uploads, each waited for right before the first kernel that
-        reads that input ("qk", "v", "do"), and "lse_free" (the previous
-        step's raw-order LSE has been read back) before the scatter; ``sig``
-        receives events recorded once RoPE has read Q/K ("rope"), the
-        raw-order outputs are final ("out"), the raw dO has been summed
-        ("dosum") and the step is complete ("done"); ``v`` replaces V."""
-        Vt = V if v is None else v
+    def step(dplan, ev=None, ready=None, sig=None, qkv=None, precise=False, o_lo=None):
+        """One pass of the path.  Q and K are rotated in place; the backward
+        returns dQ, dK w.r.t. the un-rotated inputs (inverse RoPE in its
+        epilogues).  End to end only: ``qkv`` replaces (Q, K, V) (double-
+        buffered inputs); ``ready`` holds events of the input uploads, each
+        waited for right before the first kernel that reads that input ("qk",
+        "v", "do"), and "lse_free" (the previous step's raw-order LSE has been
+        read back) before the scatter; ``sig`` receives events recorded once
+        the raw-order outputs are final ("out"), the raw dO has been summed
+        ("dosum") and the step is complete ("done")."""
+        Qt, Kt, Vt = (Q, K, V) if qkv is None else qkv
         mark = (lambda i: ev[i].record()) if ev is not None else (lambda i: None)
         wait = ((lambda k: torch.cuda.current_stream().wait_event(ready[k]) if k in ready else None)
                 if ready else (lambda k: None))
         note = (lambda k: sig[k].record()) if sig is not None else (lambda k: None)
         mark(0)
         wait("qk")
-        ops.rope_by_depth(Q, K, dplan.depth, w.rope_base, q_out=qr, k_out=kr)
-        note("rope")
+        ops.rope_by_depth(Qt, Kt, dplan.depth, w.rope_base)
         mark(1)
         wait("v")
-        ops.tree_attn_fwd(dplan, qr, kr, Vt, out=O, lse=LSE, dev_err=err)
+        ops.tree_attn_fwd(dplan, Qt, Kt, Vt, out=O, lse=LSE, dev_err=err, precise=precise, o_lo=o_lo)
         mark(2)
         wait("lse_free")
         ops.scatter_token_index(dplan.token_index, O, LSE, dst=O_raw, lse_dst=LSE_raw)
@@ -364,47 +445,66 @@ def run_ours(a):
         ops.sum_to_forwarded(dplan, dO_raw, dst=dO)
         note("dosum")
         mark(4)
-        ops.tree_attn_bwd(dplan, qr, kr, Vt, O, LSE, dO, dq=dq, dk=dk, dv=dv, workspace=ws, dev_err=err,
-                          phases=(0,))
-        mark(5)
-        ops.tree_attn_bwd(dplan, qr, kr, Vt, O, LSE, dO, dq=dq, dk=dk, dv=dv, workspace=ws, dev_err=err,
-                          phases=(1,))
-        mark(6)
-        ops.tree_attn_bwd(dplan, qr, kr, Vt, O, LSE, dO, dq=dq, dk=dk, dv=dv, workspace=ws, dev_err=err,
-                          phases=(2,))
-        mark(7)
-        ops.rope_by_depth(dq, dk, dplan.depth, w.rope_base, inverse=True)
+        for ph in (0, 1, 2):
+            ops.tree_attn_bwd(dplan, Qt, Kt, Vt, O, LSE, dO, dq=dq, dk=dk, dv=dv, workspace=ws, dev_err=err,
+                              phases=(ph,), precise=precise, o_lo=o_lo, rope_base=w.rope_base)
+            mark(5 + ph)
         note("done")
-        mark(8)
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
+
+    def timed(n_steps, **kw):
+        """n_steps steps between a barrier + synchronize on both sides, with
+        a clock sample; returns (ms per step, per-kernel mean ms, clocks)."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(n_steps)]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clocks = Clocks(local)
+        barrier()
+        torch.cuda.synchronize()
+        clocks.start()
+        start.record()
+        for i in range(n_steps):
+            step(dp, evs[i], **kw)
+        stop.record()
+        torch.cuda.synchronize()
+        barrier()
+        clk = clocks.stop()
+        per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n_steps))
+               for j, n in enumerate(names)}
+        if int(err.item()) != 0:
+            raise SystemExit("device wait timed out (TPK_E_TIMEOUT)")
+        return start.elapsed_time(stop) / n_steps, per, clk
 
     for _ in range(a.warmup):
         step(dp)
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise SystemExit("device wait timed out (TPK_E_TIMEOUT)")
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(a.steps)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = Clocks(local)
-    barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    start.record()
-    for i in range(a.steps):
-        step(dp, evs[i])
-    stop.record()
-    torch.cuda.synchronize()
-    barrier()
-    clk = clocks.stop()
-    ms = start.elapsed_time(stop) / a.steps
-    per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(a.steps))
-           for j, n in enumerate(names)}
+    ms, per, clk = timed(a.steps)
     ms = max_over_ranks(ms, dev, world)
-    if int(err.item()) != 0:
-        raise SystemExit("device wait timed out (TPK_E_TIMEOUT)")
+
+    # ---- the same step in the precise mode ---------------------------------
+    fwd_flop = 4.0 * d * Hq * pairs
+    bwd_flop = 10.0 * d * Hq * pairs
+    precise = None
+    if not a.no_precise:
+        O_lo = torch.empty_like(Q)
+        n_p = max(2, min(a.steps, 3))
+        for _ in range(max(1, min(a.warmup, 2))):
+            step(dp, precise=True, o_lo=O_lo)
+        ms_p, per_p, clk_p = timed(n_p, precise=True, o_lo=O_lo)
+        ms_p = max_over_ranks(ms_p, dev, world)
+        del O_lo
+        torch.cuda.empty_cache()
+        t_bwd = (per_p["bwd_prep"] + per_p["bwd_dkdv"] + per_p["bwd_dq"]) / 1e3
+        precise = {"what": "same step with P and dS as hi + lo bf16 pairs (one more product each for PV, dV, dK, "
+                           "dQ) and D from O before its rounding; gradients within the stated max-abs 1e-2",
+                   "value": job_rate(R, full.info["n_raw"], ms_p / 1e3), "unit": "raw tokens/s",
+                   "ms_per_step": ms_p, "steps": n_p, "useful_tflops": (fwd_flop + bwd_flop) / (ms_p / 1e3) / 1e12,
+                   "fwd_tflops": fwd_flop / (per_p["fwd"] / 1e3) / 1e12, "bwd_tflops": bwd_flop / t_bwd / 1e12,
+                   "kernels_ms": per_p, "clocks": clk_p, "slowdown_vs_fast": ms_p / ms}
 
     # ---- end to end through the public API, host buffers -----------------
     e2e = None
@@ -419,10 +519,10 @@ def run_ours(a):
         h2d = sum(x.numel() * x.element_size() for x in (hQ, hK, hV, hdO)) + plan.device_bytes()
         d2h = hLSE.numel() * hLSE.element_size()
 
-        # V is read until the end of the backward, so the next step's V goes
-        # to a second buffer; Q, K and the raw dO are free again once RoPE and
-        # the dO sum have read them
-        Vs = (V, torch.empty_like(V))
+        # Q, K (rotated in place) and V are read until the end of the
+        # backward, so step i+1's inputs go to a second set of buffers, as a
+        # prefetching data loader fills them; the raw dO is free once summed
+        sets = ((Q, K, V), (torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)))
         copy_stream = torch.cuda.Stream(dev)
 
         def build_plan():
@@ -433,18 +533,20 @@ def run_ours(a):
             return {k: torch.cuda.Event(enable_timing=timing) for k in keys}
 
         def upload(j, make_plan, prev, prev2):
-            """Step j's inputs on the copy stream, each behind the kernel of
-            step j-1 (``prev``) that last reads its buffer, in the order the
-            GPU reaches them; step j-1's raw-order LSE is read back in
-            between.  The host builds step j's plan (``make_plan``) while Q
-            and K go up.  Returns (device plan, events step j waits for)."""
+            """Step j's inputs on the copy stream into buffer set j % 2, behind
+            the kernel of step j-2 (``prev2``) that last read that set and,
+            for the raw dO and the LSE read-back, behind step j-1 (``prev``),
+            in the order the GPU reaches them.  The host builds step j's plan
+            (``make_plan``) while Q and K go up.  Returns (device plan, events
+            step j waits for)."""
             ready = events("q", "k", "qk", "v", "do", "lse_free", timing=True)
+            qj, kj, vj = sets[j % 2]
             with torch.cuda.stream(copy_stream):
-                if prev:
-                    copy_stream.wait_event(prev["rope"])
-                Q.copy_(hQ, non_blocking=True)
+                if prev2:
+                    copy_stream.wait_event(prev2["done"])   # step j-2 read this set
+                qj.copy_(hQ, non_blocking=True)
                 ready["q"].record()
-                K.copy_(hK, non_blocking=True)
+                kj.copy_(hK, non_blocking=True)
                 ready["k"].record()
                 t_host = [time.perf_counter()]
                 p2 = make_plan()
@@ -453,9 +555,7 @@ def run_ours(a):
                 t_host.append(time.perf_counter())
                 ready["qk"].record()
                 ready["host_s"] = t_host
-                if prev2:
-                    copy_stream.wait_event(prev2["done"])   # step j-2 read this V buffer
-                Vs[j % 2].copy_(hV, non_blocking=True)
+                vj.copy_(hV, non_blocking=True)
                 ready["v"].record()
                 if prev:
                     copy_stream.wait_event(prev["out"])
@@ -485,8 +585,8 @@ def run_ours(a):
             live = [None, d_cur]          # device plans of steps i-1, i
             sigs = []
             for i in range(n):
-                sig = events("rope", "out", "dosum", "done", timing=True)
-                step(live[-1], ready=ready, sig=sig, v=Vs[i % 2])
+                sig = events("out", "dosum", "done", timing=True)
+                step(live[-1], ready=ready, sig=sig, qkv=sets[i % 2])
                 sigs.append(sig)
                 if i + 1 < n:
                     d_nxt, ready = upload(i + 1, build_plan, sig, sigs[-2] if i > 0 else None)
@@ -505,7 +605,7 @@ def run_ours(a):
             first = {k: round(origin.elapsed_time(e), 1) for k, e in
                      (("q_ready", ready0["q"]), ("k_ready", ready0["k"]), ("qk_plan_ready", ready0["qk"]),
                       ("v_ready", ready0["v"]), ("do_ready", ready0["do"]),
-                      ("rope_done", sigs[0]["rope"]), ("step_done", sigs[0]["done"]))}
+                      ("step_out", sigs[0]["out"]), ("step_done", sigs[0]["done"]))}
             hs = ready0["host_s"]
             first["host_plan_build"] = round(1e3 * (hs[1] - hs[0]), 1)
             first["host_plan_upload_call"] = round(1e3 * (hs[2] - hs[1]), 1)
@@ -521,9 +621,9 @@ def run_ours(a):
                "statistic": "wall time of all steps / steps",
                "includes": "one plan build on the host per step, plan image + Q/K/V + raw-order dO "
                            "host->device and the raw-order LSE device->host every step; step i+1's "
-                           "plan is built and its inputs uploaded while the GPU runs step i (V double-"
-                           "buffered); the first step's uploads are not overlapped"}
-        del hQ, hK, hV, hdO
+                           "plan is built and its inputs uploaded while the GPU runs step i (Q, K, V "
+                           "double-buffered); the first step's uploads are not overlapped"}
+        del hQ, hK, hV, hdO, sets
 
     # ---- CPU baseline (oracle), rank 0 only ----------------------------------
     cpu = None
@@ -536,14 +636,11 @@ def run_ours(a):
                          "24000-token sequences (%.1f s); dK/dV rows not included" % (n, dt)}
 
     # ---- roofline of the dominant kernel ------------------------------------
-    fwd_flop = 4.0 * d * Hq * pairs
-    bwd_flop = 10.0 * d * Hq * pairs
     algo = {   # algorithmic FLOPs (tensor kernels) or bytes (HBM kernels) per launch
         "fwd": ("tensor", fwd_flop),
         "bwd_dkdv": ("tensor", 8.0 * d * Hq * pairs),     # S^T, dP^T, dV, dK products
         "bwd_dq": ("tensor", 2.0 * d * Hq * pairs),       # dQ product (S, dP recomputed on top)
         "rope": ("hbm", F * (Hq + Hkv) * d * 2 * 2 + 4 * F),
-        "rope_inv": ("hbm", F * (Hq + Hkv) * d * 2 * 2 + 4 * F),
         "scatter": ("hbm", R * Hq * (2 * d + 4) * 2 + 4 * R),
         "dO_sum": ("hbm", (R + F) * Hq * d * 2 + 4 * (F + 1) + 4 * R),
         "bwd_prep": ("hbm", F * Hq * d * 2 * 2 + 4 * F * Hq),
@@ -555,7 +652,8 @@ def run_ours(a):
         peak = peaks["bf16_tflops_sustained"]
         roof = {"kernel": dom, "bound": "tensor", "achieved": amount / secs / 1e12, "peak": peak,
                 "unit": "TFLOP/s", "frac": amount / secs / 1e12 / peak, "traffic": recorded_traffic(dom, a.workload),
-                "peak_kind": "sustained bf16 (%s)" % peaks["source"]}
+                "peak_kind": "sustained bf16 (%s)" % peaks["source"],
+                "frac_of_burst": amount / secs / 1e12 / peaks["bf16_tflops"]}
     else:
         peak = peaks["hbm_gbs"]
         roof = {"kernel": dom, "bound": "hbm", "achieved": amount / secs / 1e9, "peak": peak, "unit": "GB/s",
@@ -567,6 +665,13 @@ def run_ours(a):
         kernels[n] = {"ms": per[n], ("tflops" if b == "tensor" else "gbs"):
                       amt / t_s / (1e12 if b == "tensor" else 1e9)}
 
+    # ---- forward on the other workloads (after the deep tree's buffers go) --
+    configs = None
+    if not a.no_configs and rank == 0:
+        del Q, K, V, dO_raw, dO, O, LSE, O_raw, LSE_raw, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+        configs = run_configs(peaks, local, a.warmup)
+
     useful_tflops = (fwd_flop + bwd_flop) / (ms / 1e3) / 1e12
     out = {
         "metric": METRIC, "value": job_rate(R, full.info["n_raw"], ms / 1e3), "unit": "raw tokens/s", "n_gpus": world,
@@ -575,7 +680,8 @@ def run_ours(a):
         "config": {"workload": WORKLOAD_DESC, "raw_tokens": R, "forwarded_tokens": F, "rows": info["n_rows"],
                    "packing_ratio": info["packing_ratio"], "useful_pairs": pairs,
                    "visited_pairs_fwd": info["visited_pairs"], "Hq": Hq, "Hkv": Hkv, "head_dim": d,
-                   "row_capacity": w.row_capacity, "l2": "inputs larger than L2 (Q alone %.1f GB)" % (F * Hq * d * 2 / 1e9),
+                   "row_capacity": w.row_capacity, "precision": "fast (bf16 P and dS operands)",
+                   "l2": "inputs larger than L2 (Q alone %.1f GB)" % (F * Hq * d * 2 / 1e9),
                    "parallelism": ("one batch, whole rows per rank (longest first), no collective" if sharded
                                    else "one batch per rank, no collective" if world > 1 else "single GPU")},
         "useful_tflops": useful_tflops,
@@ -589,6 +695,8 @@ def run_ours(a):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "precise": precise,
+        "configs": configs,
         "gpu_launches": LAUNCHES_PER_STEP * a.steps,
         "clocks": clk,
     }
@@ -603,7 +711,8 @@ def run_sweep(a):
     1.00 .. 3.56, and over the same raw tokens laid out without sharing
     (sequence packing: min shared length above every run).  L2 is flushed
     (a 256 MiB write) before every timed launch; CUDA events bracket the
-    attention kernel alone on the current stream."""
+    attention kernel alone on the current stream; each point carries its own
+    nvidia-smi clock sample."""
     import torch
     import workloads
     from prefix_tree_packed_dfs_gb300 import ops
@@ -625,25 +734,19 @@ def run_sweep(a):
         o = torch.empty_like(q)
         lse = torch.empty((Hq, F), dtype=torch.float32, device="cuda")
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        for _ in range(a.warmup):
-            ops.tree_attn_fwd(dp, q, k, v, out=o, lse=lse, dev_err=err)
-        times = []
-        for _ in range(max(a.steps, 3)):
-            flush.fill_(1)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            ops.tree_attn_fwd(dp, q, k, v, out=o, lse=lse, dev_err=err)
-            e1.record()
-            torch.cuda.synchronize()
-            times.append(e0.elapsed_time(e1))
+        clocks = Clocks(0)
+        torch.cuda.synchronize()
+        clocks.start()
+        ms, n = _time_launches(lambda: ops.tree_attn_fwd(dp, q, k, v, out=o, lse=lse, dev_err=err), flush,
+                               min_n=max(a.steps, 10), warmup=max(a.warmup, 3))
+        clk = clocks.stop()
         if int(err.item()) != 0:
             raise SystemExit("device wait timed out (TPK_E_TIMEOUT)")
-        ms = statistics.median(times)
         flops = 4.0 * d * Hq * info["useful_pairs"]
         return {"raw_tokens": info["n_raw"], "forwarded_tokens": F, "rows": info["n_rows"],
                 "useful_pairs": info["useful_pairs"], "visited_pairs": info["visited_pairs"], "ms": ms,
-                "useful_tflops": flops / ms / 1e9, "raw_tokens_per_s": info["n_raw"] / ms * 1e3,
-                "forwarded_tokens_per_s": F / ms * 1e3}
+                "launches_timed": n, "useful_tflops": flops / ms / 1e9, "raw_tokens_per_s": info["n_raw"] / ms * 1e3,
+                "forwarded_tokens_per_s": F / ms * 1e3, "clocks": clk}
 
     for rho in workloads.SWEEP_RHOS:
         tree = time_fwd("sweep_%.2f" % rho)

@@ -60,6 +60,8 @@ extern "C" {
 #define TPK_E_TIMEOUT       -6  /* a device wait gave up (read from dev_err) */
 #define TPK_E_WORKSPACE     -7  /* workspace missing or smaller than required */
 #define TPK_E_SCRATCH_LIMIT -8  /* problem too large for tpk_tree_attn_bwd_noalloc's static scratch */
+#define TPK_E_HOST          -9  /* host-side failure in the planner: out of host memory or
+                                   another C++ exception, caught before it reaches the caller */
 
 /* ---- placement rules ---------------------------------------------------- */
 #define TPK_PLACE_BFD       0   /* [ART] "Bin packing, with a twist": best-fit decreasing
@@ -123,7 +125,10 @@ typedef struct {
  * TPK_PLANNER_THREADS sets another limit, >= 1); its result does not
  * depend on the number.
  * Errors: TPK_E_ARG (bad offsets / negative token / NULL), TPK_E_SEQ_TOO_LONG,
- *         TPK_E_OVERFLOW (F or R >= 2^31).  Inputs are copied; the caller
+ *         TPK_E_OVERFLOW (F or R >= 2^31), TPK_E_HOST (host memory exhausted or
+ *         another exception inside the planner; no exception crosses the ABI).
+ *         If fewer worker threads can be created than asked for, the planner
+ *         runs on the ones it has (same result).  Inputs are copied; the caller
  *         keeps ownership of its buffers. */
 int tpk_plan_build(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs,
                    const uint8_t* trained, const int32_t* group_ids,
@@ -238,6 +243,44 @@ int tpk_rope_by_depth(const void* q_in, const void* k_in, void* q_out, void* k_o
                       const int32_t* depth, int64_t F, int32_t Hq, int32_t Hkv, int32_t d,
                       double base, int32_t inverse, void* stream);
 
+/* Options of the attention calls (tpk_tree_attn_fwd_ex, tpk_tree_attn_bwd_ex).
+ * No counterpart on the pages: they choose the arithmetic, not the result.
+ *   precision  TPK_PREC_FAST: the probabilities P (forward and backward) and
+ *              the score gradients dS (backward) enter their tensor-core
+ *              products as bf16, as in any bf16 flash-attention kernel.  The
+ *              backward's error is then about 1.3% of max(1, |gradient|) at
+ *              worst on unit-variance inputs, against 0.4% for the bf16
+ *              rounding of the gradient itself.
+ *              TPK_PREC_PRECISE: each of P and dS is split into a bf16 high
+ *              part and the bf16 rounding of the remainder, and both parts
+ *              are multiplied (two products where the fast mode has one), so
+ *              they carry about 16 significant bits.  The forward also returns
+ *              O's rounding residual (o_lo), and the backward's row terms
+ *              D = dO . O use it, so D is taken from O before its bf16 rounding.
+ *              dQ, dK and dV then differ from the exact gradients by about the
+ *              bf16 rounding of the outputs alone.  Costs one more product for
+ *              each of PV, dV, dK and dQ.
+ *   rope_base  backward only: > 1 returns dq and dk with respect to the
+ *              un-rotated q and k -- the inverse of tpk_rope_by_depth at depth
+ *              ("DAG packing", section "Positions") is applied to the fp32
+ *              gradients in the kernels' epilogues, before their one bf16
+ *              rounding -- so no inverse RoPE pass is needed; the plan's depths
+ *              must be below 2^24 (TPK_E_UNSUPPORTED otherwise).  0 = with
+ *              respect to the rotated inputs (no rotation).
+ *   o_lo       [F, Hq, d] bf16, 16-byte aligned.  Forward, precise: output,
+ *              bf16(O - bf16(O)) of the fp32 output (NULL: not written).
+ *              Backward, precise: input, D = dO . (o + o_lo) (NULL: D = dO . o).
+ *              Ignored in the fast mode.
+ * A NULL options pointer means fast, no rotation, no o_lo. */
+#define TPK_PREC_FAST     0
+#define TPK_PREC_PRECISE  1
+typedef struct {
+    int32_t precision;   /* TPK_PREC_FAST or TPK_PREC_PRECISE */
+    int32_t reserved;    /* 0 */
+    double rope_base;    /* backward: 0, or > 1 for gradients w.r.t. the un-rotated q, k */
+    void* o_lo;          /* see above */
+} tpk_attn_opts;
+
 /* Workspace bytes for the attention calls (0 for the forward). */
 size_t tpk_attn_workspace_bytes(const tpk_plan* plan, int32_t Hq, int32_t Hkv,
                                 int32_t d, int32_t backward);
@@ -259,6 +302,15 @@ int tpk_tree_attn_fwd(const tpk_plan* plan, const void* dev_image,
                       void* o, float* lse, int32_t Hq, int32_t Hkv, int32_t d,
                       float scale, void* workspace, size_t ws_bytes,
                       int32_t* dev_err, void* stream);
+
+/* tpk_tree_attn_fwd with options (precision, O's rounding residual; see
+ * tpk_attn_opts).  rope_base must be 0 (the forward takes rotated q, k).
+ * Same arguments and errors as tpk_tree_attn_fwd otherwise. */
+int tpk_tree_attn_fwd_ex(const tpk_plan* plan, const void* dev_image,
+                         const void* q, const void* k, const void* v,
+                         void* o, float* lse, int32_t Hq, int32_t Hkv, int32_t d,
+                         float scale, const tpk_attn_opts* opts,
+                         int32_t* dev_err, void* stream);
 
 /* Tree attention backward: gradients of sum_{f,h} <dout[f,h], O[f,h]> w.r.t.
  * the rotated q and k and w.r.t. v (apply tpk_rope_by_depth(inverse=1) to dq
@@ -283,6 +335,7 @@ int tpk_tree_attn_bwd(const tpk_plan* plan, const void* dev_image,
  *   TPK_BWD_DKDV  key-major pass: dk, dv
  *   TPK_BWD_DQ    query-major pass: dq
  * Arguments a phase does not read may be NULL. */
+#define TPK_BWD_ALL  -1   /* tpk_tree_attn_bwd_ex only: phases 0, 1, 2 in order */
 #define TPK_BWD_PREP 0
 #define TPK_BWD_DKDV 1
 #define TPK_BWD_DQ   2
@@ -292,6 +345,20 @@ int tpk_tree_attn_bwd_phase(int32_t phase, const tpk_plan* plan, const void* dev
                             void* dq, void* dk, void* dv, int32_t Hq, int32_t Hkv,
                             int32_t d, float scale, void* workspace, size_t ws_bytes,
                             int32_t* dev_err, void* stream);
+
+/* tpk_tree_attn_bwd / tpk_tree_attn_bwd_phase with options (see
+ * tpk_attn_opts): precision, the forward's rounding residual of O, and the
+ * inverse RoPE fused into the epilogues.  phase = TPK_BWD_ALL runs the three
+ * phases in order; one phase runs that phase alone (same rules as
+ * tpk_tree_attn_bwd_phase).  Deterministic in both precisions.  Errors as
+ * tpk_tree_attn_bwd; TPK_E_ARG also for an unknown precision or a rope_base
+ * that is neither 0 nor > 1. */
+int tpk_tree_attn_bwd_ex(int32_t phase, const tpk_plan* plan, const void* dev_image,
+                         const void* q, const void* k, const void* v,
+                         const void* o, const float* lse, const void* dout,
+                         void* dq, void* dk, void* dv, int32_t Hq, int32_t Hkv,
+                         int32_t d, float scale, const tpk_attn_opts* opts,
+                         void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream);
 
 /* Backward for callers that cannot allocate device memory at call time.
  * The pages have no counterpart: this is a deployment variant of
@@ -303,8 +370,11 @@ int tpk_tree_attn_bwd_phase(int32_t phase, const tpk_plan* plan, const void* dev
  * 32 MiB array inside the library, which every GPU that loads the library
  * keeps until the process exits.  Problems with Hq * F > 8,388,608 return
  * TPK_E_SCRATCH_LIMIT (use tpk_tree_attn_bwd with a workspace instead).
- * The first call on each device looks up the array's device address with
- * that device current; make that first call before any stream capture.
+ * The first call in each CUDA context -- per device, for the runtime's
+ * primary contexts -- looks up the array's device address in that context;
+ * make that first call before any stream capture.  The address is cached by
+ * the context's unique id, so a context created after cudaDeviceReset, or
+ * another context the caller makes current, gets its own lookup.
  * Every call on a device shares the one array, so calls that overlap on the
  * GPU (different streams without ordering) race; calls on one stream are
  * ordered and safe.  Nothing needs clearing: each call overwrites the part it

@@ -290,3 +290,62 @@ def backward_rows_kv(plan, Q_rows, K_rows, V_rows, dO_rows, fwd, base, scale=Non
         dks.append(rope(dk_acc[None], [pj], base, inverse=True)[0])
         dvs.append(dv_acc)
     return np.stack(dks), np.stack(dvs)
+
+
+def backward_keys(plan, Q_rows, K_rows, V_rows, dO_rows, fwd, base, scale=None, chunk=256):
+    """dK (w.r.t. un-rotated K) and dV at forwarded key positions ``fwd``, the
+    same quantities as ``backward_rows_kv`` for keys with long subtrees.
+
+    The queries that see key j are the positions of its subtree [j,
+    subtree_end[j]); each is taken through the sequence that owns it, with its
+    full softmax row over that sequence's prefix.  The queries one sequence
+    owns inside the subtree are positions of that sequence, so they are taken
+    together: the sequence's prefix is rotated once and each head's scores of
+    those queries are one matrix product (``chunk`` query rows at a time,
+    keys after a query's own position masked).  Returns ([n, Hkv, d],
+    [n, Hkv, d])."""
+    off = plan["seq_offsets"]
+    ti = plan["token_index"]
+    src = plan["fwd_src"]
+    se = plan["subtree_end"]
+    depth = plan["depth"]
+    dks, dvs = [], []
+    for j in fwd:
+        j = int(j)
+        pj = int(depth[j])
+        qs = np.arange(j, int(se[j]))
+        seq_of = np.searchsorted(off, src[qs], side="right") - 1
+        dk_acc = dv_acc = None
+        for s in np.unique(seq_of):
+            mine = qs[seq_of == s]
+            pos = depth[mine].astype(np.int64)        # positions of those queries in sequence s
+            path = ti[off[s]:off[s] + int(pos.max()) + 1]
+            if path[pj] != j:
+                continue
+            q = round_to_bf16(rope(Q_rows(path[pos]), pos, base))
+            k = round_to_bf16(rope(K_rows(path), np.arange(len(path)), base))
+            v = np.asarray(V_rows(path), dtype=np.float64)
+            do = np.asarray(dO_rows(path[pos]), dtype=np.float64)
+            hq, d = q.shape[1], q.shape[2]
+            hkv = k.shape[1]
+            sc = 1.0 / np.sqrt(d) if scale is None else scale
+            if dk_acc is None:
+                dk_acc = np.zeros((hkv, d))
+                dv_acc = np.zeros((hkv, d))
+            for lo in range(0, len(pos), chunk):
+                hi = min(len(pos), lo + chunk)
+                masked = np.arange(len(path))[None, :] > pos[lo:hi, None]
+                for h in range(hq):
+                    g = _kv_head(h, hq, hkv)
+                    sv = (q[lo:hi, h, :] @ k[:, g, :].T) * sc
+                    sv[masked] = -np.inf
+                    w = np.exp(sv - sv.max(axis=1, keepdims=True))
+                    pr = w / w.sum(axis=1, keepdims=True)
+                    o = pr @ v[:, g, :]
+                    dp_j = do[lo:hi, h, :] @ v[pj, g, :]
+                    ds_j = pr[:, pj] * (dp_j - np.sum(do[lo:hi, h, :] * o, axis=1))
+                    dv_acc[g] += pr[:, pj] @ do[lo:hi, h, :]
+                    dk_acc[g] += sc * (ds_j @ q[lo:hi, h, :])
+        dks.append(rope(dk_acc[None], [pj], base, inverse=True)[0])
+        dvs.append(dv_acc)
+    return np.stack(dks), np.stack(dvs)

@@ -13,9 +13,10 @@ TPK_OK = 0
 STATUS = {
     0: "TPK_OK", -1: "TPK_E_ARG", -2: "TPK_E_SEQ_TOO_LONG", -3: "TPK_E_OVERFLOW",
     -4: "TPK_E_UNSUPPORTED", -5: "TPK_E_CUDA", -6: "TPK_E_TIMEOUT", -7: "TPK_E_WORKSPACE",
-    -8: "TPK_E_SCRATCH_LIMIT",
+    -8: "TPK_E_SCRATCH_LIMIT", -9: "TPK_E_HOST",
 }
-BWD_PREP, BWD_DKDV, BWD_DQ = 0, 1, 2
+BWD_ALL, BWD_PREP, BWD_DKDV, BWD_DQ = -1, 0, 1, 2
+PREC_FAST, PREC_PRECISE = 0, 1
 PLACE_BFD = 0
 PLACE_NEXT_FIT = 1
 PLACE_GROUPS = 2
@@ -27,8 +28,8 @@ EXPORTS = [
     "tpk_plan_build", "tpk_plan_info_get", "tpk_plan_export", "tpk_plan_worklists", "tpk_plan_raw_of_forwarded",
     "tpk_plan_shard_rows",
     "tpk_plan_device_bytes", "tpk_plan_field_offset", "tpk_plan_upload", "tpk_plan_destroy",
-    "tpk_rope_by_depth", "tpk_attn_workspace_bytes", "tpk_tree_attn_fwd", "tpk_tree_attn_bwd",
-    "tpk_tree_attn_bwd_phase", "tpk_tree_attn_bwd_noalloc", "tpk_selftest_wait_timeout",
+    "tpk_rope_by_depth", "tpk_attn_workspace_bytes", "tpk_tree_attn_fwd", "tpk_tree_attn_fwd_ex",
+    "tpk_tree_attn_bwd", "tpk_tree_attn_bwd_ex", "tpk_tree_attn_bwd_phase", "tpk_tree_attn_bwd_noalloc", "tpk_selftest_wait_timeout",
     "tpk_scatter_token_index", "tpk_gather_to_forwarded", "tpk_sum_to_forwarded", "tpk_status_string",
     "tpk_version",
 ]
@@ -42,6 +43,12 @@ class TpkError(RuntimeError):
 
 class PlanOpts(ctypes.Structure):
     _fields_ = [("row_capacity", ctypes.c_int64), ("min_shared", ctypes.c_int32), ("placement", ctypes.c_int32)]
+
+
+class AttnOpts(ctypes.Structure):
+    """tpk_attn_opts: precision, inverse RoPE base (backward), O's rounding residual."""
+    _fields_ = [("precision", ctypes.c_int32), ("reserved", ctypes.c_int32), ("rope_base", ctypes.c_double),
+                ("o_lo", ctypes.c_void_p)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -80,6 +87,10 @@ def _sig(lib):
     lib.tpk_tree_attn_fwd.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, ctypes.c_float, P, SZ, P, P]
     lib.tpk_tree_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, ctypes.c_float, P, SZ, P, P]
     lib.tpk_tree_attn_bwd_phase.argtypes = [I32] + lib.tpk_tree_attn_bwd.argtypes
+    lib.tpk_tree_attn_fwd_ex.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, ctypes.c_float,
+                                         ctypes.POINTER(AttnOpts), P, P]
+    lib.tpk_tree_attn_bwd_ex.argtypes = [I32, P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, ctypes.c_float,
+                                         ctypes.POINTER(AttnOpts), P, SZ, P, P]
     lib.tpk_tree_attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I32, I32, I32, ctypes.c_float, P, P]
     lib.tpk_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P, P]
     lib.tpk_scatter_token_index.argtypes = [P, I64, I64, P, P, P, P, I32, I32, P]

@@ -99,10 +99,14 @@ int tpk_plan_build(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_
   if (!h) return TPK_E_ARG;
   take_plan_storage(&h->p);
   int st;
+  // nothing thrown inside the planner (out of host memory, a worker thread
+  // that could not be created, ...) may cross the C ABI
   try {
     st = tpk::build_plan(tokens, seq_offsets, n_seqs, trained, group_ids, o, &h->p);
   } catch (const std::bad_alloc&) {
-    st = TPK_E_OVERFLOW;
+    st = TPK_E_HOST;
+  } catch (...) {
+    st = TPK_E_HOST;
   }
   if (st != TPK_OK) {
     delete h;
@@ -271,6 +275,7 @@ const char* tpk_status_string(int status) {
     case TPK_E_TIMEOUT: return "a device wait gave up";
     case TPK_E_WORKSPACE: return "workspace missing or too small";
     case TPK_E_SCRATCH_LIMIT: return "problem too large for the no-allocation backward's 32 MiB static scratch (Hq * F > 8388608)";
+    case TPK_E_HOST: return "host-side failure inside the planner (out of host memory or another C++ exception)";
     default: return "unknown status";
   }
 }

@@ -21,10 +21,25 @@
 // Pass 3 recomputes S and dP (7 matrix products instead of 5) in exchange for
 // a dQ that needs neither an fp32 accumulator nor atomics.
 //
+// Precision.  The fast mode feeds P and dS to their products as bf16, as a
+// bf16 flash-attention backward does.  The precise mode splits each of them
+// into a bf16 high part and the bf16 rounding of the remainder and multiplies
+// both (one more product for each of dV, dK and dQ), so they enter with about
+// 16 significant bits; the prep pass then also adds the forward's rounding
+// residual of O (D = dO . (O + O_lo)).  In TMEM every 32-column part of a
+// score tile holds its high half in the first 16 columns and its low half in
+// the next 16, so a part's stores only touch columns its own loads have read.
+// Inverse RoPE: with rope set, the dK and dQ epilogues rotate each fp32
+// gradient row back by its depth's angle ("DAG packing", section
+// "Positions") before the one bf16 rounding, giving gradients w.r.t. the
+// un-rotated inputs without another pass over them.
+//
 // Warp roles in passes 2 and 3: warp 0 TMA producer, warp 1 MMA issuer and
 // TMEM owner, warps 4-7 the 128 row threads (one TMEM lane each).  Waits are
 // bounded as in the forward; a timeout sets *dev_err = TPK_E_TIMEOUT.
 #include <cuda_bf16.h>
+
+#include <cmath>
 
 #include "common.cuh"
 #include "plan_handle.h"
@@ -59,13 +74,21 @@ struct BwdParams {
   int32_t F, Hq, Hkv, group_size;
   float scale, scale_log2;
   int32_t* err;
+  // inverse RoPE in the dK / dQ epilogues (rope != 0): depth [F] and the
+  // per-frequency turn factors base^(-2i/d) / (2 pi) as fp32 pairs hi + lo
+  const int32_t* depth;
+  int32_t rope;
+  float rope_hi[64], rope_lo[64];
 };
 
 // ----------------------------------------------------------------- pass 1
 // D[h, f] = dO[f, h, :] . O[f, h, :] in fp32.  A row of D bf16 is D/8
 // 16-byte chunks; that many lanes share a row (two rows per warp at D = 128,
 // four at D = 64) and add their partial dots with shuffles inside the group.
+// With o_lo (the precise mode's rounding residual of O from the forward) the
+// dot is taken with O + O_lo.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                                       const __nv_bfloat16* __restrict__ o_lo,
                                                        const __nv_bfloat16* __restrict__ dout,
                                                        float* __restrict__ dsum, int64_t F, int Hq, int D) {
   const int lane = threadIdx.x & 31;
@@ -87,10 +110,65 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
         acc = fmaf(__uint_as_float(x[j] << 16), __uint_as_float(y[j] << 16), acc);
         acc = fmaf(__uint_as_float(x[j] & 0xFFFF0000u), __uint_as_float(y[j] & 0xFFFF0000u), acc);
       }
+      if (o_lo) {
+        const uint4 c = __ldg(reinterpret_cast<const uint4*>(o_lo + w * D) + cl);
+        const uint32_t z[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc = fmaf(__uint_as_float(z[j] << 16), __uint_as_float(y[j] << 16), acc);
+          acc = fmaf(__uint_as_float(z[j] & 0xFFFF0000u), __uint_as_float(y[j] & 0xFFFF0000u), acc);
+        }
+      }
     }
     for (int off = lpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (cl == 0 && w < n) dsum[(w % Hq) * F + w / Hq] = acc;
   }
+}
+
+// cos and sin of the RoPE angle of one frequency at depth p (p < 2^24, exact
+// in fp32).  The angle in turns is p * t with t = base^(-2i/d) / (2 pi) given
+// as an fp32 pair hi + lo: the product p * hi is split exactly with an fma,
+// its whole turns dropped, the remainders added (the fraction of a turn to
+// ~3e-8), and the hardware sine / cosine evaluated on the reduced angle,
+// which lies in [-pi, pi].
+__device__ __forceinline__ void rope_cs(float pf, float hi, float lo, float& c, float& s) {
+  const float a = pf * hi;
+  const float e = fmaf(pf, hi, -a);
+  const float f = (a - rintf(a)) + fmaf(pf, lo, e);
+  __sincosf(6.28318530717958647692f * f, &s, &c);
+}
+
+// Inverse rotation of W frequency pairs of one gradient row and their store:
+// ua holds columns [f0, f0 + W) and ub columns [f0 + D/2, f0 + D/2 + W) (fp32
+// TMEM words), scaled by mul; x' = x cos + y sin, y' = y cos - x sin.
+template <int W>
+__device__ __forceinline__ void store_rotated(__nv_bfloat16* row, int f0, int half_d, const uint32_t* ua,
+                                              const uint32_t* ub, float mul, float pf, const BwdParams& p) {
+  uint32_t pa[W / 2], pb[W / 2];
+#pragma unroll
+  for (int j = 0; j < W; j += 2) {
+    float c0, s0, c1, s1;
+    rope_cs(pf, p.rope_hi[f0 + j], p.rope_lo[f0 + j], c0, s0);
+    rope_cs(pf, p.rope_hi[f0 + j + 1], p.rope_lo[f0 + j + 1], c1, s1);
+    const float x0 = __uint_as_float(ua[j]) * mul, y0 = __uint_as_float(ub[j]) * mul;
+    const float x1 = __uint_as_float(ua[j + 1]) * mul, y1 = __uint_as_float(ub[j + 1]) * mul;
+    pa[j / 2] = ptx::pack_bf16x2(fmaf(x0, c0, y0 * s0), fmaf(x1, c1, y1 * s1));
+    pb[j / 2] = ptx::pack_bf16x2(fmaf(y0, c0, -x0 * s0), fmaf(y1, c1, -x1 * s1));
+  }
+  uint4* da = reinterpret_cast<uint4*>(row + f0);
+  uint4* db = reinterpret_cast<uint4*>(row + half_d + f0);
+#pragma unroll
+  for (int j = 0; j < W / 8; ++j) {
+    da[j] = make_uint4(pa[4 * j], pa[4 * j + 1], pa[4 * j + 2], pa[4 * j + 3]);
+    db[j] = make_uint4(pb[4 * j], pb[4 * j + 1], pb[4 * j + 2], pb[4 * j + 3]);
+  }
+}
+
+// TMEM column of the bf16 A operand for the 16-row K-step kk of a 64-wide
+// score tile: part kk/2 (32 rows) starts at column 32*(kk/2), its high half in
+// the first 16 columns (8 per K-step), its low half 16 columns further.
+__device__ __forceinline__ constexpr uint32_t a_col(int kk, bool lo) {
+  return 32u * static_cast<uint32_t>(kk >> 1) + 8u * static_cast<uint32_t>(kk & 1) + (lo ? 16u : 0u);
 }
 
 // Row epilogue helper: 32 fp32 TMEM columns * mul -> 32 bf16 stored to dst.
@@ -110,9 +188,10 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
 //   MMA order per step n:  S/dP(n, half 0) | dV/dK(n-1, half 1) | S/dP(n, half 1) | dV/dK(n, half 0)
 // TMEM: slot h at [128h, 128h+128): S^T (64 cols) then dP^T (64 cols);
 // dV at [256, 256+D), dK at [256+D, 256+2D).  P^T and dS^T (bf16) overwrite
-// the first 32 columns of S^T and dP^T of their slot, in two 32-query parts
-// that the softmax releases one after the other (p_part, p_full) so the
-// first part's dV/dK products start early.  S^T and dP^T read K and V from
+// S^T and dP^T of their slot in two 32-query parts (columns 32c.., high
+// halves first, low halves 16 columns on in the precise mode) that the
+// softmax releases one after the other (p_part, p_full) so the first part's
+// dV/dK products start early.  S^T and dP^T read K and V from
 // shared memory: the two slots and dK, dV fill TMEM.
 // Warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 2 loads LSE*log2(e) and D
 // of each step's 128 queries into shared memory, 4-7 softmax of half 0,
@@ -136,7 +215,7 @@ struct KVSmem {
   int abort_flag;
 };
 
-template <int D, int NH>
+template <int D, int NH, bool kHiLo>
 __global__ void __launch_bounds__(384, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -298,9 +377,10 @@ __global__ void __launch_bounds__(384, 1)
         ptx::mma_commit(&S.s_full[slot]);
       };
       // dV += P^T dO_half, dK += dS^T Q_half (half-stages as MN-major B
-      // operands: d-column groups one 64-row box apart), then release the stage
-      // in two parts of 32 queries, each issued as soon as the softmax has
-      // stored that part's P^T and dS^T (p_part, then p_full)
+      // operands: d-column groups one 64-row box apart; the precise mode adds
+      // the low halves' products), then release the stage in two parts of 32
+      // queries, each issued as soon as the softmax has stored that part's
+      // P^T and dS^T (p_part, then p_full)
       auto issue_acc = [&](int m, int slot, bool first, uint32_t parity) {
         const uint32_t qb = ptx::smem_addr(S.q[m % NH][0]);
         const uint32_t ob = ptx::smem_addr(S.dO[m % NH][0]);
@@ -312,10 +392,14 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int kk = part * (kHalf / 32); kk < (part + 1) * (kHalf / 32); ++kk) {
             const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-            ptx::mma_ts(tmem + cdV, tmem + cS + kk * 8, ptx::desc_add(ptx::sw128_desc(ob, kHalfBox, 1024), kk * 2048),
-                        idesc_acc, acc);
-            ptx::mma_ts(tmem + cdK, tmem + cdP + kk * 8, ptx::desc_add(ptx::sw128_desc(qb, kHalfBox, 1024), kk * 2048),
-                        idesc_acc, acc);
+            const uint64_t bo = ptx::desc_add(ptx::sw128_desc(ob, kHalfBox, 1024), kk * 2048);
+            const uint64_t bq = ptx::desc_add(ptx::sw128_desc(qb, kHalfBox, 1024), kk * 2048);
+            ptx::mma_ts(tmem + cdV, tmem + cS + a_col(kk, false), bo, idesc_acc, acc);
+            ptx::mma_ts(tmem + cdK, tmem + cdP + a_col(kk, false), bq, idesc_acc, acc);
+            if constexpr (kHiLo) {
+              ptx::mma_ts(tmem + cdV, tmem + cS + a_col(kk, true), bo, idesc_acc, 1u);
+              ptx::mma_ts(tmem + cdK, tmem + cdP + a_col(kk, true), bq, idesc_acc, 1u);
+            }
           }
         }
         ptx::mma_commit(&S.q_empty[m % NH]);
@@ -396,6 +480,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         // P = 2^arg; dS = P * (dP - D), two per instruction
         uint32_t pp[16], pd[16];
+        uint32_t pl[kHiLo ? 16 : 1], dl[kHiLo ? 16 : 1];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const ulonglong2 nd = ptx::lds128u(dds + c * 32 + e);
@@ -406,13 +491,25 @@ __global__ void __launch_bounds__(384, 1)
           ptx::unf2(ptx::mul2(pa, ptx::add2(ptx::f2(__uint_as_float(ud[e]), __uint_as_float(ud[e + 1])), nd.x)), d0, d1);
           ptx::unf2(ptx::mul2(pb, ptx::add2(ptx::f2(__uint_as_float(ud[e + 2]), __uint_as_float(ud[e + 3])), nd.y)), d2,
                     d3);
-          pp[e / 2] = ptx::pack_bf16x2(p0, p1);
-          pp[e / 2 + 1] = ptx::pack_bf16x2(p2, p3);
-          pd[e / 2] = ptx::pack_bf16x2(d0, d1);
-          pd[e / 2 + 1] = ptx::pack_bf16x2(d2, d3);
+          if constexpr (kHiLo) {
+            ptx::split_bf16x2(p0, p1, pp[e / 2], pl[e / 2]);
+            ptx::split_bf16x2(p2, p3, pp[e / 2 + 1], pl[e / 2 + 1]);
+            ptx::split_bf16x2(d0, d1, pd[e / 2], dl[e / 2]);
+            ptx::split_bf16x2(d2, d3, pd[e / 2 + 1], dl[e / 2 + 1]);
+          } else {
+            pp[e / 2] = ptx::pack_bf16x2(p0, p1);
+            pp[e / 2 + 1] = ptx::pack_bf16x2(p2, p3);
+            pd[e / 2] = ptx::pack_bf16x2(d0, d1);
+            pd[e / 2 + 1] = ptx::pack_bf16x2(d2, d3);
+          }
         }
-        ptx::tmem_st16(tS + c * 16, pp);
-        ptx::tmem_st16(tdP + c * 16, pd);
+        // part c: columns 32c.. (already read above), high halves first
+        ptx::tmem_st16(tS + c * 32, pp);
+        ptx::tmem_st16(tdP + c * 32, pd);
+        if constexpr (kHiLo) {
+          ptx::tmem_st16(tS + c * 32 + 16, pl);
+          ptx::tmem_st16(tdP + c * 32 + 16, dl);
+        }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(c == 0 ? &S.p_part[half] : &S.p_full[half]);
@@ -431,12 +528,26 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t col = half == 0 ? cdV : cdK;
       const float mul = half == 0 ? 1.f : p.scale;
       __nv_bfloat16* row = (half == 0 ? p.dv : p.dk) + (static_cast<int64_t>(j) * p.Hkv + g) * D;
+      if (half == 1 && p.rope) {
+        // dK w.r.t. the un-rotated keys: frequency chunk c pairs columns
+        // 32c.. with 32c + D/2..
+        const float pf = t < nk ? static_cast<float>(__ldg(p.depth + j)) : 0.f;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t u[32];
-        ptx::tmem_ld32(tmem + lane_off + col + c * 32, u);
-        ptx::tmem_wait_ld();
-        if (t < nk) store_row32(row + c * 32, u, mul);
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t ua[32], ub[32];
+          ptx::tmem_ld32(tmem + lane_off + col + c * 32, ua);
+          ptx::tmem_ld32(tmem + lane_off + col + D / 2 + c * 32, ub);
+          ptx::tmem_wait_ld();
+          if (t < nk) store_rotated<32>(row, c * 32, D / 2, ua, ub, mul, pf, p);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          ptx::tmem_ld32(tmem + lane_off + col + c * 32, u);
+          ptx::tmem_wait_ld();
+          if (t < nk) store_row32(row + c * 32, u, mul);
+        }
       }
     }
   }
@@ -458,8 +569,9 @@ __global__ void __launch_bounds__(384, 1)
 // boxes), each released as soon as its half's dQ product is issued.
 // TMEM: slot h at [128h, 128h+128): S (64 cols) then dP (64 cols); dQ at
 // [256, 256+D); the query tile's Q and dO (bf16, D/2 cols each) after it.
-// dS (bf16) overwrites the first 32 columns of S of its slot, released to
-// the dQ products in two 32-key parts (p_part, p_full).  Q and dO are the A
+// dS (bf16) overwrites S of its slot in two 32-key parts (columns 32c..,
+// high halves first, low halves 16 columns on in the precise mode), released
+// to the dQ products one after the other (p_part, p_full).  Q and dO are the A
 // operands of the S and dP products straight from TMEM, so shared memory only
 // feeds the 64-key K / V halves: on this part an M=128, N=64 product took
 // about 75 cycles with its A tile in shared memory and 32-42 with it in TMEM
@@ -479,7 +591,7 @@ struct QSmem {
   int abort_flag;
 };
 
-template <int D, int NH>
+template <int D, int NH, bool kHiLo>
 __global__ void __launch_bounds__(384, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -591,9 +703,11 @@ __global__ void __launch_bounds__(384, 1)
             return false;
           ptx::tc_fence_after();
 #pragma unroll
-          for (int kk = part * (kHalf / 32); kk < (part + 1) * (kHalf / 32); ++kk)
-            ptx::mma_ts(tmem + cdQ, tmem + cS + kk * 8, ptx::desc_add(ptx::sw128_desc(kb, kHalfBox, 1024), kk * 2048),
-                        idesc_dq, (first && kk == 0) ? 0u : 1u);
+          for (int kk = part * (kHalf / 32); kk < (part + 1) * (kHalf / 32); ++kk) {
+            const uint64_t bk = ptx::desc_add(ptx::sw128_desc(kb, kHalfBox, 1024), kk * 2048);
+            ptx::mma_ts(tmem + cdQ, tmem + cS + a_col(kk, false), bk, idesc_dq, (first && kk == 0) ? 0u : 1u);
+            if constexpr (kHiLo) ptx::mma_ts(tmem + cdQ, tmem + cS + a_col(kk, true), bk, idesc_dq, 1u);
+          }
         }
         ptx::mma_commit(&S.kv_empty[m % NH]);
         return true;
@@ -710,14 +824,20 @@ __global__ void __launch_bounds__(384, 1)
           for (int e = 0; e < 32; ++e) arg[e] = -INFINITY;
         }
         uint32_t pd[16];
+        uint32_t dl[kHiLo ? 16 : 1];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const uint64_t pp = ptx::f2(ptx::ex2(arg[e]), ptx::ex2(arg[e + 1]));
           float d0, d1;
           ptx::unf2(ptx::mul2(pp, ptx::add2(ptx::f2(__uint_as_float(ud[e]), __uint_as_float(ud[e + 1])), ndd2)), d0, d1);
-          pd[e / 2] = ptx::pack_bf16x2(d0, d1);
+          if constexpr (kHiLo)
+            ptx::split_bf16x2(d0, d1, pd[e / 2], dl[e / 2]);
+          else
+            pd[e / 2] = ptx::pack_bf16x2(d0, d1);
         }
-        ptx::tmem_st16(tS + c * 16, pd);
+        // part c: columns 32c.. (already read above), high halves first
+        ptx::tmem_st16(tS + c * 32, pd);
+        if constexpr (kHiLo) ptx::tmem_st16(tS + c * 32 + 16, dl);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(c == 0 ? &S.p_part[half] : &S.p_full[half]);
@@ -728,15 +848,33 @@ __global__ void __launch_bounds__(384, 1)
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
-      // epilogue: each warpgroup writes half of the head dimension
       ptx::tc_fence_after();
       __nv_bfloat16* row = p.dq + (static_cast<int64_t>(i) * p.Hq + h) * D;
-#pragma unroll
-      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
-        uint32_t u[32];
-        ptx::tmem_ld32(tmem + lane_off + cdQ + c * 32, u);
+      if (p.rope) {
+        // dQ w.r.t. the un-rotated queries: each warpgroup takes a quarter of
+        // the columns, frequencies [half*D/4, +D/4), and their partners D/2 on
+        constexpr int W = D / 4;
+        const int f0 = half * W;
+        const float pf = row_ok ? static_cast<float>(__ldg(p.depth + i)) : 0.f;
+        uint32_t ua[W], ub[W];
+        if constexpr (W == 32) {
+          ptx::tmem_ld32(tmem + lane_off + cdQ + f0, ua);
+          ptx::tmem_ld32(tmem + lane_off + cdQ + D / 2 + f0, ub);
+        } else {
+          ptx::tmem_ld16(tmem + lane_off + cdQ + f0, ua);
+          ptx::tmem_ld16(tmem + lane_off + cdQ + D / 2 + f0, ub);
+        }
         ptx::tmem_wait_ld();
-        if (row_ok) store_row32(row + c * 32, u, p.scale);
+        if (row_ok) store_rotated<W>(row, f0, D / 2, ua, ub, p.scale, pf, p);
+      } else {
+        // each warpgroup writes half of the head dimension
+#pragma unroll
+        for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
+          uint32_t u[32];
+          ptx::tmem_ld32(tmem + lane_off + cdQ + c * 32, u);
+          ptx::tmem_wait_ld();
+          if (row_ok) store_row32(row + c * 32, u, p.scale);
+        }
       }
     }
   }
@@ -750,85 +888,50 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0 && S.abort_flag && p.err) atomicExch(p.err, TPK_E_TIMEOUT);
 }
 
-template <typename Kern>
-int set_smem(Kern kern, size_t bytes, bool& done) {
-  if (!done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) != cudaSuccess)
-      return TPK_E_CUDA;
-    done = true;
-  }
-  return TPK_OK;
-}
-
-template <int D, int NH>
+template <int D, int NH, bool kHiLo>
 int launch_kv(const BwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
               const CUtensorMap& tdo, int64_t n_ktiles, cudaStream_t stream) {
   constexpr size_t smem = sizeof(KVSmem<D, NH>) + 1024;
   static_assert(smem <= 227 * 1024, "shared memory");
-  static bool cfg = false;
-  int st = set_smem(bwd_kv_kernel<D, NH>, smem, cfg);
+  static PerContext<int> cfg;   // the shared-memory limit is per context (per device)
+  int st = set_smem_once(cfg, bwd_kv_kernel<D, NH, kHiLo>, smem);
   if (st != TPK_OK) return st;
   const int64_t items = n_ktiles * prm.Hkv;
   if (items > 0x7fffffff) return TPK_E_OVERFLOW;
-  if (items > 0) bwd_kv_kernel<D, NH><<<static_cast<unsigned>(items), 384, smem, stream>>>(tq, tk, tv, tdo, prm);
+  if (items > 0)
+    bwd_kv_kernel<D, NH, kHiLo><<<static_cast<unsigned>(items), 384, smem, stream>>>(tq, tk, tv, tdo, prm);
   return cuda_status(cudaGetLastError());
 }
 
-template <int D, int NH>
+template <int D, int NH, bool kHiLo>
 int launch_q(const BwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
              const CUtensorMap& tdo, int64_t n_qtiles, cudaStream_t stream) {
   constexpr size_t smem = sizeof(QSmem<D, NH>) + 1024;
   static_assert(smem <= 227 * 1024, "shared memory");
-  static bool cfg = false;
-  int st = set_smem(bwd_q_kernel<D, NH>, smem, cfg);
+  static PerContext<int> cfg;
+  int st = set_smem_once(cfg, bwd_q_kernel<D, NH, kHiLo>, smem);
   if (st != TPK_OK) return st;
   const int64_t items = n_qtiles * prm.Hq;
   if (items > 0x7fffffff) return TPK_E_OVERFLOW;
-  if (items > 0) bwd_q_kernel<D, NH><<<static_cast<unsigned>(items), 384, smem, stream>>>(tq, tk, tv, tdo, prm);
+  if (items > 0)
+    bwd_q_kernel<D, NH, kHiLo><<<static_cast<unsigned>(items), 384, smem, stream>>>(tq, tk, tv, tdo, prm);
   return cuda_status(cudaGetLastError());
 }
 
-}  // namespace
-}  // namespace tpk
-
-extern "C" size_t tpk_attn_workspace_bytes(const tpk_plan* plan, int32_t Hq, int32_t Hkv, int32_t d, int32_t backward) {
-  (void)Hkv;
-  (void)d;
-  if (!plan || !backward || Hq <= 0) return 0;
-  // D[h, f] = dO . O, fp32 [Hq, F]
-  return (static_cast<size_t>(Hq) * static_cast<size_t>(plan->p.F) * 4 + 255) & ~size_t(255);
-}
-
-extern "C" int tpk_tree_attn_bwd_phase(int32_t phase, const tpk_plan* plan, const void* dev_image, const void* q,
-                                       const void* k, const void* v, const void* o, const float* lse,
-                                       const void* dout, void* dq, void* dk, void* dv, int32_t Hq, int32_t Hkv,
-                                       int32_t d, float scale, void* workspace, size_t ws_bytes, int32_t* dev_err,
-                                       void* stream) {
-  using namespace tpk;
-  if (!plan || phase < TPK_BWD_PREP || phase > TPK_BWD_DQ) return TPK_E_ARG;
-  if (Hq <= 0 || Hkv <= 0 || !(scale > 0.f)) return TPK_E_ARG;
-  if ((d != 64 && d != 128) || Hq % Hkv != 0) return TPK_E_UNSUPPORTED;
-  if (phase == TPK_BWD_PREP && (!o || !dout)) return TPK_E_ARG;
-  if (phase == TPK_BWD_DKDV && (!dev_image || !q || !k || !v || !lse || !dout || !dk || !dv)) return TPK_E_ARG;
-  if (phase == TPK_BWD_DQ && (!dev_image || !q || !k || !v || !lse || !dout || !dq)) return TPK_E_ARG;
-  if ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv) |
-       reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dout)) % 16)
-    return TPK_E_ARG;
-  const Plan& P = plan->p;
-  if (P.F == 0) return TPK_OK;
-  const size_t need = tpk_attn_workspace_bytes(plan, Hq, Hkv, d, 1);
-  if (!workspace || ws_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256) return TPK_E_WORKSPACE;
-  int st = check_device();
-  if (st != TPK_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+// One phase of the backward, options already checked.
+int bwd_phase(int32_t phase, const Plan& P, const void* dev_image, const void* q, const void* k, const void* v,
+              const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv, int32_t Hq,
+              int32_t Hkv, int32_t d, float scale, bool precise, double rope_base, const void* o_lo,
+              void* workspace, int32_t* dev_err, cudaStream_t s) {
+  int st;
   if (phase == TPK_BWD_PREP) {
     const int64_t rows_per_block = 8 * (32 / (d / 8));   // 8 warps, 32/(d/8) rows each
     int64_t blocks = (P.F * Hq + rows_per_block - 1) / rows_per_block;
     const int64_t cap = int64_t{num_sms()} * 32;
     if (blocks > cap) blocks = cap;
-    bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(o),
-                                                                  static_cast<const __nv_bfloat16*>(dout),
-                                                                  static_cast<float*>(workspace), P.F, Hq, d);
+    bwd_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(o), precise ? static_cast<const __nv_bfloat16*>(o_lo) : nullptr,
+        static_cast<const __nv_bfloat16*>(dout), static_cast<float*>(workspace), P.F, Hq, d);
     return cuda_status(cudaGetLastError());
   }
   CUtensorMap tq, tk, tv, tdo;
@@ -861,20 +964,96 @@ extern "C" int tpk_tree_attn_bwd_phase(int32_t phase, const tpk_plan* plan, cons
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
   prm.err = dev_err;
+  prm.depth = reinterpret_cast<const int32_t*>(img + P.off_depth);
+  prm.rope = rope_base > 0.0 ? 1 : 0;
+  for (int i = 0; i < 64; ++i) {
+    // turns per unit depth of frequency i: base^(-2i/d) / (2 pi), as hi + lo
+    const double t = i < d / 2 && prm.rope ? std::pow(rope_base, -2.0 * i / d) / 6.283185307179586476925286766559 : 0.0;
+    prm.rope_hi[i] = static_cast<float>(t);
+    prm.rope_lo[i] = static_cast<float>(t - static_cast<double>(prm.rope_hi[i]));
+  }
   const int64_t nkt = static_cast<int64_t>(P.kt_k0.size()), nqt = static_cast<int64_t>(P.qt_q0.size());
   if (phase == TPK_BWD_DKDV) {
     // the dK/dV pass streams Q and dO in 64-query half-stages
     CUtensorMap tq64, tdo64;
     if ((st = make_map_bf16(&tq64, q, P.F, Hq, d, 64)) != TPK_OK) return st;
     if ((st = make_map_bf16(&tdo64, dout, P.F, Hq, d, 64)) != TPK_OK) return st;
-    return d == 128 ? launch_kv<128, 4>(prm, tq64, tk, tv, tdo64, nkt, s)
-                    : launch_kv<64, 8>(prm, tq64, tk, tv, tdo64, nkt, s);
+    if (d == 128)
+      return precise ? launch_kv<128, 4, true>(prm, tq64, tk, tv, tdo64, nkt, s)
+                     : launch_kv<128, 4, false>(prm, tq64, tk, tv, tdo64, nkt, s);
+    return precise ? launch_kv<64, 8, true>(prm, tq64, tk, tv, tdo64, nkt, s)
+                   : launch_kv<64, 8, false>(prm, tq64, tk, tv, tdo64, nkt, s);
   }
   // the dQ pass streams K and V in 64-key half-stages
   CUtensorMap tk64, tv64;
   if ((st = make_map_bf16(&tk64, k, P.F, Hkv, d, 64)) != TPK_OK) return st;
   if ((st = make_map_bf16(&tv64, v, P.F, Hkv, d, 64)) != TPK_OK) return st;
-  return d == 128 ? launch_q<128, 4>(prm, tq, tk64, tv64, tdo, nqt, s) : launch_q<64, 8>(prm, tq, tk64, tv64, tdo, nqt, s);
+  if (d == 128)
+    return precise ? launch_q<128, 4, true>(prm, tq, tk64, tv64, tdo, nqt, s)
+                   : launch_q<128, 4, false>(prm, tq, tk64, tv64, tdo, nqt, s);
+  return precise ? launch_q<64, 8, true>(prm, tq, tk64, tv64, tdo, nqt, s)
+                 : launch_q<64, 8, false>(prm, tq, tk64, tv64, tdo, nqt, s);
+}
+
+}  // namespace
+}  // namespace tpk
+
+extern "C" size_t tpk_attn_workspace_bytes(const tpk_plan* plan, int32_t Hq, int32_t Hkv, int32_t d, int32_t backward) {
+  (void)Hkv;
+  (void)d;
+  if (!plan || !backward || Hq <= 0) return 0;
+  // D[h, f] = dO . O, fp32 [Hq, F]
+  return (static_cast<size_t>(Hq) * static_cast<size_t>(plan->p.F) * 4 + 255) & ~size_t(255);
+}
+
+extern "C" int tpk_tree_attn_bwd_ex(int32_t phase, const tpk_plan* plan, const void* dev_image, const void* q,
+                                    const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                                    void* dq, void* dk, void* dv, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                                    const tpk_attn_opts* opts, void* workspace, size_t ws_bytes, int32_t* dev_err,
+                                    void* stream) {
+  using namespace tpk;
+  if (!plan || phase < TPK_BWD_ALL || phase > TPK_BWD_DQ) return TPK_E_ARG;
+  if (Hq <= 0 || Hkv <= 0 || !(scale > 0.f)) return TPK_E_ARG;
+  if ((d != 64 && d != 128) || Hq % Hkv != 0) return TPK_E_UNSUPPORTED;
+  const bool all = phase == TPK_BWD_ALL;
+  const bool prep = all || phase == TPK_BWD_PREP, kv = all || phase == TPK_BWD_DKDV, qp = all || phase == TPK_BWD_DQ;
+  if (prep && (!o || !dout)) return TPK_E_ARG;
+  if ((kv || qp) && (!dev_image || !q || !k || !v || !lse || !dout)) return TPK_E_ARG;
+  if ((kv && (!dk || !dv)) || (qp && !dq)) return TPK_E_ARG;
+  const bool precise = opts && opts->precision == TPK_PREC_PRECISE;
+  const double rope_base = opts ? opts->rope_base : 0.0;
+  const void* o_lo = opts ? opts->o_lo : nullptr;
+  if (opts && opts->precision != TPK_PREC_FAST && opts->precision != TPK_PREC_PRECISE) return TPK_E_ARG;
+  if (!(rope_base == 0.0 || rope_base > 1.0)) return TPK_E_ARG;
+  if ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv) |
+       reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(o_lo)) % 16)
+    return TPK_E_ARG;
+  const Plan& P = plan->p;
+  // the fused inverse rotation forms the angle from the depth in fp32
+  if (rope_base > 1.0 && P.max_depth >= (int64_t{1} << 24)) return TPK_E_UNSUPPORTED;
+  if (P.F == 0) return TPK_OK;
+  const size_t need = tpk_attn_workspace_bytes(plan, Hq, Hkv, d, 1);
+  if (!workspace || ws_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256) return TPK_E_WORKSPACE;
+  int st = check_device();
+  if (st != TPK_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int32_t ph = TPK_BWD_PREP; ph <= TPK_BWD_DQ; ++ph) {
+    if (!all && ph != phase) continue;
+    st = bwd_phase(ph, P, dev_image, q, k, v, o, lse, dout, dq, dk, dv, Hq, Hkv, d, scale, precise, rope_base, o_lo,
+                   workspace, dev_err, s);
+    if (st != TPK_OK) return st;
+  }
+  return TPK_OK;
+}
+
+extern "C" int tpk_tree_attn_bwd_phase(int32_t phase, const tpk_plan* plan, const void* dev_image, const void* q,
+                                       const void* k, const void* v, const void* o, const float* lse,
+                                       const void* dout, void* dq, void* dk, void* dv, int32_t Hq, int32_t Hkv,
+                                       int32_t d, float scale, void* workspace, size_t ws_bytes, int32_t* dev_err,
+                                       void* stream) {
+  if (phase < TPK_BWD_PREP || phase > TPK_BWD_DQ) return TPK_E_ARG;
+  return tpk_tree_attn_bwd_ex(phase, plan, dev_image, q, k, v, o, lse, dout, dq, dk, dv, Hq, Hkv, d, scale, nullptr,
+                              workspace, ws_bytes, dev_err, stream);
 }
 
 extern "C" int tpk_tree_attn_bwd(const tpk_plan* plan, const void* dev_image, const void* q, const void* k,
@@ -882,12 +1061,8 @@ extern "C" int tpk_tree_attn_bwd(const tpk_plan* plan, const void* dev_image, co
                                  void* dv, int32_t Hq, int32_t Hkv, int32_t d, float scale, void* workspace,
                                  size_t ws_bytes, int32_t* dev_err, void* stream) {
   if (!plan || !dev_image || !q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return TPK_E_ARG;
-  for (int32_t phase = TPK_BWD_PREP; phase <= TPK_BWD_DQ; ++phase) {
-    const int st = tpk_tree_attn_bwd_phase(phase, plan, dev_image, q, k, v, o, lse, dout, dq, dk, dv, Hq, Hkv, d,
-                                           scale, workspace, ws_bytes, dev_err, stream);
-    if (st != TPK_OK) return st;
-  }
-  return TPK_OK;
+  return tpk_tree_attn_bwd_ex(TPK_BWD_ALL, plan, dev_image, q, k, v, o, lse, dout, dq, dk, dv, Hq, Hkv, d, scale,
+                              nullptr, workspace, ws_bytes, dev_err, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -901,32 +1076,25 @@ extern "C" int tpk_tree_attn_bwd(const tpk_plan* plan, const void* dev_image, co
 // file-scope device array instead.  Every GPU that loads the library keeps it
 // (32 MiB) until the process exits.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
 namespace tpk {
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t{32} << 20;   // 32 MiB: Hq * F <= 8,388,608
 static __device__ __align__(256) uint8_t g_bwd_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+// Device address of g_bwd_scratch in the current context, looked up once per
+// context (with it current) and cached by the context's unique id: another
+// device, a context the caller made current, or the context that replaces one
+// destroyed by cudaDeviceReset each get their own lookup, never a stale
+// address.  In host code the name g_bwd_scratch is a host-side stand-in, not
+// a device address, so kernels only ever receive the looked-up pointer.
+PerContext<void*> g_scratch_addr;
 
-// Device address of g_bwd_scratch on the current device, looked up once per
-// device (with that device current) and cached.
 int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TPK_E_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return TPK_E_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) return TPK_E_CUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
-  return TPK_OK;
+  return g_scratch_addr.get(out, [](void** p) {
+    *p = nullptr;
+    return (cudaGetSymbolAddress(p, g_bwd_scratch) == cudaSuccess && *p) ? TPK_OK : TPK_E_CUDA;
+  });
 }
 
 }  // namespace

@@ -41,6 +41,12 @@
 // Online softmax with a lazily raised running maximum: O and the row sum are
 // rescaled only when the block maximum exceeds the one in use by more than
 // 2^8, which keeps exponentials <= 256 and skips almost every rescale.
+// P is stored part by part: part c (half of the S columns' keys) at column
+// c*kCols/2, as bf16.  The precise mode stores the bf16 rounding of what that
+// leaves out kCols/4 columns further and adds its PV product, so P enters PV
+// with about 16 significant bits; it can also write the bf16 rounding
+// residual of O next to O, for a backward that forms dO . O before O's
+// rounding.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -69,6 +75,7 @@ struct FwdParams {
   const int32_t* qt_order;
   const int32_t* subtree_end;
   __nv_bfloat16* o;
+  __nv_bfloat16* o_lo;   // precise mode: O - bf16(O), or null
   float* lse;
   int32_t F, Hq, n_hgroups, group_size;
   float scale_log2;
@@ -97,7 +104,7 @@ constexpr size_t fwd_smem_bytes() {
   return sizeof(FwdSmem<D, HPC, NS>) + 1024;
 }
 
-template <int D, int HPC, int NS>
+template <int D, int HPC, int NS, bool kHiLo>
 __global__ void __launch_bounds__(384, 1)
     tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -212,7 +219,10 @@ __global__ void __launch_bounds__(384, 1)
           // groups one box apart), K = 16 keys = 2 KB further per step
           const uint64_t bdesc =
               ptx::desc_add(ptx::sw128_desc(v_base, kBox, 1024), (kCols / 16 * hf + kk) * 2048);
-          ptx::mma_ts(o_col, p_col + kk * 8, bdesc, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+          // P of this step: the part's columns start at part * kCols/2
+          const uint32_t a = p_col + part * (kCols / 2) + (kk - part * kSteps) * 8;
+          ptx::mma_ts(o_col, a, bdesc, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+          if constexpr (kHiLo) ptx::mma_ts(o_col, a + kCols / 4, bdesc, idesc_pv, 1u);
         }
       };
       // PV of slot s's n-th S (block blk, keys kCols*hf..), once both parts of its P are stored
@@ -423,6 +433,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t pk[kCols / 4];
+        uint32_t pl[kHiLo ? kCols / 4 : 1];
 #pragma unroll
         for (int j = 0; j < kCols / 4; ++j) {
           float a0, a1;
@@ -430,12 +441,20 @@ __global__ void __launch_bounds__(384, 1)
                     a0, a1);
           const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
           sum2[j & 1] = ptx::add2(sum2[j & 1], ptx::f2(p0, p1));
-          pk[j] = ptx::pack_bf16x2(p0, p1);
+          if constexpr (kHiLo)
+            ptx::split_bf16x2(p0, p1, pk[j], pl[j]);
+          else
+            pk[j] = ptx::pack_bf16x2(p0, p1);
         }
-        if constexpr (kCols == 128)
-          ptx::tmem_st32(s_tm + c * 32, pk);
-        else
-          ptx::tmem_st16(s_tm + c * 16, pk);
+        // part c at column c * kCols/2 (every S column was read above); the
+        // precise mode's low halves kCols/4 further
+        if constexpr (kCols == 128) {
+          ptx::tmem_st32(s_tm + c * 64, pk);
+          if constexpr (kHiLo) ptx::tmem_st32(s_tm + c * 64 + 32, pl);
+        } else {
+          ptx::tmem_st16(s_tm + c * 32, pk);
+          if constexpr (kHiLo) ptx::tmem_st16(s_tm + c * 32 + 16, pl);
+        }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(c == 0 ? &S.p_half[slot] : &S.p_full[slot]);
@@ -476,14 +495,24 @@ __global__ void __launch_bounds__(384, 1)
           ptx::tmem_ld32(ob + c * 32, ub);
           ptx::tmem_wait_ld();
           if (r < nq) {
-            uint32_t pk[16];
+            uint32_t pk[16], pl[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              pk[j] = ptx::pack_bf16x2(__uint_as_float(ua[2 * j]) * w0 + __uint_as_float(ub[2 * j]) * w1,
-                                       __uint_as_float(ua[2 * j + 1]) * w0 + __uint_as_float(ub[2 * j + 1]) * w1);
+            for (int j = 0; j < 16; ++j) {
+              const float x0 = __uint_as_float(ua[2 * j]) * w0 + __uint_as_float(ub[2 * j]) * w1;
+              const float x1 = __uint_as_float(ua[2 * j + 1]) * w0 + __uint_as_float(ub[2 * j + 1]) * w1;
+              if constexpr (kHiLo)
+                ptx::split_bf16x2(x0, x1, pk[j], pl[j]);
+              else
+                pk[j] = ptx::pack_bf16x2(x0, x1);
+            }
             uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
             for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            if (kHiLo && p.o_lo) {
+              uint4* dlo = reinterpret_cast<uint4*>(p.o_lo + (orow - p.o) + c * 32);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) dlo[j] = make_uint4(pl[4 * j], pl[4 * j + 1], pl[4 * j + 2], pl[4 * j + 3]);
+            }
           }
         }
         if (r < nq && slot == 0) {
@@ -507,13 +536,23 @@ __global__ void __launch_bounds__(384, 1)
         ptx::tmem_ld32(o_tm + c * 32, u);
         ptx::tmem_wait_ld();
         if (r < nq) {
-          uint32_t pk[16];
+          uint32_t pk[16], pl[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[j] = ptx::pack_bf16x2(__uint_as_float(u[2 * j]) * inv_l, __uint_as_float(u[2 * j + 1]) * inv_l);
+          for (int j = 0; j < 16; ++j) {
+            const float x0 = __uint_as_float(u[2 * j]) * inv_l, x1 = __uint_as_float(u[2 * j + 1]) * inv_l;
+            if constexpr (kHiLo)
+              ptx::split_bf16x2(x0, x1, pk[j], pl[j]);
+            else
+              pk[j] = ptx::pack_bf16x2(x0, x1);
+          }
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          if (kHiLo && p.o_lo) {
+            uint4* dlo = reinterpret_cast<uint4*>(p.o_lo + (orow - p.o) + c * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dlo[j] = make_uint4(pl[4 * j], pl[4 * j + 1], pl[4 * j + 2], pl[4 * j + 3]);
+          }
         }
       }
       if (r < nq) {
@@ -533,44 +572,58 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0 && S.abort_flag && p.err) atomicExch(p.err, TPK_E_TIMEOUT);
 }
 
-template <int D, int HPC, int NS>
+template <int D, int HPC, int NS, bool kHiLo>
 int launch(const FwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, int64_t items,
            cudaStream_t stream) {
-  auto kern = tree_attn_fwd_kernel<D, HPC, NS>;
+  auto kern = tree_attn_fwd_kernel<D, HPC, NS, kHiLo>;
   constexpr size_t smem = fwd_smem_bytes<D, HPC, NS>();
   static_assert(smem <= 227 * 1024, "shared memory");
-  static bool configured = false;
-  if (!configured) {
+  // the shared-memory limit is an attribute of the kernel in one context, so
+  // it is set once per context (per device), not once per process
+  static PerContext<int> configured;
+  int unused = 0;
+  const int st = configured.get(&unused, [&](int*) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
       return TPK_E_CUDA;
-    {
-      // the warpgroups' register shares must fit in what the CTA launches with
-      cudaFuncAttributes fa;
-      if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return TPK_E_CUDA;
-      if (fa.numRegs * 384 < kRegsNeeded) return TPK_E_UNSUPPORTED;
-    }
-    configured = true;
-  }
+    // the warpgroups' register shares must fit in what the CTA launches with
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return TPK_E_CUDA;
+    if (fa.numRegs * 384 < kRegsNeeded) return TPK_E_UNSUPPORTED;
+    return TPK_OK;
+  });
+  if (st != TPK_OK) return st;
   if (items <= 0) return TPK_OK;
   if (items > 0x7fffffff) return TPK_E_OVERFLOW;
   kern<<<static_cast<unsigned>(items), 384, smem, stream>>>(tq, tk, tv, prm);
   return cuda_status(cudaGetLastError());
 }
 
+template <bool kHiLo>
+int launch_all(int d, int hpc, const FwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk,
+               const CUtensorMap& tv, int64_t items, cudaStream_t s) {
+  if (d == 128)
+    return hpc == 2 ? launch<128, 2, 2, kHiLo>(prm, tq, tk, tv, items, s) : launch<128, 1, 2, kHiLo>(prm, tq, tk, tv, items, s);
+  return hpc == 2 ? launch<64, 2, 3, kHiLo>(prm, tq, tk, tv, items, s) : launch<64, 1, 4, kHiLo>(prm, tq, tk, tv, items, s);
+}
+
 }  // namespace
 }  // namespace tpk
 
-extern "C" int tpk_tree_attn_fwd(const tpk_plan* plan, const void* dev_image, const void* q, const void* k,
-                                 const void* v, void* o, float* lse, int32_t Hq, int32_t Hkv, int32_t d, float scale,
-                                 void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
+extern "C" int tpk_tree_attn_fwd_ex(const tpk_plan* plan, const void* dev_image, const void* q, const void* k,
+                                    const void* v, void* o, float* lse, int32_t Hq, int32_t Hkv, int32_t d,
+                                    float scale, const tpk_attn_opts* opts, int32_t* dev_err, void* stream) {
   using namespace tpk;
-  (void)workspace;
-  (void)ws_bytes;
   if (!plan || !dev_image || !q || !k || !v || !o || !lse) return TPK_E_ARG;
   if (Hq <= 0 || Hkv <= 0 || !(scale > 0.f)) return TPK_E_ARG;
   if ((d != 64 && d != 128) || Hq % Hkv != 0) return TPK_E_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(dev_image) % 256) % 16) return TPK_E_ARG;
+  if (opts && ((opts->precision != TPK_PREC_FAST && opts->precision != TPK_PREC_PRECISE) || opts->rope_base != 0.0))
+    return TPK_E_ARG;
+  const bool precise = opts && opts->precision == TPK_PREC_PRECISE;
+  void* o_lo = precise ? opts->o_lo : nullptr;
+  if ((reinterpret_cast<uintptr_t>(o) | reinterpret_cast<uintptr_t>(o_lo) | reinterpret_cast<uintptr_t>(dev_image) % 256) %
+      16)
+    return TPK_E_ARG;
   const Plan& P = plan->p;
   if (P.F == 0) return TPK_OK;
   int st = check_device();
@@ -588,6 +641,7 @@ extern "C" int tpk_tree_attn_fwd(const tpk_plan* plan, const void* dev_image, co
   prm.qt_order = reinterpret_cast<const int32_t*>(img + P.off_qt_order);
   prm.subtree_end = reinterpret_cast<const int32_t*>(img + P.off_subtree_end);
   prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.o_lo = static_cast<__nv_bfloat16*>(o_lo);
   prm.lse = lse;
   prm.F = static_cast<int32_t>(P.F);
   prm.Hq = Hq;
@@ -598,6 +652,13 @@ extern "C" int tpk_tree_attn_fwd(const tpk_plan* plan, const void* dev_image, co
   prm.n_hgroups = Hq / hpc;
   const int64_t items = static_cast<int64_t>(P.qt_q0.size()) * prm.n_hgroups;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (d == 128) return hpc == 2 ? launch<128, 2, 2>(prm, tq, tk, tv, items, s) : launch<128, 1, 2>(prm, tq, tk, tv, items, s);
-  return hpc == 2 ? launch<64, 2, 3>(prm, tq, tk, tv, items, s) : launch<64, 1, 4>(prm, tq, tk, tv, items, s);
+  return precise ? launch_all<true>(d, hpc, prm, tq, tk, tv, items, s) : launch_all<false>(d, hpc, prm, tq, tk, tv, items, s);
+}
+
+extern "C" int tpk_tree_attn_fwd(const tpk_plan* plan, const void* dev_image, const void* q, const void* k,
+                                 const void* v, void* o, float* lse, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                                 void* workspace, size_t ws_bytes, int32_t* dev_err, void* stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  return tpk_tree_attn_fwd_ex(plan, dev_image, q, k, v, o, lse, Hq, Hkv, d, scale, nullptr, dev_err, stream);
 }

@@ -7,6 +7,9 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <mutex>
+#include <utility>
+#include <vector>
 
 #include "tpk.h"
 
@@ -30,16 +33,17 @@ inline int check_device() {
   return TPK_OK;
 }
 
+// Looked up once (thread-safe static initialisation).
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -58,6 +62,75 @@ inline int make_map_bf16(CUtensorMap* map, const void* base, int64_t rows, int h
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? TPK_OK : TPK_E_CUDA;
+}
+
+// Unique id of the CUDA context the calling thread's runtime calls act on
+// (the device's primary context unless the caller made another one current).
+// Ids are never reused within a process, so a context created after
+// cudaDeviceReset, or another context on the same device, gets a new one.
+// Returns false if no context is current or the driver cannot be asked.
+inline bool current_context_id(unsigned long long* id) {
+  static const auto fns = [] {
+    void* get = nullptr;
+    void* gid = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &get, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      get = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &gid, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      gid = nullptr;
+    return std::make_pair(reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(get), reinterpret_cast<PFN_cuCtxGetId_v12000>(gid));
+  }();
+  if (!fns.first || !fns.second) return false;
+  CUcontext ctx = nullptr;
+  if (fns.first(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return fns.second(ctx, id) == CUDA_SUCCESS;
+}
+
+// A value set up once per CUDA context: kernel attributes such as the
+// dynamic shared-memory limit belong to the context (one per device for the
+// runtime's primary contexts), so a process that drives several GPUs, or
+// recreates a context, has to set them again there.  Thread-safe.
+template <typename T>
+class PerContext {
+ public:
+  // The value for the current context, made by make(&value) -> status on
+  // first use there.  make runs with the lock held; it may be a runtime call
+  // that itself initialises the context, so the context is looked up after it.
+  template <typename Make>
+  int get(T* out, Make make) {
+    unsigned long long id = 0;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (current_context_id(&id))
+      for (const auto& e : done_)
+        if (e.first == id) {
+          *out = e.second;
+          return TPK_OK;
+        }
+    T v{};
+    const int st = make(&v);
+    if (st != TPK_OK) return st;
+    if (current_context_id(&id)) done_.emplace_back(id, v);
+    *out = v;
+    return TPK_OK;
+  }
+
+ private:
+  std::mutex mu_;
+  std::vector<std::pair<unsigned long long, T>> done_;
+};
+
+// Raise a kernel's dynamic shared-memory limit to `bytes`, once per context.
+template <typename Kern>
+int set_smem_once(PerContext<int>& rec, Kern kern, size_t bytes) {
+  int unused = 0;
+  return rec.get(&unused, [&](int*) {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) ==
+                   cudaSuccess
+               ? TPK_OK
+               : TPK_E_CUDA;
+  });
 }
 
 inline int num_sms() {

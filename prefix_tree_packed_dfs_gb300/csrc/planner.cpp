@@ -46,8 +46,11 @@
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
+#include <exception>
 #include <limits>
+#include <mutex>
 #include <numeric>
+#include <system_error>
 #include <thread>
 #include <unordered_map>
 
@@ -118,7 +121,13 @@ int64_t planner_threads() {
 }
 
 // fn(i) for i in [0, n) on the planner's host threads; every i writes only
-// its own outputs, so the result does not depend on the schedule
+// its own outputs, so the result does not depend on the schedule.
+// An exception thrown by fn on any thread (std::bad_alloc, say) stops the
+// remaining indices from being started and is rethrown on the calling thread
+// after every worker has joined, so it reaches the C ABI's handler instead of
+// terminating the process.  If a worker thread cannot be created (a process
+// or container thread limit), the threads that exist -- at least the calling
+// one -- take the remaining indices.
 template <typename Fn>
 void parallel_for(int64_t n, Fn fn) {
   const int64_t nt = std::min<int64_t>(planner_threads(), n);
@@ -127,14 +136,28 @@ void parallel_for(int64_t n, Fn fn) {
     return;
   }
   std::atomic<int64_t> next{0};
+  std::mutex err_mu;
+  std::exception_ptr err;
   auto worker = [&]() {
-    for (int64_t i; (i = next.fetch_add(1, std::memory_order_relaxed)) < n;) fn(i);
+    try {
+      for (int64_t i; (i = next.fetch_add(1, std::memory_order_relaxed)) < n;) fn(i);
+    } catch (...) {
+      next.store(n, std::memory_order_relaxed);   // no new indices after a failure
+      std::lock_guard<std::mutex> lock(err_mu);
+      if (!err) err = std::current_exception();
+    }
   };
   std::vector<std::thread> pool;
-  pool.reserve(static_cast<size_t>(nt - 1));
-  for (int64_t t = 1; t < nt; ++t) pool.emplace_back(worker);
+  try {
+    pool.reserve(static_cast<size_t>(nt - 1));
+    for (int64_t t = 1; t < nt; ++t) pool.emplace_back(worker);
+  } catch (const std::system_error&) {
+    // fewer threads than asked for: the ones started and this one share the work
+  } catch (const std::bad_alloc&) {
+  }
   worker();
   for (auto& th : pool) th.join();
+  if (err) std::rethrow_exception(err);
 }
 
 // std::stable_sort of v by comp, on up to 16 host threads: contiguous chunks

@@ -231,6 +231,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Two fp32 values as a bf16 pair (hi, packed as pack_bf16x2) plus the bf16
+// rounding of what the pair leaves out (lo): a ~ hi + lo to about 16
+// significant bits.  The remainders a - bf16(a) are exact in fp32.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(a, b);
+  lo = pack_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
+}
+
 // 16-byte shared-memory load through the shared window (the kernels address
 // their dynamic shared memory through an integer-aligned pointer, which the
 // compiler would otherwise access with generic loads).

@@ -20,12 +20,12 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
-def _need(t, dtype, name, ndim=None):
+def _need(t, dtype, name, ndim=None, cuda=True):
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
     if t.dtype != dtype:
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
-    if not t.is_cuda:
+    if cuda and not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor (no CPU path exists)" % name)
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
@@ -225,26 +225,71 @@ def rope_by_depth(q, k, depth, base, inverse=False, q_out=None, k_out=None):
     return q_out, k_out
 
 
-def tree_attn_fwd(dplan, q, k, v, scale=None, out=None, lse=None, dev_err=None):
-    """Forward tree attention; returns (O [F,Hq,d] bf16, LSE [Hq,F] fp32)."""
-    lib = B.load()
+def _shape(t, shape, name):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def _on_device(ref, *named):
+    """Every tensor (None skipped) a CUDA tensor on ref's device.  Checked after
+    the shapes, so a wrong shape is reported as such wherever the tensors live."""
+    for t, n in ((ref, "q"),) + named:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor (no CPU path exists)" % n)
+        if t.device != ref.device:
+            raise ValueError("%s is on %s, expected %s" % (n, t.device, ref.device))
+
+
+def _attn_shapes(dplan, q, k, v):
+    """(F, Hq, Hkv, d) of q [F,Hq,d], k/v [F,Hkv,d], checked against the plan."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _need(t, torch.bfloat16, n, 3)
+        _need(t, torch.bfloat16, n, 3, cuda=False)
     F, Hq, d = q.shape
     Hkv = k.shape[1]
-    if F != dplan.n_fwd or k.shape != v.shape or k.shape[0] != F or k.shape[2] != d:
-        raise ValueError("shape mismatch")
+    if F != dplan.n_fwd:
+        raise ValueError("q has %d rows, the plan has %d forwarded positions" % (F, dplan.n_fwd))
+    _shape(k, (F, Hkv, d), "k")
+    _shape(v, (F, Hkv, d), "v")
+    return F, Hq, Hkv, d
+
+
+def _opts(precise, rope_base=None, o_lo=None):
+    return B.AttnOpts(B.PREC_PRECISE if precise else B.PREC_FAST, 0,
+                      0.0 if rope_base is None else float(rope_base), None if o_lo is None else o_lo.data_ptr())
+
+
+def tree_attn_fwd(dplan, q, k, v, scale=None, out=None, lse=None, dev_err=None, precise=False, o_lo=None):
+    """Forward tree attention; returns (O [F,Hq,d] bf16, LSE [Hq,F] fp32).
+
+    ``precise``: P enters the PV product as a hi + lo bf16 pair, and O's bf16
+    rounding residual is written to ``o_lo`` (allocated if None); the return
+    value is then (O, LSE, O_lo)."""
+    lib = B.load()
+    F, Hq, Hkv, d = _attn_shapes(dplan, q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((Hq, F), dtype=torch.float32, device=q.device)
-    _need(out, torch.bfloat16, "out", 3)
-    _need(lse, torch.float32, "lse", 2)
-    st = lib.tpk_tree_attn_fwd(dplan.plan.handle, _ptr(dplan.image), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
-                               _ptr(lse), Hq, Hkv, d, scale, None, 0, _ptr(dev_err), _stream())
-    B.check(st, "tpk_tree_attn_fwd")
-    return out, lse
+    _need(out, torch.bfloat16, "out", 3, cuda=False)
+    _shape(out, (F, Hq, d), "out")
+    _need(lse, torch.float32, "lse", 2, cuda=False)
+    _shape(lse, (Hq, F), "lse")
+    if precise:
+        o_lo = torch.empty_like(q) if o_lo is None else o_lo
+        _need(o_lo, torch.bfloat16, "o_lo", 3, cuda=False)
+        _shape(o_lo, (F, Hq, d), "o_lo")
+    if dev_err is not None:
+        _need(dev_err, torch.int32, "dev_err", cuda=False)
+    _on_device(q, (k, "k"), (v, "v"), (dplan.image, "the plan image"), (out, "out"), (lse, "lse"),
+               (o_lo if precise else None, "o_lo"), (dev_err, "dev_err"))
+    opts = _opts(precise, None, o_lo if precise else None)
+    st = lib.tpk_tree_attn_fwd_ex(dplan.plan.handle, _ptr(dplan.image), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                  _ptr(lse), Hq, Hkv, d, scale, ctypes.byref(opts), _ptr(dev_err), _stream())
+    B.check(st, "tpk_tree_attn_fwd_ex")
+    return (out, lse, o_lo) if precise else (out, lse)
 
 
 def attn_workspace_bytes(dplan, Hq, Hkv, d, backward):
@@ -253,32 +298,53 @@ def attn_workspace_bytes(dplan, Hq, Hkv, d, backward):
 
 
 def tree_attn_bwd(dplan, q, k, v, o, lse, do, scale=None, dq=None, dk=None, dv=None, workspace=None,
-                  dev_err=None, phases=(0, 1, 2)):
-    """Backward tree attention; returns (dQ, dK, dV) w.r.t. the rotated q, k and v.
+                  dev_err=None, phases=(0, 1, 2), precise=False, o_lo=None, rope_base=None):
+    """Backward tree attention; returns (dQ, dK, dV).
 
+    Gradients are w.r.t. the rotated q, k unless ``rope_base`` is given, in
+    which case the inverse RoPE at depth is applied inside the kernels and
+    dQ, dK are w.r.t. the un-rotated inputs.  ``precise`` selects the hi + lo
+    bf16 products (and uses the forward's ``o_lo`` for dO . O when given).
     ``phases`` selects the launches (0 prep, 1 dK/dV pass, 2 dQ pass); the
     default runs all three in order."""
     lib = B.load()
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
-        _need(t, torch.bfloat16, n, 3)
-    _need(lse, torch.float32, "lse", 2)
-    F, Hq, d = q.shape
-    Hkv = k.shape[1]
+    F, Hq, Hkv, d = _attn_shapes(dplan, q, k, v)
+    for t, n in ((o, "o"), (do, "do")):
+        _need(t, torch.bfloat16, n, 3, cuda=False)
+        _shape(t, (F, Hq, d), n)
+    _need(lse, torch.float32, "lse", 2, cuda=False)
+    _shape(lse, (Hq, F), "lse")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    for t, n, shp in ((dq, "dq", (F, Hq, d)), (dk, "dk", (F, Hkv, d)), (dv, "dv", (F, Hkv, d))):
+        _need(t, torch.bfloat16, n, 3, cuda=False)
+        _shape(t, shp, n)
+    if o_lo is not None:
+        _need(o_lo, torch.bfloat16, "o_lo", 3, cuda=False)
+        _shape(o_lo, (F, Hq, d), "o_lo")
     need = attn_workspace_bytes(dplan, Hq, Hkv, d, True)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if ws_bytes < need:
+        raise ValueError("workspace has %d bytes, the backward needs %d" % (ws_bytes, need))
+    if dev_err is not None:
+        _need(dev_err, torch.int32, "dev_err", cuda=False)
+    _on_device(q, (k, "k"), (v, "v"), (dplan.image, "the plan image"), (o, "o"), (do, "do"), (lse, "lse"),
+               (dq, "dq"), (dk, "dk"), (dv, "dv"), (o_lo, "o_lo"), (workspace, "workspace"), (dev_err, "dev_err"))
+    opts = _opts(precise, rope_base, o_lo)
     args = (dplan.plan.handle, _ptr(dplan.image), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
-            _ptr(dq), _ptr(dk), _ptr(dv), Hq, Hkv, d, scale, _ptr(workspace), workspace.numel(), _ptr(dev_err),
-            _stream())
+            _ptr(dq), _ptr(dk), _ptr(dv), Hq, Hkv, d, scale, ctypes.byref(opts), _ptr(workspace), ws_bytes,
+            _ptr(dev_err), _stream())
     if tuple(phases) == (0, 1, 2):
-        B.check(lib.tpk_tree_attn_bwd(*args), "tpk_tree_attn_bwd")
+        B.check(lib.tpk_tree_attn_bwd_ex(B.BWD_ALL, *args), "tpk_tree_attn_bwd_ex")
     else:
         for ph in phases:
-            B.check(lib.tpk_tree_attn_bwd_phase(int(ph), *args), "tpk_tree_attn_bwd_phase")
+            B.check(lib.tpk_tree_attn_bwd_ex(int(ph), *args), "tpk_tree_attn_bwd_ex")
     return dq, dk, dv
 
 

@@ -239,6 +239,74 @@ def test_min_shared_dissolves_short_runs(seed):
             assert p["n_fwd"] == p["n_raw"] - _dup_raw(seqs)
 
 
+# Hand-counted forwarded totals for the minimum shared-segment length
+# ("Prefix Tree Packing in ART", section "The tree": a shared run shorter than
+# the minimum is not shared; the walk splits there and recurses from the same
+# start, so the children's runs include the positions above them).  Every
+# position is trained, so position p of a sequence is shared with another
+# sequence iff their tokens 0..p+1 agree (the target is part of the key).
+#
+#   P = [1, 2, 3]; X = [10..19]; Y = [20..29]   (10 tokens each)
+#   s0 = P + X + [100, 101]     s1 = P + X + [200, 201]
+#   s2 = P + Y + [300, 301]     s3 = P + Y + [400, 401]    (R = 4 * 15 = 60)
+#
+# All four agree on tokens 0..2 and split at token 3 (X[0] vs Y[0]), so the
+# run shared by all four is positions 0, 1 (position 2's key holds token 3):
+# length 2.  s0, s1 agree on tokens 0..12 and split at token 13, so they share
+# positions 2..11 (10 positions); likewise s2, s3.  Each sequence keeps
+# positions 12..14 (3) to itself: the join token X[9] / Y[9] at position 12
+# appears once per branch.
+#   m <= 2:  root 2 + two runs of 10 + 4 leaves of 3            F = 34
+#   m = 3:   the root run (2 < 3) is copied into both children, whose runs
+#            become positions 0..11 (12 >= 3, kept):  12 + 12 + 4 * 3 = 36
+#   m = 11, 12: the children's runs count their carried positions: 12 >= m,
+#            kept (counting only their own 10 positions would dissolve them
+#            at m = 11 and give 60)                               F = 36
+#   m = 13:  12 < 13, dissolved as well: nothing is shared        F = 60
+MIN_SHARED_CASE = {1: 34, 2: 34, 3: 36, 11: 36, 12: 36, 13: 60}
+
+
+def _min_shared_case():
+    P, X, Y = [1, 2, 3], list(range(10, 20)), list(range(20, 30))
+    return [np.array(P + X + [100, 101]), np.array(P + X + [200, 201]),
+            np.array(P + Y + [300, 301]), np.array(P + Y + [400, 401])]
+
+
+@pytest.mark.parametrize("m", sorted(MIN_SHARED_CASE))
+def test_min_shared_carry_down_hand_counted(m):
+    seqs = _min_shared_case()
+    p = op.plan(seqs, min_shared=m, row_capacity=1000)
+    assert p["n_raw"] == 60
+    assert p["n_fwd"] == MIN_SHARED_CASE[m]
+    _check_layout_invariants(p, seqs)
+    # the shared segments' lengths, as counted above
+    shared = sorted(seg.end - seg.start for seg in p["segments"] if not seg.is_leaf)
+    want = {34: [2, 10, 10], 36: [12, 12], 60: []}[MIN_SHARED_CASE[m]]
+    assert shared == want
+
+
+def test_min_shared_tiny_workload_hand_counted():
+    # the tiny workload: 4 sequences share 128 tokens; sequences 1 and 2 share
+    # 64 more; tails of 64..128 own tokens.  Position 127's key holds token
+    # 128, which is the first token of a tail for sequences 0, 3 and of the
+    # 64-token run for 1, 2: all four share positions 0..126 (127), sequences
+    # 1, 2 share 127..190 (64), and each sequence keeps its last
+    # tail + 1 positions (the join token repeated per branch).  Both shared
+    # runs are >= 16, so min_shared = 16 keeps them:
+    #   F = 127 + 64 + sum(tail_i + 1) = 195 + sum(tails) = R - 445.
+    import workloads
+    w = workloads.get("tiny")
+    L = [len(x) for x in w.sequences]
+    tails = [L[0] - 128, L[1] - 192, L[2] - 192, L[3] - 128]
+    assert all(64 <= t <= 128 for t in tails)
+    p = op.plan(w.sequences, group_ids=w.group_ids, min_shared=16, row_capacity=10**6)
+    assert p["n_fwd"] == 195 + sum(tails)
+    assert p["n_raw"] - p["n_fwd"] == 3 * 127 + 64
+    # min_shared = 65 drops the 64-token run (carried into the two tails)
+    p65 = op.plan(w.sequences, group_ids=w.group_ids, min_shared=65, row_capacity=10**6)
+    assert p65["n_fwd"] == 127 + sum(t + 1 for t in tails) + 2 * 64
+
+
 def _dup_raw(seqs):
     seen, extra = set(), 0
     for s in seqs:
@@ -461,6 +529,12 @@ def test_backward_rows_match_full_backward():
     dk, dv = oa.backward_rows_kv(p, rows(Q), rows(K), rows(V), rows(dO), fw, 1e4)
     assert np.allclose(dk, dK[fw], atol=1e-12)
     assert np.allclose(dv, dV[fw], atol=1e-12)
+    # the batched per-key form (queries of one sequence as one product, in
+    # chunks smaller than a sequence) gives the same gradients at every key
+    every = list(range(p["n_fwd"]))
+    dk, dv = oa.backward_keys(p, rows(Q), rows(K), rows(V), rows(dO), every, 1e4, chunk=3)
+    assert np.allclose(dk, dK, atol=1e-12)
+    assert np.allclose(dv, dV, atol=1e-12)
 
 
 def test_backward_dv_sums_to_do_per_kv_head():

@@ -281,3 +281,65 @@ def test_plan_does_not_depend_on_the_thread_count(lib, monkeypatch, name):
         assert all(np.array_equal(w0[k], wl[k]) for k in w0)
         assert all(np.array_equal(a, b) for a, b in zip(r0, r))
         assert i == i0 and d == d0
+
+
+@pytest.mark.parametrize("m", [1, 2, 3, 11, 12, 13])
+def test_min_shared_carry_down_hand_counted(lib, m):
+    """The library on the hand-counted carry-down case of the oracle pins:
+    forwarded totals 34 / 36 / 60 as derived there, and bit-exact layouts."""
+    from tests.test_oracle_pins import MIN_SHARED_CASE, _min_shared_case
+    seqs = _min_shared_case()
+    ref, got = _compare(seqs, min_shared=m, cap=1000)
+    assert got.info["n_fwd"] == MIN_SHARED_CASE[m]
+
+
+def test_shape_checks_before_any_launch(lib, monkeypatch):
+    """The torch wrappers check every tensor's shape against the plan (and
+    each other) before calling the library: a mismatched tensor would make
+    the kernels read or write outside its allocation."""
+    import types
+    import torch
+    from prefix_tree_packed_dfs_gb300 import binding as B
+    from prefix_tree_packed_dfs_gb300 import ops
+
+    class NoKernels:
+        """The real library, with its GPU entry points replaced by a trap."""
+        def __getattr__(self, name):
+            if name.startswith("tpk_tree_attn_") and name != "tpk_tree_attn_workspace_bytes":
+                raise AssertionError("%s reached despite a bad argument" % name)
+            return getattr(lib, name)
+    monkeypatch.setattr(B, "load", lambda *a, **k: NoKernels())
+    w = workloads.get("tiny_fit")
+    plan = _cpp_plan(w.sequences, min_shared=w.min_shared, cap=w.row_capacity)
+    F = plan.info["n_fwd"]
+    dp = types.SimpleNamespace(plan=plan, n_fwd=F, image=torch.empty(256, dtype=torch.uint8))
+    Hq, Hkv, d = 4, 2, 64
+    bf = dict(dtype=torch.bfloat16)
+    q, k, v = torch.zeros(F, Hq, d, **bf), torch.zeros(F, Hkv, d, **bf), torch.zeros(F, Hkv, d, **bf)
+    o, do, lse = torch.zeros(F, Hq, d, **bf), torch.zeros(F, Hq, d, **bf), torch.zeros(Hq, F)
+
+    def raises(fn, what):
+        with pytest.raises(ValueError, match=what):
+            fn()
+    # forward: rows against the plan, k/v against q, caller-supplied outputs
+    raises(lambda: ops.tree_attn_fwd(dp, q[:-1], k[:-1], v[:-1]), "forwarded positions")
+    raises(lambda: ops.tree_attn_fwd(dp, q, k, v[:, :1].contiguous()), "v must have shape")
+    raises(lambda: ops.tree_attn_fwd(dp, q, k[:, :, :32].contiguous(), v), "k must have shape")
+    raises(lambda: ops.tree_attn_fwd(dp, q, k, v, out=o[:-1]), "out must have shape")
+    raises(lambda: ops.tree_attn_fwd(dp, q, k, v, lse=lse[:-1]), "lse must have shape")
+    raises(lambda: ops.tree_attn_fwd(dp, q, k, v, precise=True, o_lo=o[:, :2].contiguous()), "o_lo must have shape")
+    # backward: o, do, lse, every caller-supplied gradient, o_lo, workspace
+    bwd = lambda **kw: ops.tree_attn_bwd(dp, kw.get("q", q), k, v, kw.get("o", o), kw.get("lse", lse),
+                                         kw.get("do", do), dq=kw.get("dq"), dk=kw.get("dk"), dv=kw.get("dv"),
+                                         o_lo=kw.get("o_lo"), workspace=kw.get("ws"))
+    raises(lambda: bwd(o=o[:-1]), "o must have shape")
+    raises(lambda: bwd(do=do[:, :1].contiguous()), "do must have shape")
+    raises(lambda: bwd(lse=lse[:1].contiguous()), "lse must have shape")
+    raises(lambda: bwd(dq=torch.zeros(F, Hkv, d, **bf)), "dq must have shape")
+    raises(lambda: bwd(dk=torch.zeros(F, Hq, d, **bf)), "dk must have shape")
+    raises(lambda: bwd(dv=torch.zeros(F + 1, Hkv, d, **bf)), "dv must have shape")
+    raises(lambda: bwd(o_lo=o[:-2]), "o_lo must have shape")
+    raises(lambda: bwd(ws=torch.empty(16, dtype=torch.uint8)), "workspace has 16 bytes")
+    # right shapes, host tensors: refused as such (there is no CPU path)
+    raises(lambda: ops.tree_attn_fwd(dp, q, k, v), "must be a CUDA tensor")
+    raises(lambda: bwd(), "must be a CUDA tensor")
