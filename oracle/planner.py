@@ -2,7 +2,8 @@
 
 TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  Plain Python with
 NumPy used only to compare token runs.  Each step follows a passage of the
-pages; the readings taken where the pages are silent are listed in the design doc.
+pages; where the pages are silent, the reading taken is stated at the step
+it affects.
 
 Steps and the passages they follow
 ----------------------------------

@@ -55,7 +55,12 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
 
 // One warp per forwarded row; each lane owns 16-byte chunks (8 bf16) of the
 // row and adds the raw rows in ascending raw order, starting from the first
-// (a position with one raw token is copied bit for bit).
+// (a position with one raw token is copied bit for bit).  A lane takes kU
+// chunks 32 apart at a time and issues their loads together, so each warp
+// keeps kU * 512 bytes in flight per raw row: with one load per lane the
+// resident warps held too few bytes in flight to cover HBM latency.
+constexpr int kU = 4;
+
 __global__ void __launch_bounds__(kThreads) sum_rows_kernel(const int32_t* __restrict__ begin,
                                                             const int32_t* __restrict__ raw, int64_t F,
                                                             const uint4* __restrict__ src, uint4* __restrict__ dst,
@@ -64,23 +69,42 @@ __global__ void __launch_bounds__(kThreads) sum_rows_kernel(const int32_t* __res
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
   for (int64_t f = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5); f < F; f += warps) {
     const int b = __ldg(begin + f), e = __ldg(begin + f + 1);
-    const int64_t r0 = __ldg(raw + b);
-    for (int c = lane; c < vpr; c += 32) {
-      const uint4 first = __ldg(src + r0 * vpr + c);
+    const uint4* s0 = src + static_cast<int64_t>(__ldg(raw + b)) * vpr;
+    uint4* d = dst + f * vpr;
+    for (int c0 = lane; c0 < vpr; c0 += 32 * kU) {
+      uint4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (c0 + 32 * u < vpr) v[u] = __ldg(s0 + c0 + 32 * u);
       if (e - b == 1) {
-        dst[f * vpr + c] = first;
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+          if (c0 + 32 * u < vpr) d[c0 + 32 * u] = v[u];
         continue;
       }
-      float acc[8];
-      const uint32_t w[4] = {first.x, first.y, first.z, first.w};
+      float acc[kU][8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        acc[2 * j] = __uint_as_float(w[j] << 16);
-        acc[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      for (int u = 0; u < kU; ++u) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[u][2 * j] = __uint_as_float(w[j] << 16);
+          acc[u][2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
       }
-      for (int k = b + 1; k < e; ++k) add_bf16x8(acc, __ldg(src + static_cast<int64_t>(__ldg(raw + k)) * vpr + c));
-      dst[f * vpr + c] = make_uint4(bf16x2_bits(acc[0], acc[1]), bf16x2_bits(acc[2], acc[3]),
-                                    bf16x2_bits(acc[4], acc[5]), bf16x2_bits(acc[6], acc[7]));
+      for (int k = b + 1; k < e; ++k) {
+        const uint4* sk = src + static_cast<int64_t>(__ldg(raw + k)) * vpr;
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+          if (c0 + 32 * u < vpr) v[u] = __ldg(sk + c0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) add_bf16x8(acc[u], v[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (c0 + 32 * u < vpr)
+          d[c0 + 32 * u] = make_uint4(bf16x2_bits(acc[u][0], acc[u][1]), bf16x2_bits(acc[u][2], acc[u][3]),
+                                      bf16x2_bits(acc[u][4], acc[u][5]), bf16x2_bits(acc[u][6], acc[u][7]));
     }
   }
 }
