@@ -318,8 +318,10 @@ def plan(sequences, trained=None, group_ids=None, min_shared=64,
     row_offsets = [0]
     order_key = cmp_to_key(lambda a, b: compare_symbol_sequences(symbols[a.representative],
                                                                  symbols[b.representative]))
+    instances = []                       # (first position, length, parent instance) in placement order
     for r, row in enumerate(rows):
         placed = {}                      # segment id -> forwarded index of its first position
+        placed_inst = {}                 # segment id -> its instance (the segment placed in this row)
         for leaf in sorted(row.leaves, key=order_key):
             rep = seqs[leaf.representative]
             prev_seg = -1
@@ -328,6 +330,8 @@ def plan(sequences, trained=None, group_ids=None, min_shared=64,
                 if seg_id not in placed:
                     f0 = len(depth)
                     placed[seg_id] = f0
+                    placed_inst[seg_id] = len(instances)
+                    instances.append((f0, seg.end - seg.start, placed_inst[prev_seg] if prev_seg >= 0 else -1))
                     depth.extend(range(seg.start, seg.end))
                     fwd_token.extend(int(t) for t in rep[seg.start:seg.end])
                     if prev_seg >= 0:
@@ -357,6 +361,7 @@ def plan(sequences, trained=None, group_ids=None, min_shared=64,
             subtree_end[parent[f]] = subtree_end[f]
     depth = np.asarray(depth, dtype=np.int64)
     rows_arr = np.asarray(row_offsets, dtype=np.int64)
+    seg_levels = segment_levels(instances)
     forks = sum(1 for s in segments if len(s.children) >= 2)
     return {
         "row_offsets": rows_arr,
@@ -379,6 +384,39 @@ def plan(sequences, trained=None, group_ids=None, min_shared=64,
         "useful_pairs": int(np.sum(depth + 1)),
         "segments": segments,
         "leaves": leaves,
+        **seg_levels,
+    }
+
+
+def segment_levels(instances):
+    """Segment instances (a segment placed in one row) grouped by tree level,
+    the order in which a recurrent layer threads its state through the tree
+    ("Prefix Tree Packing in ART", section "Token-mixing layers": the GDN
+    planner walks the tree depth by depth, every segment of a depth across
+    all rows in one pass; a child starts from its parent's final state, a
+    root from zero).  ``instances``: (first position, length, parent
+    instance or -1) in placement order, parents before children.  Level = the
+    number of ancestor instances; within a level, placement order.  Returns
+    level_begin [n_levels+1] and seg_start / seg_len / seg_parent [n] in that
+    order, parents given as indices into it."""
+    n = len(instances)
+    level = [0] * n
+    for i, (_, _, par) in enumerate(instances):
+        level[i] = 0 if par < 0 else level[par] + 1
+    order = sorted(range(n), key=lambda i: (level[i], i))
+    new_index = {old: new for new, old in enumerate(order)}
+    n_levels = (max(level) + 1) if n else 0
+    begin = [0] * (n_levels + 1)
+    for lv in level:
+        begin[lv + 1] += 1
+    for lv in range(n_levels):
+        begin[lv + 1] += begin[lv]
+    return {
+        "seg_level_begin": np.asarray(begin, dtype=np.int64),
+        "seg_start": np.asarray([instances[i][0] for i in order], dtype=np.int64),
+        "seg_len": np.asarray([instances[i][1] for i in order], dtype=np.int64),
+        "seg_parent": np.asarray([new_index[instances[i][2]] if instances[i][2] >= 0 else -1 for i in order],
+                                 dtype=np.int64),
     }
 
 
