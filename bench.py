@@ -58,19 +58,24 @@ TRAFFIC = {"digest": "7e8b7c106cb59e452654d87cee8512d830ae7f78db7a41e19f06576c7b
            "fwd": 174837319424, "bwd_dkdv": 476082206464, "bwd_dq": 270328367616}
 
 
+# the sources that decide the recorded kernels' memory traffic: the attention
+# kernels, the device headers they include, and the planner that orders their
+# work (csrc/planner.*, plan_handle.h)
+TRAFFIC_SOURCES = ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "common.cuh", "planner.cpp", "planner.h",
+                   "plan_handle.h")
+
+
 def source_digest():
-    """sha256 over the sources that decide the kernels' memory traffic -- the
-    device code (csrc/*.cu, *.cuh) and the planner that orders their work
-    (csrc/planner.*, plan_handle.h) -- in name order, with comments and
-    whitespace removed: edits to comments, or to host-side API code, leave
-    it alone."""
+    """sha256 over TRAFFIC_SOURCES, in name order, with comments and
+    whitespace removed: edits to comments, to host-side API code or to other
+    kernels leave it alone."""
     import hashlib
     import re
     h = hashlib.sha256()
     dirs = [os.path.join(ROOT, "prefix_tree_packed_dfs_gb300", "csrc")]
     for d in dirs:
         for name in sorted(os.listdir(d)):
-            if name.endswith((".cu", ".cuh")) or name in ("planner.cpp", "planner.h", "plan_handle.h"):
+            if name in TRAFFIC_SOURCES:
                 with open(os.path.join(d, name)) as f:
                     code = f.read()
                 code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
@@ -101,6 +106,8 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-precise", action="store_true", help="skip the precise-mode step")
     ap.add_argument("--no-configs", action="store_true", help="skip the forward on the other workloads")
+    ap.add_argument("--no-gdn", action="store_true", help="skip the GDN tree path sub-bench")
+    ap.add_argument("--gdn", action="store_true", help="the GDN tree path alone on --workload; one line")
     ap.add_argument("--planner", action="store_true",
                     help="host planner of the library vs the oracle's planner on every workload (no GPU)")
     ap.add_argument("--layout", action="store_true",
@@ -358,6 +365,71 @@ def run_configs(peaks, local, warmup):
                     "of >= 10 launches and >= 0.5 s; frac against the burst bf16 peak (%s); "
                     "sweep_<rho>_seqpack = the same raw tokens without sharing" % peaks["source"],
             "peak_tflops": peaks["bf16_tflops"], "workloads": out}
+
+
+GDN_WORKLOADS = ("grpo", "deep")
+GDN_SHAPE = {"H": 16, "dk": 128, "dv": 128, "W": 4}
+
+
+def fp32_peak_tflops(sm_mhz=None):
+    """Dense fp32 FMA peak of this GPU: SMs x 128 fp32 lanes x 2 FLOP per FMA
+    x the SM clock (the maximum clock unless one is given)."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    mhz = sm_mhz or 2070.0
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, sms
+
+
+def run_gdn(peaks, local, warmup, names=GDN_WORKLOADS):
+    """The GDN tree path (causal conv + gated delta rule, H 16, dk = dv 128,
+    conv width 4) on the tree batches: each call timed alone with L2 flushed
+    before it, median, with its own clock sample."""
+    import torch
+    import workloads
+    from prefix_tree_packed_dfs_gb300 import ops
+    from workloads import rng as wrng
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    H, dk, dv, W = GDN_SHAPE["H"], GDN_SHAPE["dk"], GDN_SHAPE["dv"], GDN_SHAPE["W"]
+    C = H * (2 * dk + dv)
+    out = {}
+    for name in names:
+        w = workloads.get(name)
+        plan = ops.Plan.from_sequences(w.sequences, group_ids=w.group_ids, row_capacity=w.row_capacity,
+                                       min_shared=w.min_shared)
+        dp = plan.to_device()
+        info = plan.info
+        F = info["n_fwd"]
+        x, wc, g, b = wrng.gdn_inputs(w.seed_base + 50, F, C, H, W, "cuda")
+        y = torch.empty_like(x)
+        o = torch.empty((F, H, dv), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(max(int(ops.B.load().tpk_gdn_workspace_bytes(plan.handle, H, dk, dv)), 256),
+                         dtype=torch.uint8, device="cuda")
+        q, k, v = (y[:, :H * dk].unflatten(1, (H, dk)), y[:, H * dk:2 * H * dk].unflatten(1, (H, dk)),
+                   y[:, 2 * H * dk:].unflatten(1, (H, dv)))
+        clocks = Clocks(local)
+        torch.cuda.synchronize()
+        clocks.start()
+        ms_conv, n_conv = _time_launches(lambda: ops.gdn_conv(dp, x, wc, y=y), flush, min_s=0.3, warmup=warmup)
+        ms_delta, n_delta = _time_launches(lambda: ops.gdn_delta_rule(dp, q, k, v, g, b, out=o, workspace=ws),
+                                           flush, min_s=0.5, min_n=5, warmup=warmup)
+        clk = clocks.stop()
+        conv_bytes = 2 * F * C * 2 + 4 * F + 4 * C * W          # x read, y written, parent, weights
+        delta_flop = 6.0 * dk * dv * F * H                      # S k, the update, S q per token and head
+        peak32, sms = fp32_peak_tflops(clk.get("sm_mhz"))
+        out[name] = {"forwarded_tokens": F, "raw_tokens": info["n_raw"], "segment_instances": info["n_seg_instances"],
+                     "levels": info["n_seg_levels"], "conv_ms": ms_conv, "conv_gbs": conv_bytes / ms_conv / 1e6,
+                     "conv_frac_of_copy_peak": conv_bytes / ms_conv / 1e6 / peaks["hbm_gbs"],
+                     "delta_ms": ms_delta, "delta_tflops": delta_flop / ms_delta / 1e9,
+                     "delta_frac_of_fp32_peak": delta_flop / ms_delta / 1e9 / peak32,
+                     "fp32_peak_tflops": peak32, "forwarded_tokens_per_s": F / (ms_conv + ms_delta) * 1e3,
+                     "raw_tokens_per_s": info["n_raw"] / (ms_conv + ms_delta) * 1e3,
+                     "launches_timed": [n_conv, n_delta], "clocks": clk}
+        del x, y, o, ws, q, k, v, dp, plan
+        torch.cuda.empty_cache()
+    return {"what": "GDN tree path, H %d, dk = dv = %d, conv width %d: conv (one launch, HBM-bound: against the "
+                    "copy peak) and gated delta rule (one launch per tree level, fp32 state: against the fp32 FMA "
+                    "peak = SMs x 128 lanes x 2 x the median SM clock); L2 flushed before every timed call"
+                    % (H, dk, W), "workloads": out}
 
 
 def run_ours(a):
@@ -666,11 +738,14 @@ def run_ours(a):
                       amt / t_s / (1e12 if b == "tensor" else 1e9)}
 
     # ---- forward on the other workloads (after the deep tree's buffers go) --
-    configs = None
-    if not a.no_configs and rank == 0:
+    configs = gdn = None
+    if (not a.no_configs or not a.no_gdn) and rank == 0:
         del Q, K, V, dO_raw, dO, O, LSE, O_raw, LSE_raw, dq, dk, dv, ws
         torch.cuda.empty_cache()
+    if not a.no_configs and rank == 0:
         configs = run_configs(peaks, local, a.warmup)
+    if not a.no_gdn and rank == 0:
+        gdn = run_gdn(peaks, local, max(1, min(a.warmup, 3)))
 
     useful_tflops = (fwd_flop + bwd_flop) / (ms / 1e3) / 1e12
     out = {
@@ -697,6 +772,7 @@ def run_ours(a):
         "e2e": e2e,
         "precise": precise,
         "configs": configs,
+        "gdn": gdn,
         "gpu_launches": LAUNCHES_PER_STEP * a.steps,
         "clocks": clk,
     }
@@ -888,6 +964,9 @@ def main():
         run_sweep(a)
     elif a.layout:
         run_layout(a)
+    elif a.gdn:
+        import torch
+        print(json.dumps({"mode": "gdn", **run_gdn(_peaks(), 0, max(a.warmup, 1), names=(a.workload,))}), flush=True)
     elif a.impl == "reference":
         run_reference(a)
     else:

@@ -102,6 +102,8 @@ typedef struct {
     double packing_ratio;  /* R / F ([TRL] "How tree packing works") */
     double row_fill_frac;  /* F / (n_rows * row_capacity) */
     double fork_frac;      /* segments with >= 2 children / segments */
+    int64_t n_seg_instances; /* segment instances (a segment placed in one row), see tpk_plan_segments */
+    int64_t n_seg_levels;    /* tree levels of the segment instances */
 } tpk_plan_info;
 
 /* ---- planner (host only, no GPU needed) --------------------------------- */
@@ -182,6 +184,20 @@ int tpk_plan_worklists(const tpk_plan* plan, int32_t* qt_q0, int32_t* qt_nq,
  * tpk_gather_to_forwarded and tpk_sum_to_forwarded. */
 int tpk_plan_raw_of_forwarded(const tpk_plan* plan, int32_t* fwd_raw_begin, int32_t* fwd_raw);
 
+/* Segment instances by tree level ([ART] "Token-mixing layers", GDN: a
+ * recurrent layer threads its state through the tree one depth at a time --
+ * every segment of a depth, across all rows, in one pass -- and a child
+ * starts from its parent's final state, a root from zero).  An instance is a
+ * segment placed in one row: a chain of forwarded positions [seg_start,
+ * seg_start + seg_len).  Instances are ordered by level (the number of
+ * ancestor instances), then by placement; level l is [level_begin[l],
+ * level_begin[l+1]) (n_seg_levels + 1 entries); seg_parent is the parent's
+ * index in this order, -1 at a root.  Host int32 copies, any pointer may be
+ * NULL; sizes from tpk_plan_info (n_seg_instances, n_seg_levels).  The
+ * device image holds seg_start, seg_len, seg_parent (TPK_FIELD_SEG_*). */
+int tpk_plan_segments(const tpk_plan* plan, int32_t* level_begin, int32_t* seg_start, int32_t* seg_len,
+                      int32_t* seg_parent);
+
 /* Rows across ranks (no counterpart on the pages, which run one GPU per
  * row batch): the mask never crosses a row ("Prefix Tree Packing in ART",
  * section "Token-mixing layers": a token sees only its own root-to-leaf
@@ -218,6 +234,9 @@ int tpk_plan_shard_rows(const tpk_plan* plan, int32_t world, int32_t* rank_of_ro
 #define TPK_FIELD_PARENT       3   /* int32 [F] */
 #define TPK_FIELD_FWD_RAW_BEGIN 4  /* int32 [F+1] */
 #define TPK_FIELD_FWD_RAW      5   /* int32 [R] */
+#define TPK_FIELD_SEG_START    6   /* int32 [n_seg_instances], level order (tpk_plan_segments) */
+#define TPK_FIELD_SEG_LEN      7   /* int32 [n_seg_instances] */
+#define TPK_FIELD_SEG_PARENT   8   /* int32 [n_seg_instances] */
 size_t tpk_plan_device_bytes(const tpk_plan* plan);
 int tpk_plan_field_offset(const tpk_plan* plan, int32_t field, size_t* offset);
 int tpk_plan_upload(const tpk_plan* plan, void* dev_image, void* stream);
@@ -425,6 +444,50 @@ int tpk_gather_to_forwarded(const int32_t* fwd_raw_begin, const int32_t* fwd_raw
 int tpk_sum_to_forwarded(const int32_t* fwd_raw_begin, const int32_t* fwd_raw, int64_t F, int64_t R,
                          const void* src, void* dst, const float* lse_src, float* lse_dst,
                          int32_t H, int32_t d, void* stream);
+
+/* ---- GDN (Gated DeltaNet) token mixing over the tree ---------------------
+ * [ART] "Token-mixing layers": GDN is recurrent -- a running state threaded
+ * token by token along each root-to-leaf path, forked once per branch point,
+ * reset at every tree root -- and runs as a short causal convolution followed
+ * by the gated delta rule.  The pages name the layer without defining it; the
+ * library computes the published Gated DeltaNet layer, below. */
+
+/* Causal depthwise convolution + SiLU along every position's own path:
+ *   y[f, c] = silu( sum_{j<W} w[c, j] * x[a_{W-1-j}(f), c] ),
+ * a_0(f) = f, a_{t+1}(f) = parent(a_t(f)); taps above a root read 0.  One
+ * launch covers the whole packed batch (each position gathers its window
+ * through the plan's parent array).
+ *   x, y  [F, C] bf16 device, 16-byte aligned rows; C % 8 == 0
+ *   w     [C, W] fp32 device, 16-byte aligned; 1 <= W <= 8
+ * Errors: TPK_E_ARG on a NULL pointer, a bad C / W or misalignment. */
+int tpk_gdn_conv(const tpk_plan* plan, const void* dev_image, const void* x, const float* w, void* y,
+                 int32_t C, int32_t W, void* stream);
+
+/* Workspace of tpk_gdn_delta_rule: one fp32 dv x dk state per segment
+ * instance and head (n_seg_instances * H * dk * dv * 4 bytes, rounded up to
+ * 256). */
+size_t tpk_gdn_workspace_bytes(const tpk_plan* plan, int32_t H, int32_t dk, int32_t dv);
+
+/* The gated delta rule along every root-to-leaf path, per head h:
+ *   k~ = k / |k|,  q~ = q / |q|   (L2 over dk; k and q must be nonzero)
+ *   S_t = exp(g_t) S_{t-1} (I - beta_t k~_t k~_t^T) + beta_t v_t k~_t^T,  S = 0 at a root
+ *   o_t = S_t (scale q~_t)
+ * S is dv x dk, kept in fp32.  The segment instances of the plan run level by
+ * level (tpk_plan_segments), one launch per level and one CTA per (instance,
+ * head): a chain starts from its parent's final state, stored in the
+ * workspace, so the state is forked at every branch point.
+ *   q, k   [F, H, dk] bf16 with row stride ld_qk elements (may be column
+ *          slices of one [F, ld] tensor, e.g. the convolution's output)
+ *   v      [F, H, dv] bf16 with row stride ld_v
+ *   g, beta [F, H] fp32: log decay (<= 0) and write strength
+ *   o      [F, H, dv] bf16 (contiguous)
+ *   (dk, dv) in {(64, 64), (128, 128)}; scale > 0 (usually 1/sqrt(dk))
+ *   workspace: >= tpk_gdn_workspace_bytes bytes, 256-byte aligned; need not be
+ *   cleared.
+ * Pointers and strides must give 16-byte aligned rows (TPK_E_ARG). */
+int tpk_gdn_delta_rule(const tpk_plan* plan, const void* dev_image, const void* q, const void* k, const void* v,
+                       int64_t ld_qk, int64_t ld_v, const float* g, const float* beta, void* o, int32_t H,
+                       int32_t dk, int32_t dv, float scale, void* workspace, size_t ws_bytes, void* stream);
 
 /* Self-test of the device-side failure path (no counterpart on the pages):
  * launches one small kernel that waits, with the same bounded mbarrier wait

@@ -22,15 +22,17 @@ PLACE_NEXT_FIT = 1
 PLACE_GROUPS = 2
 FIELD_DEPTH, FIELD_TOKEN_INDEX, FIELD_SUBTREE_END, FIELD_PARENT = 0, 1, 2, 3
 FIELD_FWD_RAW_BEGIN, FIELD_FWD_RAW = 4, 5
+FIELD_SEG_START, FIELD_SEG_LEN, FIELD_SEG_PARENT = 6, 7, 8
 
 # every symbol include/tpk.h declares
 EXPORTS = [
     "tpk_plan_build", "tpk_plan_info_get", "tpk_plan_export", "tpk_plan_worklists", "tpk_plan_raw_of_forwarded",
-    "tpk_plan_shard_rows",
+    "tpk_plan_shard_rows", "tpk_plan_segments",
     "tpk_plan_device_bytes", "tpk_plan_field_offset", "tpk_plan_upload", "tpk_plan_destroy",
     "tpk_rope_by_depth", "tpk_attn_workspace_bytes", "tpk_tree_attn_fwd", "tpk_tree_attn_fwd_ex",
     "tpk_tree_attn_bwd", "tpk_tree_attn_bwd_ex", "tpk_tree_attn_bwd_phase", "tpk_tree_attn_bwd_noalloc", "tpk_selftest_wait_timeout",
-    "tpk_scatter_token_index", "tpk_gather_to_forwarded", "tpk_sum_to_forwarded", "tpk_status_string",
+    "tpk_scatter_token_index", "tpk_gather_to_forwarded", "tpk_sum_to_forwarded", "tpk_gdn_conv",
+    "tpk_gdn_workspace_bytes", "tpk_gdn_delta_rule", "tpk_status_string",
     "tpk_version",
 ]
 
@@ -55,7 +57,8 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "n_seqs", "n_rows", "n_fwd", "n_raw", "n_segments", "n_leaves", "n_qtiles", "n_kblocks",
         "n_ktiles", "n_qblocks", "useful_pairs", "visited_pairs", "max_depth")] + \
-        [(n, ctypes.c_double) for n in ("packing_ratio", "row_fill_frac", "fork_frac")]
+        [(n, ctypes.c_double) for n in ("packing_ratio", "row_fill_frac", "fork_frac")] + \
+        [(n, ctypes.c_int64) for n in ("n_seg_instances", "n_seg_levels")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -77,6 +80,7 @@ def _sig(lib):
     lib.tpk_plan_device_bytes.argtypes = [P]
     lib.tpk_plan_device_bytes.restype = SZ
     lib.tpk_plan_shard_rows.argtypes = [P, I32, P, P]
+    lib.tpk_plan_segments.argtypes = [P, P, P, P, P]
     lib.tpk_plan_field_offset.argtypes = [P, I32, ctypes.POINTER(SZ)]
     lib.tpk_plan_upload.argtypes = [P, P, P]
     lib.tpk_plan_destroy.argtypes = [P]
@@ -96,6 +100,10 @@ def _sig(lib):
     lib.tpk_scatter_token_index.argtypes = [P, I64, I64, P, P, P, P, I32, I32, P]
     lib.tpk_gather_to_forwarded.argtypes = [P, P, I64, I64, P, P, I64, P]
     lib.tpk_sum_to_forwarded.argtypes = [P, P, I64, I64, P, P, P, P, I32, I32, P]
+    lib.tpk_gdn_conv.argtypes = [P, P, P, P, P, I32, I32, P]
+    lib.tpk_gdn_workspace_bytes.argtypes = [P, I32, I32, I32]
+    lib.tpk_gdn_workspace_bytes.restype = SZ
+    lib.tpk_gdn_delta_rule.argtypes = [P, P, P, P, P, I64, I64, P, P, P, I32, I32, I32, ctypes.c_float, P, SZ, P]
     lib.tpk_status_string.argtypes = [ctypes.c_int]
     lib.tpk_status_string.restype = ctypes.c_char_p
     lib.tpk_version.argtypes = []

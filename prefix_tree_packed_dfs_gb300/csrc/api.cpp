@@ -135,6 +135,8 @@ int tpk_plan_info_get(const tpk_plan* plan, tpk_plan_info* out) {
   out->packing_ratio = P.packing_ratio;
   out->row_fill_frac = P.row_fill_frac;
   out->fork_frac = P.fork_frac;
+  out->n_seg_instances = static_cast<int64_t>(P.seg_start.size());
+  out->n_seg_levels = P.seg_level_begin.empty() ? 0 : static_cast<int64_t>(P.seg_level_begin.size()) - 1;
   return TPK_OK;
 }
 
@@ -182,6 +184,16 @@ int tpk_plan_raw_of_forwarded(const tpk_plan* plan, int32_t* fwd_raw_begin, int3
   return TPK_OK;
 }
 
+int tpk_plan_segments(const tpk_plan* plan, int32_t* level_begin, int32_t* seg_start, int32_t* seg_len,
+                      int32_t* seg_parent) {
+  if (!plan) return TPK_E_ARG;
+  copy_out(level_begin, plan->p.seg_level_begin);
+  copy_out(seg_start, plan->p.seg_start);
+  copy_out(seg_len, plan->p.seg_len);
+  copy_out(seg_parent, plan->p.seg_parent);
+  return TPK_OK;
+}
+
 int tpk_plan_shard_rows(const tpk_plan* plan, int32_t world, int32_t* rank_of_row, int64_t* rank_pairs) {
   if (!plan || world <= 0 || !rank_of_row) return TPK_E_ARG;
   const tpk::Plan& P = plan->p;
@@ -218,6 +230,9 @@ int tpk_plan_field_offset(const tpk_plan* plan, int32_t field, size_t* offset) {
     case TPK_FIELD_PARENT: *offset = plan->p.off_parent; return TPK_OK;
     case TPK_FIELD_FWD_RAW_BEGIN: *offset = plan->p.off_fwd_raw_begin; return TPK_OK;
     case TPK_FIELD_FWD_RAW: *offset = plan->p.off_fwd_raw; return TPK_OK;
+    case TPK_FIELD_SEG_START: *offset = plan->p.off_seg_start; return TPK_OK;
+    case TPK_FIELD_SEG_LEN: *offset = plan->p.off_seg_len; return TPK_OK;
+    case TPK_FIELD_SEG_PARENT: *offset = plan->p.off_seg_parent; return TPK_OK;
     default: return TPK_E_ARG;
   }
 }

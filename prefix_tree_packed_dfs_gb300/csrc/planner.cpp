@@ -432,6 +432,34 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
       if (p >= 0 && P.subtree_end[f] > P.subtree_end[p]) P.subtree_end[p] = P.subtree_end[f];
     }
   });
+  // segment instances by tree level: the order in which a recurrent token
+  // mixer threads its state through the tree ([ART] "Token-mixing layers",
+  // GDN: one pass per tree depth, a child starting from its parent's final
+  // state).  Level = number of ancestor instances (parents come first in
+  // placement order); stable in placement order within a level.
+  {
+    const size_t ni = inst_start.size();
+    std::vector<int32_t> level(ni);
+    int32_t n_levels = 0;
+    for (size_t i = 0; i < ni; ++i) {
+      level[i] = inst_parent[i] < 0 ? 0 : level[static_cast<size_t>(inst_parent[i])] + 1;
+      n_levels = std::max(n_levels, level[i] + 1);
+    }
+    P.seg_level_begin.assign(static_cast<size_t>(n_levels) + 1, 0);
+    for (size_t i = 0; i < ni; ++i) ++P.seg_level_begin[static_cast<size_t>(level[i]) + 1];
+    for (int32_t l = 0; l < n_levels; ++l) P.seg_level_begin[l + 1] += P.seg_level_begin[l];
+    std::vector<int32_t> at(P.seg_level_begin.begin(), P.seg_level_begin.end() - 1), pos(ni);
+    for (size_t i = 0; i < ni; ++i) pos[i] = at[static_cast<size_t>(level[i])]++;
+    P.seg_start.resize(ni);
+    P.seg_len.resize(ni);
+    P.seg_parent.resize(ni);
+    for (size_t i = 0; i < ni; ++i) {
+      const size_t k = static_cast<size_t>(pos[i]);
+      P.seg_start[k] = inst_start[i];
+      P.seg_len[k] = inst_len[i];
+      P.seg_parent[k] = inst_parent[i] < 0 ? -1 : pos[static_cast<size_t>(inst_parent[i])];
+    }
+  }
   int64_t forks = 0;
   for (auto& s : segs) forks += (s.n_children >= 2);
   P.useful_pairs = 0;
@@ -611,6 +639,9 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   place(P.off_kt_qb_begin, 4 * P.kt_qb_begin.size());
   place(P.off_qb, 4 * P.qb.size());
   place(P.off_kt_order, 4 * P.kt_order.size());
+  place(P.off_seg_start, 4 * P.seg_start.size());
+  place(P.off_seg_len, 4 * P.seg_len.size());
+  place(P.off_seg_parent, 4 * P.seg_parent.size());
   // every byte is written once: the sections by copy, the padding after
   // each section (up to the next 256-byte boundary) with zeros; copied in
   // pieces of up to 4 MB on the host threads
@@ -641,6 +672,9 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   put(P.off_kt_qb_begin, P.kt_qb_begin);
   put(P.off_qb, P.qb);
   put(P.off_kt_order, P.kt_order);
+  put(P.off_seg_start, P.seg_start);
+  put(P.off_seg_len, P.seg_len);
+  put(P.off_seg_parent, P.seg_parent);
   parallel_for(static_cast<int64_t>(pieces.size()), [&](int64_t i) {
     const Piece& pc = pieces[static_cast<size_t>(i)];
     if (pc.bytes == 0) return;

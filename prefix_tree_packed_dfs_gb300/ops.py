@@ -118,6 +118,14 @@ class Plan:
                 "tpk_plan_raw_of_forwarded")
         return begin, raw
 
+    def segments(self):
+        """Segment instances by tree level: (level_begin [n_levels+1],
+        seg_start, seg_len, seg_parent [n_instances]), int32."""
+        n, L = self.info["n_seg_instances"], self.info["n_seg_levels"]
+        out = (np.zeros(L + 1, np.int32), np.zeros(n, np.int32), np.zeros(n, np.int32), np.zeros(n, np.int32))
+        B.check(self._lib.tpk_plan_segments(self._h, *[a.ctypes.data for a in out]), "tpk_plan_segments")
+        return out
+
     def shard_rows(self, world):
         """Whole rows to `world` data-parallel ranks, heaviest row first to the
         least-loaded rank (work = useful pairs).  Returns (rank_of_row int32
@@ -185,6 +193,10 @@ class DevicePlan:
         self.parent = self._field(B.FIELD_PARENT, F)
         self.fwd_raw_begin = self._field(B.FIELD_FWD_RAW_BEGIN, F + 1)
         self.fwd_raw = self._field(B.FIELD_FWD_RAW, R)
+        n_inst = plan.info["n_seg_instances"]
+        self.seg_start = self._field(B.FIELD_SEG_START, n_inst)
+        self.seg_len = self._field(B.FIELD_SEG_LEN, n_inst)
+        self.seg_parent = self._field(B.FIELD_SEG_PARENT, n_inst)
 
     def _field(self, field, n):
         off = self.plan.field_offset(field)
@@ -419,3 +431,64 @@ def sum_to_forwarded(dplan, src=None, lse_src=None, dst=None, lse_dst=None):
     B.check(lib.tpk_sum_to_forwarded(_ptr(dplan.fwd_raw_begin), _ptr(dplan.fwd_raw), F, R, _ptr(src), _ptr(dst),
                                      _ptr(lse_src), _ptr(lse_dst), H, d, _stream()), "tpk_sum_to_forwarded")
     return dst, lse_dst
+
+
+def gdn_conv(dplan, x, w, y=None):
+    """Causal depthwise convolution + SiLU along each position's path
+    (``tpk_gdn_conv``): x [F, C] bf16, w [C, W] fp32 -> y [F, C] bf16."""
+    lib = B.load()
+    _need(x, torch.bfloat16, "x", 2, cuda=False)
+    _need(w, torch.float32, "w", 2, cuda=False)
+    F, C = x.shape
+    if F != dplan.n_fwd:
+        raise ValueError("x has %d rows, the plan has %d forwarded positions" % (F, dplan.n_fwd))
+    if w.shape[0] != C:
+        raise ValueError("w must have shape (%d, W)" % C)
+    y = torch.empty_like(x) if y is None else y
+    _need(y, torch.bfloat16, "y", 2, cuda=False)
+    _shape(y, (F, C), "y")
+    _on_device(x, (w, "w"), (y, "y"), (dplan.image, "the plan image"))
+    B.check(lib.tpk_gdn_conv(dplan.plan.handle, _ptr(dplan.image), _ptr(x), _ptr(w), _ptr(y), C, w.shape[1],
+                             _stream()), "tpk_gdn_conv")
+    return y
+
+
+def gdn_delta_rule(dplan, q, k, v, g, beta, scale=None, out=None, workspace=None):
+    """Gated delta rule along every root-to-leaf path (``tpk_gdn_delta_rule``).
+
+    q, k [F, H, dk] and v [F, H, dv] bf16 -- views whose rows may be strided
+    (e.g. column slices of the convolution's output), unit stride inside a
+    row; g (log decay), beta [F, H] fp32.  Returns o [F, H, dv] bf16."""
+    lib = B.load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.dim() != 3:
+            raise TypeError("%s must be a 3-d bf16 tensor" % n)
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError("%s: heads and elements must be contiguous inside a row" % n)
+    F, H, dk = q.shape
+    dv = v.shape[2]
+    if F != dplan.n_fwd:
+        raise ValueError("q has %d rows, the plan has %d forwarded positions" % (F, dplan.n_fwd))
+    _shape(k, (F, H, dk), "k")
+    _shape(v, (F, H, dv), "v")
+    if q.stride(0) != k.stride(0):
+        raise ValueError("q and k must share one row stride")
+    for t, n in ((g, "g"), (beta, "beta")):
+        _need(t, torch.float32, n, 2, cuda=False)
+        _shape(t, (F, H), n)
+    scale = 1.0 / math.sqrt(dk) if scale is None else float(scale)
+    out = torch.empty((F, H, dv), dtype=torch.bfloat16, device=q.device) if out is None else out
+    _need(out, torch.bfloat16, "out", 3, cuda=False)
+    _shape(out, (F, H, dv), "out")
+    need = int(lib.tpk_gdn_workspace_bytes(dplan.plan.handle, H, dk, dv))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if ws_bytes < need:
+        raise ValueError("workspace has %d bytes, the delta rule needs %d" % (ws_bytes, need))
+    _on_device(q, (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (out, "out"), (workspace, "workspace"),
+               (dplan.image, "the plan image"))
+    B.check(lib.tpk_gdn_delta_rule(dplan.plan.handle, _ptr(dplan.image), _ptr(q), _ptr(k), _ptr(v), q.stride(0),
+                                   v.stride(0), _ptr(g), _ptr(beta), _ptr(out), H, dk, dv, scale, _ptr(workspace),
+                                   ws_bytes, _stream()), "tpk_gdn_delta_rule")
+    return out

@@ -37,7 +37,7 @@ def test_binding_export_list_matches_header():
 
 
 def test_status_strings(lib):
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         assert lib.tpk_status_string(code)
     assert b"sm_103a" in lib.tpk_version()
 

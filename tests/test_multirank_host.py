@@ -70,11 +70,16 @@ def test_source_digest_ignores_comments(tmp_path, monkeypatch):
     shutil.copytree(os.path.join(bench.ROOT, "include"), root / "include")
     monkeypatch.setattr(bench, "ROOT", str(root))
     d0 = bench.source_digest()
-    f = root / "prefix_tree_packed_dfs_gb300" / "csrc" / "scatter.cu"
+    f = root / "prefix_tree_packed_dfs_gb300" / "csrc" / "attn_bwd.cu"
     f.write_text("// a new comment line\n" + f.read_text().replace("{", "{ /* inline */", 1))
     assert bench.source_digest() == d0
-    f.write_text(f.read_text().replace("kThreads = 256", "kThreads = 128"))
+    f.write_text(f.read_text().replace("constexpr int kStat = 4;", "constexpr int kStat = 3;"))
     assert bench.source_digest() != d0
+    # other kernels do not change what the attention kernels move
+    d2 = bench.source_digest()
+    g = root / "prefix_tree_packed_dfs_gb300" / "csrc" / "scatter.cu"
+    g.write_text(g.read_text().replace("kThreads = 256", "kThreads = 128"))
+    assert bench.source_digest() == d2
     # host-side API code does not change what the kernels move
     d1 = bench.source_digest()
     api = root / "prefix_tree_packed_dfs_gb300" / "csrc" / "api.cpp"

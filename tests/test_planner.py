@@ -34,6 +34,10 @@ def _compare(seqs, trained=None, groups=None, min_shared=64, cap=65536, placemen
     assert info["packing_ratio"] == ref["packing_ratio"]
     assert info["row_fill_frac"] == ref["row_fill_frac"]
     assert info["fork_frac"] == ref["fork_frac"]
+    # segment instances by tree level (the recurrent layers' schedule)
+    lb, start, length, par = got.segments()
+    for mine, key in ((lb, "seg_level_begin"), (start, "seg_start"), (length, "seg_len"), (par, "seg_parent")):
+        assert np.array_equal(np.asarray(mine, np.int64), np.asarray(ref[key], np.int64)), key
     return ref, got
 
 

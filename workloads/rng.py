@@ -82,3 +82,26 @@ def rows_bf16(seed, rows, row_elems):
     rows = torch.as_tensor(rows, dtype=torch.int64)
     idx = rows[:, None] * row_elems + torch.arange(row_elems, dtype=torch.int64)[None, :]
     return normal_bf16_at(seed, idx)
+
+
+def gdn_inputs(seed, F, C, H, W, device="cpu"):
+    """Synthetic inputs of the GDN token mixer on F forwarded positions:
+    x [F, C] bf16 (the q|k|v projections, N(0,1)), w [C, W] fp32 conv
+    weights (N(0,1) / W), g [F, H] fp32 log decays in (-0.5, 0] and
+    beta [F, H] fp32 write strengths in (0.05, 0.95).  g and beta are made
+    from generator values z by -0.1|z| and 0.05 + 0.9 |z| / (1 + |z|):
+    float32 operations that round correctly on every device, so the CPU and
+    the GPU get the same bits."""
+    x = normal_bf16(seed, (F, C), device)
+    w = normal_bf16(seed + 1, (C, W), device).to(torch.float32) / float(W)
+    zg = normal_bf16(seed + 2, (F, H), device).to(torch.float32).abs()
+    zb = normal_bf16(seed + 3, (F, H), device).to(torch.float32).abs()
+    return x, w, zg * -0.1, 0.05 + 0.9 * (zb / (1.0 + zb))
+
+
+def gdn_rows(seed, rows, C, H):
+    """Rows ``rows`` of gdn_inputs' x, g and beta, on the CPU (same bits)."""
+    x = rows_bf16(seed, rows, C)
+    zg = rows_bf16(seed + 2, rows, H).to(torch.float32).abs()
+    zb = rows_bf16(seed + 3, rows, H).to(torch.float32).abs()
+    return x, zg * -0.1, 0.05 + 0.9 * (zb / (1.0 + zb))
