@@ -31,6 +31,11 @@ Contents
                token_index and its transpose, the sum over a position's raw
                tokens ("TRL Tree Packing for AsyncGRPO", section "How tree
                packing works").
+``gdn``        the GDN token mixer (causal convolution + gated delta rule)
+               along every unpacked root-to-leaf sequence, its gradients by
+               fp64 autograd over the unpacked sequences, and the pages'
+               level-by-level schedule ("Prefix Tree Packing in ART", section
+               "Token-mixing layers").
 ``bf16``       round-to-nearest-even rounding of fp64 values to bfloat16.
 
 Every function is pinned by a ``-m "not gpu"`` test against values the pages

@@ -145,3 +145,144 @@ def delta_rule_tree(plan, Q, K, V, G, B, scale=None):
                 S, out[f] = _step(S, Q[f], K[f], V[f], G[f], B[f], scale)
             final[i] = S
     return out
+
+
+# ---------------------------------------------------------------- gradients
+# The packed layer is a function of the packed inputs, and its output at a
+# position f is the output of any sequence through f (they agree: a causal
+# layer sees only f's own path).  Its vector-Jacobian product with dO is
+# therefore the sum over f of the gradient of <dO[f], out(f)> taken through
+# ONE sequence containing f (the first, as ``_assign`` keeps), with that
+# sequence's inputs read out of the packed arrays -- so the gradients of a
+# shared position's inputs, and of a forked state, are summed over every
+# branch below it, as the pages have autograd do for the broadcast initial
+# state of each child ("Prefix Tree Packing in ART", section "Token-mixing
+# layers").  The per-sequence forwards below restate ``conv`` and ``_step``
+# in torch fp64 so that autograd can differentiate them; the tests pin the
+# gradients to central differences of the NumPy forwards above.
+
+def _torch():
+    import torch
+    return torch
+
+
+def _conv_seq_t(x, w):
+    """``conv`` for one sequence in torch: x [L, C], w [C, W] -> y [L, C]."""
+    torch = _torch()
+    L, C = x.shape
+    W = w.shape[1]
+    xs = torch.cat([torch.zeros((W - 1, C), dtype=x.dtype), x], dim=0)
+    acc = sum(w[:, j] * xs[j:j + L] for j in range(W))
+    return acc * torch.sigmoid(acc)
+
+
+def _delta_seq_t(q, k, v, g, b, scale):
+    """``delta_rule`` for one sequence in torch from S = 0: q, k [L, H, dk],
+    v [L, H, dv], g, b [L, H] -> o [L, H, dv]."""
+    torch = _torch()
+    k = k / torch.linalg.norm(k, dim=-1, keepdim=True)
+    q = scale * q / torch.linalg.norm(q, dim=-1, keepdim=True)
+    L, H, dk = k.shape
+    S = torch.zeros((H, v.shape[2], dk), dtype=k.dtype)
+    out = []
+    for t in range(L):
+        a = torch.exp(g[t])[:, None, None]
+        bt = b[t][:, None, None]
+        Sk = torch.einsum("hec,hc->he", S, k[t])
+        S = a * (S - bt * torch.einsum("he,hc->hec", Sk, k[t])) + bt * torch.einsum("he,hc->hec", v[t], k[t])
+        out.append(torch.einsum("hec,hc->he", S, q[t]))
+    return torch.stack(out)
+
+
+def _vjp(plan, per_pos, params, dout, fn):
+    """Gradients of sum_f <dout[f], out[f]> w.r.t. ``per_pos`` (packed arrays
+    [F, ...]) and ``params`` (shared by every position); ``fn(*rows,
+    *params)`` is one sequence's forward on its gathered rows."""
+    torch = _torch()
+    dout = np.asarray(dout, dtype=np.float64)
+    leaves = [torch.tensor(np.asarray(a, dtype=np.float64), requires_grad=True) for a in per_pos]
+    pleaves = [torch.tensor(np.asarray(a, dtype=np.float64), requires_grad=True) for a in params]
+    dO = torch.tensor(dout)
+    seen = np.zeros(plan["n_fwd"], dtype=bool)
+    loss = torch.zeros((), dtype=torch.float64)
+    for path in _paths(plan):
+        own = np.nonzero(~seen[path])[0]
+        seen[path] = True
+        if len(own) == 0:
+            continue
+        pt = torch.as_tensor(np.asarray(path, dtype=np.int64))
+        out = fn(*[l[pt] for l in leaves], *pleaves)
+        loss = loss + (out[torch.as_tensor(own)] * dO[torch.as_tensor(np.asarray(path[own], dtype=np.int64))]).sum()
+    loss.backward()
+    return [np.zeros(l.shape) if l.grad is None else l.grad.numpy() for l in leaves + pleaves]
+
+
+def conv_bwd(plan, X, w, dY):
+    """Gradients of ``conv``: returns (dX [F, C], dw [C, W]) for the output
+    gradient dY [F, C]."""
+    dX, dw = _vjp(plan, [X], [w], dY, _conv_seq_t)
+    return dX, dw
+
+
+def delta_rule_bwd(plan, Q, K, V, G, B, dO, scale=None):
+    """Gradients of ``delta_rule`` (w.r.t. the un-normalised q, k; v; the log
+    decay g; beta) for the output gradient dO [F, H, dv]: returns
+    (dQ, dK, dV, dG, dB)."""
+    dk = np.asarray(Q).shape[2]
+    scale = 1.0 / np.sqrt(dk) if scale is None else scale
+    return tuple(_vjp(plan, [Q, K, V, G, B], [], dO, lambda q, k, v, g, b: _delta_seq_t(q, k, v, g, b, scale)))
+
+
+def _prefix(plan, r):
+    off = plan["seq_offsets"]
+    s = int(np.searchsorted(off, r, side="right") - 1)
+    return plan["token_index"][off[s]:r + 1]
+
+
+def delta_rule_bwd_rows(plan, rows, picks, scale=None):
+    """The gradients for an output gradient that is zero except at the
+    forwarded positions of a few raw tokens: ``picks`` is a list of (raw
+    token r, dO row [H, dv]) with distinct forwarded positions; ``rows(key,
+    idx)`` returns rows ``idx`` of input ``key`` in ("q", "k", "v", "g",
+    "b").  Each pick's sequence prefix is run from S = 0.  Returns (pos,
+    (dQ, dK, dV, dG, dB)) with the gradient rows at the sorted forwarded
+    positions ``pos`` (every other row's gradient is zero)."""
+    torch = _torch()
+    ti = plan["token_index"]
+    assert len({int(ti[r]) for r, _ in picks}) == len(picks), "picks share a forwarded position"
+    paths = [_prefix(plan, r) for r, _ in picks]
+    pos = np.unique(np.concatenate(paths))
+    leaves = [torch.tensor(np.asarray(rows(key, pos), dtype=np.float64), requires_grad=True)
+              for key in ("q", "k", "v", "g", "b")]
+    dk = leaves[0].shape[2]
+    sc = 1.0 / np.sqrt(dk) if scale is None else scale
+    loss = torch.zeros((), dtype=torch.float64)
+    for path, (_, d) in zip(paths, picks):
+        at = torch.as_tensor(np.searchsorted(pos, path))
+        o = _delta_seq_t(*[l[at] for l in leaves], sc)
+        loss = loss + (o[-1] * torch.tensor(np.asarray(d, dtype=np.float64))).sum()
+    loss.backward()
+    return pos, tuple(l.grad.numpy() for l in leaves)
+
+
+def conv_bwd_rows(plan, rows, w, picks):
+    """``conv_bwd`` for an output gradient that is zero except at the
+    forwarded positions of a few raw tokens: ``picks`` is a list of (raw
+    token r, dY row [C]) with distinct forwarded positions; ``rows(idx)``
+    returns rows ``idx`` of x.  Returns (pos, dX rows at pos, dw)."""
+    torch = _torch()
+    ti = plan["token_index"]
+    assert len({int(ti[r]) for r, _ in picks}) == len(picks), "picks share a forwarded position"
+    W = np.asarray(w).shape[1]
+    paths = [_prefix(plan, r)[-W:] for r, _ in picks]
+    pos = np.unique(np.concatenate(paths))
+    x = torch.tensor(np.asarray(rows(pos), dtype=np.float64), requires_grad=True)
+    wt = torch.tensor(np.asarray(w, dtype=np.float64), requires_grad=True)
+    loss = torch.zeros((), dtype=torch.float64)
+    for path, (r, d) in zip(paths, picks):
+        # the window of the last position: its own path, zero above a root
+        # (a prefix shorter than W starts at the root)
+        y = _conv_seq_t(x[torch.as_tensor(np.searchsorted(pos, path))], wt)
+        loss = loss + (y[-1] * torch.tensor(np.asarray(d, dtype=np.float64))).sum()
+    loss.backward()
+    return pos, x.grad.numpy(), wt.grad.numpy()

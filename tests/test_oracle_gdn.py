@@ -203,3 +203,131 @@ def test_sampled_rows_match_the_full_run():
     raw = [0, 5, p["n_raw"] // 2, p["n_raw"] - 1]
     got = og.delta_rule_rows(p, lambda key, idx: keys[key][idx], raw)
     assert np.allclose(got, full[p["token_index"][raw]], rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------- gradients
+def _fd(f, arrays, i, h=1e-6):
+    """Central differences of the scalar f(*arrays) w.r.t. every entry of
+    arrays[i]."""
+    base = [np.array(a, dtype=np.float64) for a in arrays]
+    x = base[i]
+    out = np.zeros_like(x)
+    for j in np.ndindex(x.shape):
+        old = x[j]
+        x[j] = old + h
+        up = f(*base)
+        x[j] = old - h
+        dn = f(*base)
+        x[j] = old
+        out[j] = (up - dn) / (2 * h)
+    return out
+
+
+def test_conv_bwd_matches_central_differences():
+    # a small tree with branch points, width 3: dX sums over every
+    # descendant within two steps on every branch, dw over all positions
+    p = _tree(1, n=4)
+    rng = np.random.Generator(np.random.PCG64(31))
+    F, C, W = p["n_fwd"], 2, 3
+    X = rng.standard_normal((F, C))
+    w = rng.standard_normal((C, W))
+    dY = rng.standard_normal((F, C))
+    dX, dw = og.conv_bwd(p, X, w, dY)
+    loss = lambda X_, w_: float(np.sum(dY * og.conv(p, X_, w_)))
+    assert np.allclose(dX, _fd(loss, [X, w], 0), rtol=1e-7, atol=1e-8)
+    assert np.allclose(dw, _fd(loss, [X, w], 1), rtol=1e-7, atol=1e-8)
+    # the tree has a branch point, so some dX row gathers from two children
+    assert np.any(np.bincount(p["parent"][p["parent"] >= 0]) >= 2)
+
+
+def test_conv_bwd_width_one_closed_form():
+    # W = 1: y = silu(w x) per channel, so dX = dY silu'(w x) w and
+    # dw = sum_f dY silu'(w x) x, with silu'(a) = s(a) (1 + a (1 - s(a)))
+    p = _tree(2)
+    rng = np.random.Generator(np.random.PCG64(32))
+    F, C = p["n_fwd"], 4
+    X, dY = rng.standard_normal((F, C)), rng.standard_normal((F, C))
+    w = rng.standard_normal((C, 1))
+    a = X * w[:, 0]
+    s = 1 / (1 + np.exp(-a))
+    ds = s * (1 + a * (1 - s))
+    dX, dw = og.conv_bwd(p, X, w, dY)
+    assert np.allclose(dX, dY * ds * w[:, 0], rtol=1e-12, atol=1e-14)
+    assert np.allclose(dw[:, 0], np.sum(dY * ds * X, axis=0), rtol=1e-12, atol=1e-12)
+
+
+def test_delta_bwd_matches_central_differences():
+    # every input, on a tree whose sequences fork: gradients of the forked
+    # states are summed over the children
+    p = _tree(4, n=4)
+    rng = np.random.Generator(np.random.PCG64(33))
+    F, H, dk, dv = p["n_fwd"], 2, 3, 2
+    Q, K, V, G, B = _rand(rng, F, H, dk, dv)
+    dO = rng.standard_normal((F, H, dv))
+    grads = og.delta_rule_bwd(p, Q, K, V, G, B, dO, scale=0.6)
+    loss = lambda *a: float(np.sum(dO * og.delta_rule(p, *a, scale=0.6)))
+    for i, gr in enumerate(grads):
+        assert np.allclose(gr, _fd(loss, [Q, K, V, G, B], i), rtol=1e-6, atol=1e-8), "input %d" % i
+    assert np.any(np.bincount(p["parent"][p["parent"] >= 0]) >= 2)
+
+
+def test_delta_bwd_zero_beta_closed_form():
+    # beta = 0 writes nothing (S = 0), so dq, dk, dv and dg vanish, and to
+    # first order in beta, o_s = sum_{t <= s} beta_t Gamma(s, t) (k_t . q_s) v_t
+    # with Gamma(s, t) = prod_{t < r <= s} alpha_r: on a chain,
+    # dbeta_t = sum_{s >= t} Gamma(s, t) (k_t . q_s) (v_t . dO_s)
+    L, H, dk, dv = 11, 2, 5, 3
+    p = _chain_plan(L)
+    rng = np.random.Generator(np.random.PCG64(34))
+    Q, K, V, G, B = _rand(rng, L, H, dk, dv)
+    dO = rng.standard_normal((L, H, dv))
+    dQ, dK, dV, dG, dB = og.delta_rule_bwd(p, Q, K, V, G, np.zeros_like(B), dO, scale=0.3)
+    for z in (dQ, dK, dV, dG):
+        assert np.all(z == 0)
+    kn = K / np.linalg.norm(K, axis=-1, keepdims=True)
+    qn = 0.3 * Q / np.linalg.norm(Q, axis=-1, keepdims=True)
+    want = np.zeros((L, H))
+    for t in range(L):
+        for s in range(t, L):
+            gam = np.exp(np.sum(G[t + 1:s + 1], axis=0))
+            want[t] += gam * np.sum(kn[t] * qn[s], axis=-1) * np.sum(V[t] * dO[s], axis=-1)
+    assert np.allclose(dB, want, rtol=1e-12, atol=1e-13)
+
+
+def test_bwd_rows_match_the_dense_gradients():
+    # an output gradient at three positions only: the sampled form (each
+    # pick's prefix run alone) equals the dense one, which is zero elsewhere
+    p = _tree(5)
+    rng = np.random.Generator(np.random.PCG64(35))
+    F, H, dk, dv, C, W = p["n_fwd"], 2, 4, 3, 5, 3
+    X = _rand(rng, F, H, dk, dv)
+    ti = p["token_index"]
+    raw = [3, p["n_raw"] // 2, p["n_raw"] - 1]
+    assert len({int(ti[r]) for r in raw}) == 3
+    dO = np.zeros((F, H, dv))
+    picks = []
+    for r in raw:
+        d = rng.standard_normal((H, dv))
+        dO[ti[r]] = d
+        picks.append((r, d))
+    dense = og.delta_rule_bwd(p, *X, dO)
+    keys = dict(zip(("q", "k", "v", "g", "b"), X))
+    pos, rows = og.delta_rule_bwd_rows(p, lambda key, idx: keys[key][idx], picks)
+    for a, b in zip(dense, rows):
+        assert np.allclose(a[pos], b, rtol=1e-10, atol=1e-12)
+        rest = np.ones(F, dtype=bool)
+        rest[pos] = False
+        assert np.all(a[rest] == 0)
+    xc, wc = rng.standard_normal((F, C)), rng.standard_normal((C, W))
+    dY = np.zeros((F, C))
+    cp = []
+    for r in raw:
+        d = rng.standard_normal(C)
+        dY[ti[r]] = d
+        cp.append((r, d))
+    dX, dw = og.conv_bwd(p, xc, wc, dY)
+    pos, dXr, dwr = og.conv_bwd_rows(p, lambda idx: xc[idx], wc, cp)
+    assert np.allclose(dX[pos], dXr, rtol=1e-10, atol=1e-12) and np.allclose(dw, dwr, rtol=1e-10, atol=1e-12)
+    rest = np.ones(F, dtype=bool)
+    rest[pos] = False
+    assert np.all(dX[rest] == 0)
