@@ -194,7 +194,10 @@ int tpk_plan_raw_of_forwarded(const tpk_plan* plan, int32_t* fwd_raw_begin, int3
  * level_begin[l+1]) (n_seg_levels + 1 entries); seg_parent is the parent's
  * index in this order, -1 at a root.  Host int32 copies, any pointer may be
  * NULL; sizes from tpk_plan_info (n_seg_instances, n_seg_levels).  The
- * device image holds seg_start, seg_len, seg_parent (TPK_FIELD_SEG_*). */
+ * device image holds seg_start, seg_len, seg_parent and seg_off, the number
+ * of positions of the instances before it on its level (TPK_FIELD_SEG_*).
+ * Within a level instances are in ascending seg_start, so the children of an
+ * instance are one contiguous run of the next level. */
 int tpk_plan_segments(const tpk_plan* plan, int32_t* level_begin, int32_t* seg_start, int32_t* seg_len,
                       int32_t* seg_parent);
 
@@ -237,6 +240,7 @@ int tpk_plan_shard_rows(const tpk_plan* plan, int32_t world, int32_t* rank_of_ro
 #define TPK_FIELD_SEG_START    6   /* int32 [n_seg_instances], level order (tpk_plan_segments) */
 #define TPK_FIELD_SEG_LEN      7   /* int32 [n_seg_instances] */
 #define TPK_FIELD_SEG_PARENT   8   /* int32 [n_seg_instances] */
+#define TPK_FIELD_SEG_OFF      9   /* int32 [n_seg_instances]: positions of the instances before it on its level */
 size_t tpk_plan_device_bytes(const tpk_plan* plan);
 int tpk_plan_field_offset(const tpk_plan* plan, int32_t field, size_t* offset);
 int tpk_plan_upload(const tpk_plan* plan, void* dev_image, void* stream);
@@ -488,6 +492,53 @@ size_t tpk_gdn_workspace_bytes(const tpk_plan* plan, int32_t H, int32_t dk, int3
 int tpk_gdn_delta_rule(const tpk_plan* plan, const void* dev_image, const void* q, const void* k, const void* v,
                        int64_t ld_qk, int64_t ld_v, const float* g, const float* beta, void* o, int32_t H,
                        int32_t dk, int32_t dv, float scale, void* workspace, size_t ws_bytes, void* stream);
+
+/* Gradients of tpk_gdn_conv ("Prefix Tree Packing in ART", section
+ * "Token-mixing layers": the layer is differentiated through the packed
+ * tree, a position's input feeding the windows of its descendants on every
+ * branch below it).  For the output gradient dy [F, C] bf16:
+ *   dx[f, c] = sum over f' = f and the descendants of f within W-1 steps of
+ *              w[c, W-1-t] dy[f', c] silu'(a[f', c])    (t: steps from f to f')
+ *   dw[c, j] = sum_f dy[f, c] silu'(a[f, c]) x[a_{W-1-j}(f), c]
+ * with a the convolution's pre-activation (recomputed from x and w).
+ *   x, dy, dx [F, C] bf16; w [C, W] fp32 (16-byte aligned); dw [C, W] fp32,
+ *   overwritten (summed in a fixed order: deterministic).
+ *   workspace: >= tpk_gdn_conv_bwd_workspace_bytes bytes (per-stream partial
+ *   sums of dw), 256-byte aligned, need not be cleared.
+ * Same argument rules as tpk_gdn_conv; TPK_E_WORKSPACE for a short or
+ * misaligned workspace. */
+size_t tpk_gdn_conv_bwd_workspace_bytes(const tpk_plan* plan, int32_t C, int32_t W);
+int tpk_gdn_conv_bwd(const tpk_plan* plan, const void* dev_image, const void* x, const float* w, const void* dy,
+                     void* dx, float* dw, int32_t C, int32_t W, void* workspace, size_t ws_bytes, void* stream);
+
+/* Gradients of tpk_gdn_delta_rule for the output gradient dout [F, H, dv]
+ * bf16 (contiguous): dq, dk w.r.t. the un-normalised q, k ([F, H, dk] bf16,
+ * row stride ld_dqk), dv ([F, H, dv] bf16, row stride ld_dv), dg, dbeta
+ * ([F, H] fp32).  "Prefix Tree Packing in ART", section "Token-mixing
+ * layers": a child's initial state is its parent's final state, so the
+ * gradient of that state is the sum over the children; here each instance,
+ * deepest level first, hands the gradient of its initial state to its
+ * parent, which adds those of all its children (ascending order: the result
+ * is deterministic) before running its own chain backwards.  The state of
+ * each chain is recomputed from its initial state; dk = dv in {64, 128}.
+ *   q, k, v, ld_qk, ld_v, g, beta, H, dk, dv, scale: as given to the forward.
+ *   state: the workspace the forward filled (its saved final states; read
+ *   only), state_bytes >= tpk_gdn_workspace_bytes.
+ *   workspace: >= tpk_gdn_bwd_workspace_bytes bytes, 256-byte aligned, need
+ *   not be cleared: the initial-state gradients (n_seg_instances * H * dk * dv
+ *   fp32) and, reused level by level, each chain's checkpoints (its state
+ *   every 32 tokens) and per-token values (u_t, S_{t-1} k_t, 1/|k_t|,
+ *   do_t . o_t), sized by the largest level.
+ * Outputs may be column slices of one [F, ld] tensor (the convolution's
+ * gradient), with 16-byte aligned rows.  TPK_E_UNSUPPORTED for other head
+ * sizes, TPK_E_ARG for bad pointers or strides, TPK_E_WORKSPACE for a short
+ * or misaligned workspace. */
+size_t tpk_gdn_bwd_workspace_bytes(const tpk_plan* plan, int32_t H, int32_t dk, int32_t dv);
+int tpk_gdn_delta_rule_bwd(const tpk_plan* plan, const void* dev_image, const void* q, const void* k,
+                           const void* v, int64_t ld_qk, int64_t ld_v, const float* g, const float* beta,
+                           const void* dout, void* dq, void* dk_, void* dv_, int64_t ld_dqk, int64_t ld_dv,
+                           float* dg, float* dbeta, int32_t H, int32_t dk, int32_t dv, float scale,
+                           const void* state, size_t state_bytes, void* workspace, size_t ws_bytes, void* stream);
 
 /* Self-test of the device-side failure path (no counterpart on the pages):
  * launches one small kernel that waits, with the same bounded mbarrier wait

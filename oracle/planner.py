@@ -398,7 +398,8 @@ def segment_levels(instances):
     instance or -1) in placement order, parents before children.  Level = the
     number of ancestor instances; within a level, placement order.  Returns
     level_begin [n_levels+1] and seg_start / seg_len / seg_parent [n] in that
-    order, parents given as indices into it."""
+    order, parents given as indices into it, and seg_off [n]: the summed
+    length of the instances before it on its level."""
     n = len(instances)
     level = [0] * n
     for i, (_, _, par) in enumerate(instances):
@@ -411,7 +412,14 @@ def segment_levels(instances):
         begin[lv + 1] += 1
     for lv in range(n_levels):
         begin[lv + 1] += begin[lv]
+    off = [0] * n
+    for lv in range(n_levels):
+        acc = 0
+        for j in range(begin[lv], begin[lv + 1]):
+            off[j] = acc
+            acc += instances[order[j]][1]
     return {
+        "seg_off": np.asarray(off, dtype=np.int64),
         "seg_level_begin": np.asarray(begin, dtype=np.int64),
         "seg_start": np.asarray([instances[i][0] for i in order], dtype=np.int64),
         "seg_len": np.asarray([instances[i][1] for i in order], dtype=np.int64),

@@ -22,7 +22,7 @@ PLACE_NEXT_FIT = 1
 PLACE_GROUPS = 2
 FIELD_DEPTH, FIELD_TOKEN_INDEX, FIELD_SUBTREE_END, FIELD_PARENT = 0, 1, 2, 3
 FIELD_FWD_RAW_BEGIN, FIELD_FWD_RAW = 4, 5
-FIELD_SEG_START, FIELD_SEG_LEN, FIELD_SEG_PARENT = 6, 7, 8
+FIELD_SEG_START, FIELD_SEG_LEN, FIELD_SEG_PARENT, FIELD_SEG_OFF = 6, 7, 8, 9
 
 # every symbol include/tpk.h declares
 EXPORTS = [
@@ -32,7 +32,8 @@ EXPORTS = [
     "tpk_rope_by_depth", "tpk_attn_workspace_bytes", "tpk_tree_attn_fwd", "tpk_tree_attn_fwd_ex",
     "tpk_tree_attn_bwd", "tpk_tree_attn_bwd_ex", "tpk_tree_attn_bwd_phase", "tpk_tree_attn_bwd_noalloc", "tpk_selftest_wait_timeout",
     "tpk_scatter_token_index", "tpk_gather_to_forwarded", "tpk_sum_to_forwarded", "tpk_gdn_conv",
-    "tpk_gdn_workspace_bytes", "tpk_gdn_delta_rule", "tpk_status_string",
+    "tpk_gdn_workspace_bytes", "tpk_gdn_delta_rule", "tpk_gdn_conv_bwd_workspace_bytes", "tpk_gdn_conv_bwd",
+    "tpk_gdn_bwd_workspace_bytes", "tpk_gdn_delta_rule_bwd", "tpk_status_string",
     "tpk_version",
 ]
 
@@ -104,6 +105,13 @@ def _sig(lib):
     lib.tpk_gdn_workspace_bytes.argtypes = [P, I32, I32, I32]
     lib.tpk_gdn_workspace_bytes.restype = SZ
     lib.tpk_gdn_delta_rule.argtypes = [P, P, P, P, P, I64, I64, P, P, P, I32, I32, I32, ctypes.c_float, P, SZ, P]
+    lib.tpk_gdn_conv_bwd_workspace_bytes.argtypes = [P, I32, I32]
+    lib.tpk_gdn_conv_bwd_workspace_bytes.restype = SZ
+    lib.tpk_gdn_conv_bwd.argtypes = [P, P, P, P, P, P, P, I32, I32, P, SZ, P]
+    lib.tpk_gdn_bwd_workspace_bytes.argtypes = [P, I32, I32, I32]
+    lib.tpk_gdn_bwd_workspace_bytes.restype = SZ
+    lib.tpk_gdn_delta_rule_bwd.argtypes = [P, P, P, P, P, I64, I64, P, P, P, P, P, P, I64, I64, P, P, I32, I32, I32,
+                                           ctypes.c_float, P, SZ, P, SZ, P]
     lib.tpk_status_string.argtypes = [ctypes.c_int]
     lib.tpk_status_string.restype = ctypes.c_char_p
     lib.tpk_version.argtypes = []

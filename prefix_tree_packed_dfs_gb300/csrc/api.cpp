@@ -233,6 +233,7 @@ int tpk_plan_field_offset(const tpk_plan* plan, int32_t field, size_t* offset) {
     case TPK_FIELD_SEG_START: *offset = plan->p.off_seg_start; return TPK_OK;
     case TPK_FIELD_SEG_LEN: *offset = plan->p.off_seg_len; return TPK_OK;
     case TPK_FIELD_SEG_PARENT: *offset = plan->p.off_seg_parent; return TPK_OK;
+    case TPK_FIELD_SEG_OFF: *offset = plan->p.off_seg_off; return TPK_OK;
     default: return TPK_E_ARG;
   }
 }

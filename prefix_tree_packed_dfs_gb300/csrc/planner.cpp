@@ -459,6 +459,14 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
       P.seg_len[k] = inst_len[i];
       P.seg_parent[k] = inst_parent[i] < 0 ? -1 : pos[static_cast<size_t>(inst_parent[i])];
     }
+    P.seg_off.resize(ni);
+    for (int32_t l = 0; l < n_levels; ++l) {
+      int32_t acc = 0;
+      for (int32_t k = P.seg_level_begin[l]; k < P.seg_level_begin[l + 1]; ++k) {
+        P.seg_off[static_cast<size_t>(k)] = acc;
+        acc += P.seg_len[static_cast<size_t>(k)];
+      }
+    }
   }
   int64_t forks = 0;
   for (auto& s : segs) forks += (s.n_children >= 2);
@@ -642,6 +650,7 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   place(P.off_seg_start, 4 * P.seg_start.size());
   place(P.off_seg_len, 4 * P.seg_len.size());
   place(P.off_seg_parent, 4 * P.seg_parent.size());
+  place(P.off_seg_off, 4 * P.seg_off.size());
   // every byte is written once: the sections by copy, the padding after
   // each section (up to the next 256-byte boundary) with zeros; copied in
   // pieces of up to 4 MB on the host threads
@@ -675,6 +684,7 @@ int build_plan(const int32_t* tokens, const int64_t* seq_offsets, int32_t n_seqs
   put(P.off_seg_start, P.seg_start);
   put(P.off_seg_len, P.seg_len);
   put(P.off_seg_parent, P.seg_parent);
+  put(P.off_seg_off, P.seg_off);
   parallel_for(static_cast<int64_t>(pieces.size()), [&](int64_t i) {
     const Piece& pc = pieces[static_cast<size_t>(i)];
     if (pc.bytes == 0) return;

@@ -61,8 +61,10 @@ struct Plan {
   std::vector<int32_t> kt_k0, kt_nk, kt_qb_begin, qb, kt_order;
   // segment instances (a segment placed in one row) by tree level:
   // instances [seg_level_begin[l], seg_level_begin[l+1]) are level l; each
-  // covers forwarded [seg_start, +seg_len); seg_parent indexes this order
-  std::vector<int32_t> seg_level_begin, seg_start, seg_len, seg_parent;
+  // covers forwarded [seg_start, +seg_len); seg_parent indexes this order;
+  // seg_off = positions of the instances before it on its level (scratch
+  // offsets of a level-by-level pass)
+  std::vector<int32_t> seg_level_begin, seg_start, seg_len, seg_parent, seg_off;
 
   // device image: every array above that a kernel reads, 256-byte aligned sections
   std::vector<uint8_t, UninitAllocator<uint8_t>> image;
@@ -70,7 +72,7 @@ struct Plan {
   size_t off_fwd_raw_begin = 0, off_fwd_raw = 0;
   size_t off_qt_q0 = 0, off_qt_nq = 0, off_qt_kb_begin = 0, off_kb = 0, off_qt_order = 0;
   size_t off_kt_k0 = 0, off_kt_nk = 0, off_kt_qb_begin = 0, off_qb = 0, off_kt_order = 0;
-  size_t off_seg_start = 0, off_seg_len = 0, off_seg_parent = 0;
+  size_t off_seg_start = 0, off_seg_len = 0, off_seg_parent = 0, off_seg_off = 0;
 
   // Back to an empty plan, keeping every array's allocation: a plan built
   // into recycled storage writes into memory that is already mapped.  Every
@@ -85,14 +87,14 @@ struct Plan {
     for (std::vector<int32_t>* v : {&row_of_seq, &fwd_token, &fwd_src, &parent, &depth, &token_index, &subtree_end,
                                     &fwd_raw_begin, &fwd_raw, &qt_q0, &qt_nq, &qt_kb_begin, &kb, &qt_order, &kt_k0,
                                     &kt_nk, &kt_qb_begin, &qb, &kt_order, &seg_level_begin, &seg_start, &seg_len,
-                                    &seg_parent})
+                                    &seg_parent, &seg_off})
       v->clear();
     image.clear();
     off_depth = off_token_index = off_subtree_end = off_parent = 0;
     off_fwd_raw_begin = off_fwd_raw = 0;
     off_qt_q0 = off_qt_nq = off_qt_kb_begin = off_kb = off_qt_order = 0;
     off_kt_k0 = off_kt_nk = off_kt_qb_begin = off_qb = off_kt_order = 0;
-    off_seg_start = off_seg_len = off_seg_parent = 0;
+    off_seg_start = off_seg_len = off_seg_parent = off_seg_off = 0;
   }
 };
 

@@ -197,6 +197,7 @@ class DevicePlan:
         self.seg_start = self._field(B.FIELD_SEG_START, n_inst)
         self.seg_len = self._field(B.FIELD_SEG_LEN, n_inst)
         self.seg_parent = self._field(B.FIELD_SEG_PARENT, n_inst)
+        self.seg_off = self._field(B.FIELD_SEG_OFF, n_inst)
 
     def _field(self, field, n):
         off = self.plan.field_offset(field)
@@ -492,3 +493,115 @@ def gdn_delta_rule(dplan, q, k, v, g, beta, scale=None, out=None, workspace=None
                                    v.stride(0), _ptr(g), _ptr(beta), _ptr(out), H, dk, dv, scale, _ptr(workspace),
                                    ws_bytes, _stream()), "tpk_gdn_delta_rule")
     return out
+
+
+def gdn_workspace(dplan, H, dk, dv):
+    """A workspace for ``gdn_delta_rule`` (its saved per-instance final
+    states); keep it for ``gdn_delta_rule_bwd``."""
+    lib = B.load()
+    need = int(lib.tpk_gdn_workspace_bytes(dplan.plan.handle, H, dk, dv))
+    return torch.empty(max(need, 256), dtype=torch.uint8, device=dplan.image.device)
+
+
+def _rows3(t, name, shape=None):
+    """A 3-d bf16 view whose rows may be strided, contiguous inside a row."""
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.dim() != 3:
+        raise TypeError("%s must be a 3-d bf16 tensor" % name)
+    if shape is not None:
+        _shape(t, shape, name)
+    if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError("%s: heads and elements must be contiguous inside a row" % name)
+
+
+def gdn_conv_bwd(dplan, x, w, dy, dx=None, dw=None, workspace=None):
+    """Gradients of ``gdn_conv`` (``tpk_gdn_conv_bwd``): x, dy [F, C] bf16,
+    w [C, W] fp32 -> (dx [F, C] bf16, dw [C, W] fp32)."""
+    lib = B.load()
+    _need(x, torch.bfloat16, "x", 2, cuda=False)
+    _need(w, torch.float32, "w", 2, cuda=False)
+    _need(dy, torch.bfloat16, "dy", 2, cuda=False)
+    F, C = x.shape
+    W = w.shape[1]
+    if F != dplan.n_fwd:
+        raise ValueError("x has %d rows, the plan has %d forwarded positions" % (F, dplan.n_fwd))
+    if w.shape[0] != C:
+        raise ValueError("w must have shape (%d, W)" % C)
+    _shape(dy, (F, C), "dy")
+    dx = torch.empty_like(x) if dx is None else dx
+    dw = torch.empty_like(w) if dw is None else dw
+    _need(dx, torch.bfloat16, "dx", 2, cuda=False)
+    _shape(dx, (F, C), "dx")
+    _need(dw, torch.float32, "dw", 2, cuda=False)
+    _shape(dw, (C, W), "dw")
+    need = int(lib.tpk_gdn_conv_bwd_workspace_bytes(dplan.plan.handle, C, W))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if ws_bytes < need:
+        raise ValueError("workspace has %d bytes, the convolution's backward needs %d" % (ws_bytes, need))
+    _on_device(x, (w, "w"), (dy, "dy"), (dx, "dx"), (dw, "dw"), (workspace, "workspace"),
+               (dplan.image, "the plan image"))
+    B.check(lib.tpk_gdn_conv_bwd(dplan.plan.handle, _ptr(dplan.image), _ptr(x), _ptr(w), _ptr(dy), _ptr(dx), _ptr(dw),
+                                 C, W, _ptr(workspace), ws_bytes, _stream()), "tpk_gdn_conv_bwd")
+    return dx, dw
+
+
+def gdn_delta_rule_bwd(dplan, q, k, v, g, beta, dout, state, scale=None, dq=None, dk=None, dv=None, dg=None,
+                       dbeta=None, workspace=None):
+    """Gradients of ``gdn_delta_rule`` (``tpk_gdn_delta_rule_bwd``).
+
+    q, k, v, g, beta as given to the forward; ``state`` the workspace the
+    forward filled; dout [F, H, dv] bf16.  dq, dk (sharing one row stride)
+    and dv may be strided views, e.g. column slices of one [F, C] gradient.
+    Returns (dq, dk, dv, dg, dbeta)."""
+    lib = B.load()
+    _rows3(q, "q")
+    F, H, dkk = q.shape
+    dvv = v.shape[2]
+    if F != dplan.n_fwd:
+        raise ValueError("q has %d rows, the plan has %d forwarded positions" % (F, dplan.n_fwd))
+    _rows3(k, "k", (F, H, dkk))
+    _rows3(v, "v", (F, H, dvv))
+    if q.stride(0) != k.stride(0):
+        raise ValueError("q and k must share one row stride")
+    for t, n in ((g, "g"), (beta, "beta")):
+        _need(t, torch.float32, n, 2, cuda=False)
+        _shape(t, (F, H), n)
+    _need(dout, torch.bfloat16, "dout", 3, cuda=False)
+    _shape(dout, (F, H, dvv), "dout")
+    dev = q.device
+    dq = torch.empty((F, H, dkk), dtype=torch.bfloat16, device=dev) if dq is None else dq
+    dk = torch.empty((F, H, dkk), dtype=torch.bfloat16, device=dev) if dk is None else dk
+    dv = torch.empty((F, H, dvv), dtype=torch.bfloat16, device=dev) if dv is None else dv
+    _rows3(dq, "dq", (F, H, dkk))
+    _rows3(dk, "dk", (F, H, dkk))
+    _rows3(dv, "dv", (F, H, dvv))
+    if dq.stride(0) != dk.stride(0):
+        raise ValueError("dq and dk must share one row stride")
+    dg = torch.empty((F, H), dtype=torch.float32, device=dev) if dg is None else dg
+    dbeta = torch.empty((F, H), dtype=torch.float32, device=dev) if dbeta is None else dbeta
+    for t, n in ((dg, "dg"), (dbeta, "dbeta")):
+        _need(t, torch.float32, n, 2, cuda=False)
+        _shape(t, (F, H), n)
+    if not isinstance(state, torch.Tensor):
+        raise TypeError("state must be the forward's workspace tensor")
+    st_bytes = state.numel() * state.element_size()
+    need_st = int(lib.tpk_gdn_workspace_bytes(dplan.plan.handle, H, dkk, dvv))
+    if st_bytes < need_st:
+        raise ValueError("state has %d bytes, the forward's workspace has %d" % (st_bytes, need_st))
+    need = int(lib.tpk_gdn_bwd_workspace_bytes(dplan.plan.handle, H, dkk, dvv))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if ws_bytes < need:
+        raise ValueError("workspace has %d bytes, the delta rule's backward needs %d" % (ws_bytes, need))
+    scale = 1.0 / math.sqrt(dkk) if scale is None else float(scale)
+    _on_device(q, (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv"),
+               (dg, "dg"), (dbeta, "dbeta"), (state, "state"), (workspace, "workspace"),
+               (dplan.image, "the plan image"))
+    B.check(lib.tpk_gdn_delta_rule_bwd(dplan.plan.handle, _ptr(dplan.image), _ptr(q), _ptr(k), _ptr(v), q.stride(0),
+                                       v.stride(0), _ptr(g), _ptr(beta), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                       dq.stride(0), dv.stride(0), _ptr(dg), _ptr(dbeta), H, dkk, dvv, scale,
+                                       _ptr(state), st_bytes, _ptr(workspace), ws_bytes, _stream()),
+            "tpk_gdn_delta_rule_bwd")
+    return dq, dk, dv, dg, dbeta

@@ -152,3 +152,178 @@ def test_gdn_full_size_sampled(ops, name, H, d):
         want = acc / (1 + np.exp(-acc))
         got = f64(y[int(ref["token_index"][r])])
         assert np.all(np.abs(got - want) <= 2.0 ** -7 * np.abs(want) + 1e-5)
+
+
+# ---------------------------------------------------------------- backward
+BWD_CASES = [("tiny_fit", 2, 64), ("ragged_d128_h1", 3, 128), ("ragged_d64_gqa2", 2, 64), ("ragged_d64_h1", 1, 64)]
+
+
+def test_gdn_segment_arrays_on_device(ops):
+    """The plan image's level table (start, length, parent, level-local
+    offset) equals the oracle's, on a tree with six levels."""
+    w = SMALL["deep_small"]()
+    plan, dp, ref = _plans(ops, w)
+    for name in ("seg_start", "seg_len", "seg_parent", "seg_off"):
+        assert np.array_equal(getattr(dp, name).cpu().numpy(), ref[name]), name
+
+
+def _bwd_layer(ops, dp, y, gg, bg, H, d, dO, state=None):
+    """Delta rule forward and backward on views of the convolution output;
+    the gradients land as column slices of one [F, C] dy."""
+    q, k, v = _split(y, H, d, d)
+    ws = ops.gdn_workspace(dp, H, d, d) if state is None else state
+    o = ops.gdn_delta_rule(dp, q, k, v, gg, bg, workspace=ws)
+    dy = torch.empty_like(y)
+    dq, dk, dv = _split(dy, H, d, d)
+    _, _, _, dg, db = ops.gdn_delta_rule_bwd(dp, q, k, v, gg, bg, dO, ws, dq=dq, dk=dk, dv=dv)
+    return o, dy, dg, db
+
+
+@pytest.mark.parametrize("name,H,d", BWD_CASES)
+def test_gdn_bwd_full_parity(ops, name, H, d):
+    """Gradients of the delta rule (dq, dk, dv, dg, dbeta) and of the
+    convolution (dx, dw) against the oracle's fp64 autograd over the unpacked
+    sequences, on the same (bf16) inputs; the delta rule's gradients are
+    written as column slices of one dy, which feeds the convolution's
+    backward."""
+    w = SMALL[name]()
+    plan, dp, ref = _plans(ops, w)
+    F = plan.info["n_fwd"]
+    C = H * 3 * d
+    x, wc, g, b = wrng.gdn_inputs(w.seed_base + 60, F, C, H, W, "cuda")
+    dO = wrng.normal_bf16(w.seed_base + 61, (F, H, d), "cuda")
+    y = ops.gdn_conv(dp, x, wc)
+    o, dy, dg, db = _bwd_layer(ops, dp, y, g, b, H, d, dO)
+    torch.cuda.synchronize()
+    qn, kn, vn = (f64(t) for t in _split(y, H, d, d))
+    grads = og.delta_rule_bwd(ref, qn, kn, vn, f64(g), f64(b), f64(dO))
+    dq, dk, dv = _split(dy, H, d, d)
+    for got, want, n in zip((dq, dk, dv, dg, db), grads, ("dq", "dk", "dv", "dg", "dbeta")):
+        assert_close(f64(got), want, "%s gdn bwd %s" % (name, n))
+    dx, dw = ops.gdn_conv_bwd(dp, x, wc, dy)
+    torch.cuda.synchronize()
+    rdx, rdw = og.conv_bwd(ref, f64(x), f64(wc), f64(dy))
+    assert_close(f64(dx), rdx, "%s gdn conv bwd dx" % name)
+    assert_close(f64(dw), rdw, "%s gdn conv bwd dw" % name)
+
+
+def test_gdn_bwd_strong_decay_and_repeat(ops):
+    """Decay strong enough that walking the state backwards would lose it
+    (log decay -60 on one token in five, -3 on others): those steps are
+    replayed from a checkpoint; the gradients still match the oracle, and a
+    second call gives identical bits."""
+    w = SMALL["ragged_d64_h1"]()
+    plan, dp, ref = _plans(ops, w)
+    F, H, d = plan.info["n_fwd"], 2, 64
+    x, wc, g, b = wrng.gdn_inputs(w.seed_base + 70, F, H * 3 * d, H, W, "cuda")
+    sel = torch.arange(F, device="cuda") % 5 == 0
+    g = torch.where(sel[:, None], torch.full_like(g, -60.0), g - 3.0 * (torch.arange(F, device="cuda") % 7 == 1)[:, None])
+    dO = wrng.normal_bf16(w.seed_base + 71, (F, H, d), "cuda")
+    y = ops.gdn_conv(dp, x, wc)
+    o, dy, dg, db = _bwd_layer(ops, dp, y, g, b, H, d, dO)
+    o2, dy2, dg2, db2 = _bwd_layer(ops, dp, y, g, b, H, d, dO)
+    torch.cuda.synchronize()
+    assert torch.equal(dy, dy2) and torch.equal(dg, dg2) and torch.equal(db, db2)
+    qn, kn, vn = (f64(t) for t in _split(y, H, d, d))
+    grads = og.delta_rule_bwd(ref, qn, kn, vn, f64(g), f64(b), f64(dO))
+    dq, dk, dv = _split(dy, H, d, d)
+    for got, want, n in zip((dq, dk, dv, dg, db), grads, ("dq", "dk", "dv", "dg", "dbeta")):
+        assert_close(f64(got), want, "strong decay gdn bwd %s" % n)
+
+
+def _sparse_bwd(ops, name, H, d, n_picks, max_prefix, seed, last=False):
+    """The full batch's backward on the GPU with an output gradient that is
+    zero except at a few raw tokens' positions (each at most ``max_prefix``
+    tokens into its sequence, or with ``last`` each sequence's final token);
+    the oracle differentiates those outputs over their own prefixes.  Every
+    other row's gradient must be exactly zero."""
+    w = workloads.get(name) if name in ("grpo", "agentic") else SMALL[name]()
+    plan, dp, ref = _plans(ops, w)
+    F = plan.info["n_fwd"]
+    C = H * 3 * d
+    x, wc, g, b = wrng.gdn_inputs(seed, F, C, H, W, "cuda")
+    y = ops.gdn_conv(dp, x, wc)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    off, ti = ref["seq_offsets"], ref["token_index"]
+    picks, seen = [], set()
+    while len(picks) < n_picks:
+        s = int(rng.integers(0, len(off) - 1))
+        r = int(off[s + 1] - 1) if last else int(off[s] + rng.integers(0, min(max_prefix, off[s + 1] - off[s])))
+        if int(ti[r]) in seen:
+            continue
+        seen.add(int(ti[r]))
+        picks.append((r, rng.standard_normal((H, d)).astype(np.float32)))
+    dO = torch.zeros((F, H, d), dtype=torch.bfloat16, device="cuda")
+    for r, dd in picks:
+        dO[int(ti[r])] = torch.from_numpy(dd).to("cuda", torch.bfloat16)
+    o, dy, dg, db = _bwd_layer(ops, dp, y, g, b, H, d, dO)
+    torch.cuda.synchronize()
+    yc = y.cpu()
+    gc, bc = g.cpu().double().numpy(), b.cpu().double().numpy()
+
+    def rows(key, idx):
+        if key == "g":
+            return gc[idx]
+        if key == "b":
+            return bc[idx]
+        part = {"q": (0, H * d), "k": (H * d, 2 * H * d), "v": (2 * H * d, C)}[key]
+        return yc[idx, part[0]:part[1]].double().numpy().reshape(len(idx), H, d)
+    picks64 = [(r, np.asarray(f64(dO[int(ti[r])]))) for r, _ in picks]
+    pos, want = og.delta_rule_bwd_rows(ref, rows, picks64)
+    dq, dk, dv = _split(dy, H, d, d)
+    pt = torch.as_tensor(pos, device="cuda")
+    for got, wnt, n in zip((dq, dk, dv, dg, db), want, ("dq", "dk", "dv", "dg", "dbeta")):
+        assert_close(f64(got[pt]), wnt, "%s gdn bwd %s (sampled)" % (name, n))
+        rest = torch.ones(F, dtype=torch.bool, device="cuda")
+        rest[pt] = False
+        assert not bool(got[rest].any()), "%s: nonzero gradient off the picked paths" % n
+    return plan, dp, ref, x, wc, picks
+
+
+def test_gdn_bwd_deep_small_sampled(ops):
+    """Six levels of forks: the final tokens of three sequences, so each
+    picked output's gradient crosses several instance boundaries, handed
+    from child to parent."""
+    plan, _, ref, _, _, picks = _sparse_bwd(ops, "deep_small", 2, 128, 3, 0, 77, last=True)
+    starts, lens, ti = ref["seg_start"], ref["seg_len"], ref["token_index"]
+
+    def level_of(pos):
+        i = int(np.nonzero((starts <= pos) & (pos < starts + lens))[0][0])
+        return int(np.searchsorted(ref["seg_level_begin"], i, side="right") - 1)
+    assert min(level_of(int(ti[r])) for r, _ in picks) >= 2
+
+
+def test_gdn_bwd_full_size_sampled(ops):
+    """The GRPO batch at the bench's shape (16 heads, d = 128), full
+    backward launch; two picked outputs checked over their prefixes."""
+    _sparse_bwd(ops, "grpo", 16, 128, 2, 1200, 78)
+
+
+def test_gdn_conv_bwd_full_size_sampled(ops):
+    """The convolution's backward on the GRPO batch with dy nonzero at a few
+    positions: dx at their windows and dw against the oracle."""
+    w = workloads.get("grpo")
+    plan, dp, ref = _plans(ops, w)
+    F, H, d = plan.info["n_fwd"], 16, 128
+    C = H * 3 * d
+    x, wc, _, _ = wrng.gdn_inputs(w.seed_base + 80, F, C, H, W, "cuda")
+    rng = np.random.Generator(np.random.PCG64(80))
+    ti = ref["token_index"]
+    raw = sorted({int(r) for r in rng.integers(0, plan.info["n_raw"], size=4)})
+    raw = [r for i, r in enumerate(raw) if int(ti[r]) not in {int(ti[q]) for q in raw[:i]}]
+    dy = torch.zeros((F, C), dtype=torch.bfloat16, device="cuda")
+    picks = []
+    for r in raw:
+        dd = wrng.normal_bf16(w.seed_base + 81 + r, (C,))
+        dy[int(ti[r])] = dd.to("cuda")
+        picks.append((r, dd.double().numpy()))
+    dx, dw = ops.gdn_conv_bwd(dp, x, wc, dy)
+    torch.cuda.synchronize()
+    xc = x.cpu()
+    pos, rdx, rdw = og.conv_bwd_rows(ref, lambda idx: xc[idx].double().numpy(), f64(wc), picks)
+    pt = torch.as_tensor(pos, device="cuda")
+    assert_close(f64(dx[pt]), rdx, "grpo gdn conv bwd dx (sampled)")
+    assert_close(f64(dw), rdw, "grpo gdn conv bwd dw (sampled)")
+    rest = torch.ones(F, dtype=torch.bool, device="cuda")
+    rest[pt] = False
+    assert not bool(dx[rest].any())

@@ -185,6 +185,11 @@ def test_level_schedule_equals_unpacked_sequences(seed):
     for s, n in zip(start, length):
         cover[s:s + n] += 1
     assert np.all(cover == 1)
+    # level-local offsets: the lengths of the earlier instances of the level
+    for lv in range(len(begin) - 1):
+        i0, i1 = begin[lv], begin[lv + 1]
+        assert list(p["seg_off"][i0:i1]) == [int(np.sum(length[i0:i])) for i in range(i0, i1)]
+        assert np.all(np.diff(start[i0:i1]) > 0)   # ascending starts within a level
     for lv in range(len(begin) - 1):
         for i in range(begin[lv], begin[lv + 1]):
             if lv == 0:
