@@ -412,9 +412,34 @@ def run_gdn(peaks, local, warmup, names=GDN_WORKLOADS):
         ms_conv, n_conv = _time_launches(lambda: ops.gdn_conv(dp, x, wc, y=y), flush, min_s=0.3, warmup=warmup)
         ms_delta, n_delta = _time_launches(lambda: ops.gdn_delta_rule(dp, q, k, v, g, b, out=o, workspace=ws),
                                            flush, min_s=0.5, min_n=5, warmup=warmup)
+        # backward: the delta rule's gradients as column slices of one dy,
+        # which the convolution's backward reads
+        dO = wrng.normal_bf16(w.seed_base + 51, (F, H, dv), "cuda")
+        dy, dx = torch.empty_like(x), torch.empty_like(x)
+        dw = torch.empty_like(wc)
+        dq, dkk, dvv = (dy[:, :H * dk].unflatten(1, (H, dk)), dy[:, H * dk:2 * H * dk].unflatten(1, (H, dk)),
+                        dy[:, 2 * H * dk:].unflatten(1, (H, dv)))
+        dg = torch.empty((F, H), dtype=torch.float32, device="cuda")
+        db = torch.empty_like(dg)
+        lib = ops.B.load()
+        wsb = torch.empty(max(int(lib.tpk_gdn_bwd_workspace_bytes(plan.handle, H, dk, dv)), 256), dtype=torch.uint8,
+                          device="cuda")
+        wsc = torch.empty(max(int(lib.tpk_gdn_conv_bwd_workspace_bytes(plan.handle, C, W)), 256), dtype=torch.uint8,
+                          device="cuda")
+        ms_dbwd, n_dbwd = _time_launches(
+            lambda: ops.gdn_delta_rule_bwd(dp, q, k, v, g, b, dO, ws, dq=dq, dk=dkk, dv=dvv, dg=dg, dbeta=db,
+                                           workspace=wsb), flush, min_s=0.5, min_n=3, warmup=warmup)
+        ms_cbwd, n_cbwd = _time_launches(lambda: ops.gdn_conv_bwd(dp, x, wc, dy, dx=dx, dw=dw, workspace=wsc), flush,
+                                         min_s=0.3, warmup=warmup)
         clk = clocks.stop()
         conv_bytes = 2 * F * C * 2 + 4 * F + 4 * C * W          # x read, y written, parent, weights
+        # x and dy read, dx written; parent, depth, subtree_end; dw partials
+        # written and read back
+        conv_bwd_bytes = 3 * F * C * 2 + 12 * F + 2 * (wsc.numel() // 4 * 4)
         delta_flop = 6.0 * dk * dv * F * H                      # S k, the update, S q per token and head
+        # executed: the recomputed forward (6) and, walking back, the output
+        # term, D k, S^T do, D^T u, the reversal (3), S^T y, the D update (3)
+        delta_bwd_flop = 22.0 * dk * dv * F * H
         peak32, sms = fp32_peak_tflops(clk.get("sm_mhz"))
         out[name] = {"forwarded_tokens": F, "raw_tokens": info["n_raw"], "segment_instances": info["n_seg_instances"],
                      "levels": info["n_seg_levels"], "conv_ms": ms_conv, "conv_gbs": conv_bytes / ms_conv / 1e6,
@@ -423,12 +448,18 @@ def run_gdn(peaks, local, warmup, names=GDN_WORKLOADS):
                      "delta_frac_of_fp32_peak": delta_flop / ms_delta / 1e9 / peak32,
                      "fp32_peak_tflops": peak32, "forwarded_tokens_per_s": F / (ms_conv + ms_delta) * 1e3,
                      "raw_tokens_per_s": info["n_raw"] / (ms_conv + ms_delta) * 1e3,
-                     "launches_timed": [n_conv, n_delta], "clocks": clk}
-        del x, y, o, ws, q, k, v, dp, plan
+                     "delta_bwd_ms": ms_dbwd, "delta_bwd_tflops": delta_bwd_flop / ms_dbwd / 1e9,
+                     "delta_bwd_frac_of_fp32_peak": delta_bwd_flop / ms_dbwd / 1e9 / peak32,
+                     "conv_bwd_ms": ms_cbwd, "conv_bwd_gbs": conv_bwd_bytes / ms_cbwd / 1e6,
+                     "conv_bwd_frac_of_copy_peak": conv_bwd_bytes / ms_cbwd / 1e6 / peaks["hbm_gbs"],
+                     "fwd_bwd_raw_tokens_per_s": info["n_raw"] / (ms_conv + ms_delta + ms_dbwd + ms_cbwd) * 1e3,
+                     "launches_timed": [n_conv, n_delta, n_dbwd, n_cbwd], "clocks": clk}
+        del x, y, o, ws, q, k, v, dO, dy, dx, dw, dq, dkk, dvv, dg, db, wsb, wsc, dp, plan
         torch.cuda.empty_cache()
-    return {"what": "GDN tree path, H %d, dk = dv = %d, conv width %d: conv (one launch, HBM-bound: against the "
-                    "copy peak) and gated delta rule (one launch per tree level, fp32 state: against the fp32 FMA "
-                    "peak = SMs x 128 lanes x 2 x the median SM clock); L2 flushed before every timed call"
+    return {"what": "GDN tree path, H %d, dk = dv = %d, conv width %d: conv and its backward (HBM-bound: against "
+                    "the copy peak) and gated delta rule forward and backward (one launch per tree level, fp32 "
+                    "state: against the fp32 FMA peak = SMs x 128 lanes x 2 x the median SM clock; the backward's "
+                    "executed FLOP include its recomputed forward); L2 flushed before every timed call"
                     % (H, dk, W), "workloads": out}
 
 

@@ -70,32 +70,108 @@ constexpr int kCvThreads = 256;
 constexpr int kCvMaxW = 8;
 constexpr int64_t kCvThreadCap = int64_t{1} << 20;
 
+constexpr int kCvRunHost = 64;   // positions per run of the backward kernel (kCvRun)
+
 int64_t conv_streams(int64_t F, int C) {
-  const int64_t cpr = C / 8;
-  return std::max<int64_t>(1, std::min<int64_t>(F, kCvThreadCap / cpr));
+  const int64_t cpr = C / 4;   // channel groups of the backward kernel (kCh)
+  return std::max<int64_t>(1, std::min<int64_t>((F + kCvRunHost - 1) / kCvRunHost, kCvThreadCap / cpr));
 }
 
 // silu'(a) = s (1 + a (1 - s)), s = 1 / (1 + e^-a)
 __device__ __forceinline__ float dsilu(float a) {
-  const float s = 1.f / (1.f + __expf(-a));
+  const float s = __fdividef(1.f, 1.f + __expf(-a));
   return s * (1.f + a * (1.f - s));
 }
 
+// 4 channels (8 bytes) per thread in the backward: its rings hold W
+// values per channel, so this keeps them in registers
+constexpr int kCh = 4;
+
+__device__ __forceinline__ float bf_at(const uint2& r, int e) {
+  const uint32_t word = e < 2 ? r.x : r.y;
+  return (e & 1) ? hi_bf(word) : lo_bf(word);
+}
+
+// dx[f] by the general walk: f's subtree in preorder down to depth W-1
+// (subtree_end skips deeper parts), each descendant's pre-activation
+// recomputed from its window (the path between f and it, then f's own
+// ancestors).  Used where a fork lies within W-1 steps below f.
+template <int W>
+__device__ __forceinline__ void conv_bwd_walk(const int32_t* __restrict__ parent, const int32_t* __restrict__ depth,
+                                              const int32_t* __restrict__ subtree_end, const uint2* __restrict__ x,
+                                              const float (&wr)[kCh * W], const uint2* __restrict__ dy, int64_t f,
+                                              int cpr, int g, float (&dxa)[kCh]) {
+  uint2 anc[W];
+  {
+    int64_t a = f;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      anc[i] = a >= 0 ? __ldg(x + a * cpr + g) : make_uint2(0u, 0u);
+      if (i + 1 < W) a = a >= 0 ? __ldg(parent + a) : -1;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < kCh; ++e) dxa[e] = 0.f;
+  uint2 st[W];
+#pragma unroll
+  for (int i = 0; i < W; ++i) st[i] = anc[0];
+  auto visit = [&](const int T, const int64_t node) {   // T constant after unrolling
+    const uint2 dv = __ldg(dy + node * cpr + g);
+#pragma unroll
+    for (int e = 0; e < kCh; ++e) {
+      float a = 0.f;
+#pragma unroll
+      for (int i = 0; i < W; ++i) a = fmaf(wr[e * W + (W - 1 - i)], bf_at(i <= T ? st[T - i] : anc[i - T], e), a);
+      dxa[e] = fmaf(wr[e * W + (W - 1 - T)], bf_at(dv, e) * dsilu(a), dxa[e]);
+    }
+  };
+  visit(0, f);
+  const int32_t d0 = __ldg(depth + f);
+  const int64_t end = __ldg(subtree_end + f);
+  int64_t node = f + 1;
+  while (node < end) {
+    const int t = __ldg(depth + node) - d0;
+    const uint2 xv = __ldg(x + node * cpr + g);
+#pragma unroll
+    for (int T = 1; T < W; ++T)
+      if (T == t) {
+        st[T] = xv;
+        visit(T, node);
+      }
+    node = t < W - 1 ? node + 1 : static_cast<int64_t>(__ldg(subtree_end + node));
+  }
+}
+
+constexpr int kCvRun = 64;   // positions per run
+
+// A thread owns one group of kCh channels and walks runs of kCvRun
+// positions (runs s, s + streams, ..), ascending.  At each position p it
+// keeps p's window (x at p and its W-1 nearest ancestors: shifted in from
+// p-1 where p's parent is p-1, else gathered through the parent array) and
+// the last W values of da = dy silu'(a); dw takes da[p] times the window
+// (positions of the run only), and dx[p-W+1] is complete once da[p] is known:
+//   dx[f] = sum_t w_{W-1-t} da[f+t]
+// wherever the positions below f form one chain for W-1 steps (every node
+// on it has one child, the next position, until a leaf), which the kinds
+// of f .. f+W-2 tell (leaf: subtree_end = n+1; one child: subtree_end[n+1]
+// = subtree_end[n]).  Elsewhere (a fork within W-1 steps below f) the
+// general walk above computes dx[f].  A run reads W-1 positions past its
+// end (their da) and recomputes them: (W-1)/kCvRun extra work.
 template <int W>
 __global__ void __launch_bounds__(kCvThreads) gdn_conv_bwd_kernel(
     const int32_t* __restrict__ parent, const int32_t* __restrict__ depth, const int32_t* __restrict__ subtree_end,
-    const uint4* __restrict__ x, const float* __restrict__ w, const uint4* __restrict__ dy, uint4* __restrict__ dx,
+    const uint2* __restrict__ x, const float* __restrict__ w, const uint2* __restrict__ dy, uint2* __restrict__ dx,
     float* __restrict__ dw_part, int64_t F, int C, int64_t streams) {
-  const int cpr = C / 8;
+  const int cpr = C / kCh;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * kCvThreads + threadIdx.x;
   if (tid >= streams * cpr) return;
   const int g = static_cast<int>(tid % cpr);
   const int64_t s = tid / cpr;
-  float wr[8 * W];   // channel 8g + e, tap j at wr[e * W + j]
+  float wr[kCh * W];   // channel kCh g + e, tap j at wr[e * W + j]
   {
-    const float4* w4 = reinterpret_cast<const float4*>(w + static_cast<int64_t>(g) * 8 * W);
+    const float4* w4 = reinterpret_cast<const float4*>(w + static_cast<int64_t>(g) * kCh * W);
 #pragma unroll
-    for (int i = 0; i < 2 * W; ++i) {
+    for (int i = 0; i < kCh * W / 4; ++i) {
       const float4 v = __ldg(w4 + i);
       wr[4 * i] = v.x;
       wr[4 * i + 1] = v.y;
@@ -103,74 +179,92 @@ __global__ void __launch_bounds__(kCvThreads) gdn_conv_bwd_kernel(
       wr[4 * i + 3] = v.w;
     }
   }
-  float dwa[8 * W];
+  float dwa[kCh * W];
 #pragma unroll
-  for (int i = 0; i < 8 * W; ++i) dwa[i] = 0.f;
-
-  for (int64_t f = s; f < F; f += streams) {
-    // f's own window: f and its W-1 nearest ancestors
-    uint4 anc[W];
-    {
-      int64_t a = f;
+  for (int i = 0; i < kCh * W; ++i) dwa[i] = 0.f;
+  const int64_t n_runs = (F + kCvRun - 1) / kCvRun;
+  for (int64_t run = s; run < n_runs; run += streams) {
+    const int64_t f0 = run * kCvRun, f1 = min(f0 + kCvRun, F);
+    uint2 win[W];          // p's window: win[i] = x at p's i-th ancestor
+    float da[W][kCh];      // da[W-1] at p, da[W-1-i] at p - i
+    int kind[W];           // kind[W-1-i] of position p - 1 - i: 0 leaf, 1 one child, 2 fork
 #pragma unroll
-      for (int i = 0; i < W; ++i) {
-        anc[i] = a >= 0 ? __ldg(x + a * cpr + g) : make_uint4(0u, 0u, 0u, 0u);
-        if (i + 1 < W) a = a >= 0 ? __ldg(parent + a) : -1;
-      }
+    for (int i = 0; i < W; ++i) {
+      kind[i] = 0;
+      win[i] = make_uint2(0u, 0u);
+#pragma unroll
+      for (int e = 0; e < kCh; ++e) da[i][e] = 0.f;
     }
-    float dxa[8];
+    int32_t se_prev = 0;
+    for (int64_t p = f0; p < f1 + W - 1; ++p) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) dxa[e] = 0.f;
-    // one descendant at distance T whose window is st[T..0] then anc[1..];
-    // called with T a constant after unrolling, so every index is static
-    auto visit = [&](const int T, const int64_t node, const uint4 (&st)[W]) {
-      const uint4 dv = __ldg(dy + node * cpr + g);
+      for (int i = 0; i + 1 < W; ++i) {
+        kind[i] = kind[i + 1];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float a = 0.f;
+        for (int e = 0; e < kCh; ++e) da[i][e] = da[i + 1][e];
+      }
+      if (p < F) {
+        const int32_t par = __ldg(parent + p);
+        const int32_t se = __ldg(subtree_end + p);
+        const uint2 xp = __ldg(x + p * cpr + g);
+        const uint2 dv = __ldg(dy + p * cpr + g);
+        if (p > f0 && par == p - 1) {
 #pragma unroll
-        for (int i = 0; i < W; ++i) {
-          const uint4 r = i <= T ? st[T - i] : anc[i - T];
-          const uint32_t word = (&r.x)[e / 2];
-          a = fmaf(wr[e * W + (W - 1 - i)], (e & 1) ? hi_bf(word) : lo_bf(word), a);
-        }
-        const uint32_t dword = (&dv.x)[e / 2];
-        const float da = ((e & 1) ? hi_bf(dword) : lo_bf(dword)) * dsilu(a);
-        dxa[e] = fmaf(wr[e * W + (W - 1 - T)], da, dxa[e]);
-        if (T == 0) {
+          for (int i = W - 1; i > 0; --i) win[i] = win[i - 1];
+        } else {
+          int64_t a = par;
 #pragma unroll
-          for (int i = 0; i < W; ++i) {
-            const uint32_t word = (&anc[i].x)[e / 2];
-            dwa[e * W + (W - 1 - i)] = fmaf(da, (e & 1) ? hi_bf(word) : lo_bf(word), dwa[e * W + (W - 1 - i)]);
+          for (int i = 1; i < W; ++i) {
+            win[i] = a >= 0 ? __ldg(x + a * cpr + g) : make_uint2(0u, 0u);
+            if (i + 1 < W) a = a >= 0 ? __ldg(parent + a) : -1;
           }
         }
-      }
-    };
-    uint4 st[W];   // x along the path from f (st[0]) to the current descendant
+        win[0] = xp;
 #pragma unroll
-    for (int i = 0; i < W; ++i) st[i] = anc[0];
-    visit(0, f, st);
-    if (W > 1) {
-      const int32_t d0 = __ldg(depth + f);
-      const int64_t end = __ldg(subtree_end + f);
-      int64_t node = f + 1;
-      while (node < end) {   // preorder over f's subtree, cut below depth W-1
-        const int t = __ldg(depth + node) - d0;
-        const uint4 xv = __ldg(x + node * cpr + g);
+        for (int e = 0; e < kCh; ++e) {
+          float a = 0.f;
 #pragma unroll
-        for (int T = 1; T < W; ++T)
-          if (T == t) {
-            st[T] = xv;
-            visit(T, node, st);
+          for (int i = 0; i < W; ++i) a = fmaf(wr[e * W + (W - 1 - i)], bf_at(win[i], e), a);
+          const float d = bf_at(dv, e) * dsilu(a);
+          da[W - 1][e] = d;
+          if (p < f1) {
+#pragma unroll
+            for (int i = 0; i < W; ++i) dwa[e * W + (W - 1 - i)] = fmaf(d, bf_at(win[i], e), dwa[e * W + (W - 1 - i)]);
           }
-        node = t < W - 1 ? node + 1 : static_cast<int64_t>(__ldg(subtree_end + node));
+        }
+        // the kind of p - 1, now that subtree_end[p] is known
+        if (p > f0) kind[W - 1] = se_prev == p ? 0 : (se == se_prev ? 1 : 2);
+        se_prev = se;
+      } else {
+#pragma unroll
+        for (int e = 0; e < kCh; ++e) da[W - 1][e] = 0.f;
+        kind[W - 1] = 0;   // past the end: F - 1 is a leaf
+      }
+      const int64_t f = p - (W - 1);
+      if (f >= f0) {
+        float acc[kCh];
+        bool alive = true, fork = false;
+#pragma unroll
+        for (int e = 0; e < kCh; ++e) acc[e] = wr[e * W + (W - 1)] * da[0][e];
+#pragma unroll
+        for (int t = 1; t < W; ++t) {
+          // the kind of f + t - 1 is kind[t] (kind[W-1] is p - 1 = f + W - 2)
+          const int kd = kind[t];
+          if (alive && kd == 2) fork = true;
+          alive = alive && kd == 1;
+          if (alive) {
+#pragma unroll
+            for (int e = 0; e < kCh; ++e) acc[e] = fmaf(wr[e * W + (W - 1 - t)], da[t][e], acc[e]);
+          }
+        }
+        if (fork) conv_bwd_walk<W>(parent, depth, subtree_end, x, wr, dy, f, cpr, g, acc);
+        dx[f * cpr + g] = make_uint2(bf2(acc[0], acc[1]), bf2(acc[2], acc[3]));
       }
     }
-    dx[f * cpr + g] = make_uint4(bf2(dxa[0], dxa[1]), bf2(dxa[2], dxa[3]), bf2(dxa[4], dxa[5]), bf2(dxa[6], dxa[7]));
   }
-  float* dst = dw_part + (s * C + static_cast<int64_t>(g) * 8) * W;
+  float* dst = dw_part + (s * C + static_cast<int64_t>(g) * kCh) * W;
 #pragma unroll
-  for (int i = 0; i < 8 * W; ++i) dst[i] = dwa[i];
+  for (int i = 0; i < kCh * W; ++i) dst[i] = dwa[i];
 }
 
 // dw[c, j] = sum over streams of the partials, in stream order
@@ -185,9 +279,9 @@ __global__ void gdn_dw_reduce_kernel(const float* __restrict__ part, float* __re
 template <int W>
 void launch_conv_bwd(const int32_t* par, const int32_t* dep, const int32_t* sub, const void* x, const float* w,
                      const void* dy, void* dx, float* part, int64_t F, int C, int64_t streams, cudaStream_t s) {
-  const int64_t threads = streams * (C / 8);
+  const int64_t threads = streams * (C / kCh);
   gdn_conv_bwd_kernel<W><<<static_cast<unsigned>((threads + kCvThreads - 1) / kCvThreads), kCvThreads, 0, s>>>(
-      par, dep, sub, static_cast<const uint4*>(x), w, static_cast<const uint4*>(dy), static_cast<uint4*>(dx), part, F,
+      par, dep, sub, static_cast<const uint2*>(x), w, static_cast<const uint2*>(dy), static_cast<uint2*>(dx), part, F,
       C, streams);
 }
 
