@@ -333,26 +333,40 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
   const int64_t HD = static_cast<int64_t>(p.H) * D;
   if (len <= 0) return;
 
-  float S[RT][CT], Dm[RT][CT];
-  auto tile_load = [&](float (&M)[RT][CT], const float* base) {   // base: [D][D] row-major
+  // S and D as packed fp32 pairs along the columns: S2[r][i] = columns
+  // c0 + 2i, c0 + 2i + 1 of row r0 + r (two lanes per f32x2 instruction)
+  constexpr int CP = CT / 2;
+  uint64_t S2[RT][CP], D2[RT][CP];
+  auto tile_load = [&](uint64_t (&M)[RT][CP], const float* base) {   // base: [D][D] row-major
 #pragma unroll
     for (int r = 0; r < RT; ++r)
 #pragma unroll
-      for (int c = 0; c < CT; c += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(base + (r0 + r) * D + c0 + c);
-        M[r][c] = v.x;
-        M[r][c + 1] = v.y;
-        M[r][c + 2] = v.z;
-        M[r][c + 3] = v.w;
+      for (int i = 0; i < CP; i += 2) {
+        const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(base + (r0 + r) * D + c0 + 2 * i);
+        M[r][i] = v.x;
+        M[r][i + 1] = v.y;
       }
   };
-  auto tile_store = [&](const float (&M)[RT][CT], float* base) {
+  auto tile_store = [&](const uint64_t (&M)[RT][CP], float* base) {
 #pragma unroll
     for (int r = 0; r < RT; ++r)
 #pragma unroll
-      for (int c = 0; c < CT; c += 4)
-        *reinterpret_cast<float4*>(base + (r0 + r) * D + c0 + c) =
-            make_float4(M[r][c], M[r][c + 1], M[r][c + 2], M[r][c + 3]);
+      for (int i = 0; i < CP; i += 2)
+        *reinterpret_cast<ulonglong2*>(base + (r0 + r) * D + c0 + 2 * i) = make_ulonglong2(M[r][i], M[r][i + 1]);
+  };
+  auto pair_sum = [](uint64_t v) {
+    float lo, hi;
+    ptx::unf2(v, lo, hi);
+    return lo + hi;
+  };
+  // columns c0 .. c0 + CT - 1 of a staged row as pairs
+  auto row_pairs = [&](const float* rowp, uint64_t (&out)[CP]) {
+#pragma unroll
+    for (int i = 0; i < CP; i += 2) {
+      const ulonglong2 v = ptx::lds128u(rowp + c0 + 2 * i);
+      out[i] = v.x;
+      out[i + 1] = v.y;
+    }
   };
   auto ck_ptr = [&](int64_t slot) { return p.ck + (slot * p.H + h) * static_cast<int64_t>(D) * D; };
   // sum over the 16 lanes of a half warp (the column tiles of a row tile)
@@ -421,44 +435,43 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
   };
 
   // ---------------- pass A: forward from the initial state, with scratch
-  if (par >= 0) tile_load(S, p.state + (static_cast<int64_t>(par) * p.H + h) * D * D);
+  if (par >= 0) tile_load(S2, p.state + (static_cast<int64_t>(par) * p.H + h) * D * D);
   else {
 #pragma unroll
     for (int r = 0; r < RT; ++r)
 #pragma unroll
-      for (int c = 0; c < CT; ++c) S[r][c] = 0.f;
+      for (int i = 0; i < CP; ++i) S2[r][i] = 0ull;
   }
   for (int j0 = 0; j0 < len; j0 += kRT) {
     const int nt = min(kRT, len - j0);
     stage(j0, nt, false);
     for (int j = 0; j < nt; ++j) {
       const int jj = j0 + j;
-      if (jj % kCk == 0) tile_store(S, ck_ptr(slot0 + jj / kCk));
-      float kk[CT], qq[CT];
-#pragma unroll
-      for (int c = 0; c < CT; ++c) {
-        kk[c] = sm.k[j][c0 + c];
-        qq[c] = sm.q[j][c0 + c];
-      }
+      if (jj % kCk == 0) tile_store(S2, ck_ptr(slot0 + jj / kCk));
+      uint64_t k2[CP], q2[CP];
+      row_pairs(sm.k[j], k2);
+      row_pairs(sm.q[j], q2);
       const float a = sm.alpha[j], b = sm.beta[j];
+      const uint64_t a2 = ptx::f2(a, a);
       float u[RT], wv[RT], o[RT];
 #pragma unroll
       for (int r = 0; r < RT; ++r) {
-        float acc = 0.f;
+        uint64_t acc = 0ull;
 #pragma unroll
-        for (int c = 0; c < CT; ++c) acc = fmaf(S[r][c], kk[c], acc);
-        wv[r] = rowsum(acc);
+        for (int i = 0; i < CP; ++i) acc = ptx::fma2(S2[r][i], k2[i], acc);
+        wv[r] = rowsum(pair_sum(acc));
         u[r] = b * (sm.v[j][r0 + r] - a * wv[r]);
       }
 #pragma unroll
       for (int r = 0; r < RT; ++r) {
-        float acc = 0.f;
+        const uint64_t u2 = ptx::f2(u[r], u[r]);
+        uint64_t acc = 0ull;
 #pragma unroll
-        for (int c = 0; c < CT; ++c) {
-          S[r][c] = fmaf(u[r], kk[c], a * S[r][c]);
-          acc = fmaf(S[r][c], qq[c], acc);
+        for (int i = 0; i < CP; ++i) {
+          S2[r][i] = ptx::fma2(u2, k2[i], ptx::mul2(a2, S2[r][i]));
+          acc = ptx::fma2(S2[r][i], q2[i], acc);
         }
-        o[r] = rowsum(acc);
+        o[r] = rowsum(pair_sum(acc));
       }
       float dp = 0.f;
 #pragma unroll
@@ -495,7 +508,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
 #pragma unroll
     for (int r = 0; r < RT; ++r)
 #pragma unroll
-      for (int c = 0; c < CT; ++c) Dm[r][c] = 0.f;
+      for (int i = 0; i < CP; ++i) D2[r][i] = 0ull;
     int lo = p.next0, hi = p.next1;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
@@ -507,23 +520,22 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
 #pragma unroll
       for (int r = 0; r < RT; ++r)
 #pragma unroll
-        for (int cc = 0; cc < CT; cc += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(src + (r0 + r) * D + c0 + cc);
-          Dm[r][cc] += v.x;
-          Dm[r][cc + 1] += v.y;
-          Dm[r][cc + 2] += v.z;
-          Dm[r][cc + 3] += v.w;
+        for (int i = 0; i < CP; i += 2) {
+          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(src + (r0 + r) * D + c0 + 2 * i);
+          D2[r][i] = ptx::add2(D2[r][i], v.x);
+          D2[r][i + 1] = ptx::add2(D2[r][i + 1], v.y);
         }
     }
   }
   // psi at the last token: <D_children, S_end> + do_end . o_end
   float psi = 0.f;
   {
-    float s = 0.f;
+    uint64_t s2 = 0ull;
 #pragma unroll
     for (int r = 0; r < RT; ++r)
 #pragma unroll
-      for (int c = 0; c < CT; ++c) s = fmaf(Dm[r][c], S[r][c], s);
+      for (int i = 0; i < CP; ++i) s2 = ptx::fma2(D2[r][i], S2[r][i], s2);
+    float s = pair_sum(s2);
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
     if (lane == 0) sm.red[warp] = s;
@@ -542,102 +554,115 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
     stage(j0, nt, true);
     for (int j = nt - 1; j >= 0; --j) {
       const int jj = j0 + j;
-      float kk[CT], qq[CT], dor[RT], ur[RT];
-#pragma unroll
-      for (int c = 0; c < CT; ++c) {
-        kk[c] = sm.k[j][c0 + c];
-        qq[c] = sm.q[j][c0 + c];
-      }
+      uint64_t k2[CP], q2[CP];
+      row_pairs(sm.k[j], k2);
+      row_pairs(sm.q[j], q2);
+      float dor[RT], ur[RT];
 #pragma unroll
       for (int r = 0; r < RT; ++r) {
         dor[r] = sm.dO[j][r0 + r];
         ur[r] = sm.u[j][r0 + r];
       }
       const float a = sm.alpha[j], b = sm.beta[j];
+      const uint64_t a2 = ptx::f2(a, a);
       // D_t: add this token's output term
 #pragma unroll
-      for (int r = 0; r < RT; ++r)
+      for (int r = 0; r < RT; ++r) {
+        const uint64_t d2 = ptx::f2(dor[r], dor[r]);
 #pragma unroll
-        for (int c = 0; c < CT; ++c) Dm[r][c] = fmaf(dor[r], qq[c], Dm[r][c]);
+        for (int i = 0; i < CP; ++i) D2[r][i] = ptx::fma2(d2, q2[i], D2[r][i]);
+      }
       float y[RT];
 #pragma unroll
       for (int r = 0; r < RT; ++r) {
-        float acc = 0.f;
+        uint64_t acc = 0ull;
 #pragma unroll
-        for (int c = 0; c < CT; ++c) acc = fmaf(Dm[r][c], kk[c], acc);
-        y[r] = rowsum(acc);
+        for (int i = 0; i < CP; ++i) acc = ptx::fma2(D2[r][i], k2[i], acc);
+        y[r] = rowsum(pair_sum(acc));
       }
-      float pq[CT], pk[CT];
+      uint64_t pq[CP], pk[CP];
 #pragma unroll
-      for (int c = 0; c < CT; ++c) {
-        float aq = 0.f, ak = 0.f;
+      for (int i = 0; i < CP; ++i) {
+        uint64_t aq = 0ull, ak = 0ull;
 #pragma unroll
         for (int r = 0; r < RT; ++r) {
-          aq = fmaf(S[r][c], dor[r], aq);
-          ak = fmaf(Dm[r][c], ur[r], ak);
+          aq = ptx::fma2(S2[r][i], ptx::f2(dor[r], dor[r]), aq);
+          ak = ptx::fma2(D2[r][i], ptx::f2(ur[r], ur[r]), ak);
         }
-        pq[c] = aq;
-        pk[c] = ak;
+        pq[i] = aq;
+        pk[i] = ak;
       }
       // S_{t-1}
       if (jj % kCk == 0) {
-        tile_load(S, ck_ptr(slot0 + jj / kCk));
+        tile_load(S2, ck_ptr(slot0 + jj / kCk));
         amp = 1.f;
       } else {
         const float ia = 1.f / a;
         if (amp * ia > kAmpLimit) {
-          // replay from the checkpoint of this block up to token jj - 1
+          // replay from the checkpoint of this block up to token jj - 1,
+          // with the same operations as pass A
           const int jb = (jj / kCk) * kCk;
-          tile_load(S, ck_ptr(slot0 + jj / kCk));
+          tile_load(S2, ck_ptr(slot0 + jj / kCk));
           for (int m = jb; m < jj; ++m) {
             const int64_t f = start + m, tok = off + m;
             const float am = __expf(__ldg(p.g + f * p.H + h));
             const float ikm = p.invk[tok * p.H + h];
-            float km[CT], um[RT];
+            const uint64_t am2 = ptx::f2(am, am);
+            uint64_t km[CP];
 #pragma unroll
-            for (int c = 0; c < CT; ++c) km[c] = __bfloat162float(p.k[f * p.ld_qk + h * D + c0 + c]) * ikm;
+            for (int i = 0; i < CP; ++i)
+              km[i] = ptx::f2(__bfloat162float(p.k[f * p.ld_qk + h * D + c0 + 2 * i]) * ikm,
+                              __bfloat162float(p.k[f * p.ld_qk + h * D + c0 + 2 * i + 1]) * ikm);
 #pragma unroll
-            for (int r = 0; r < RT; ++r) um[r] = p.U[tok * HD + h * D + r0 + r];
+            for (int r = 0; r < RT; ++r) {
+              const float um = p.U[tok * HD + h * D + r0 + r];
+              const uint64_t um2 = ptx::f2(um, um);
 #pragma unroll
-            for (int r = 0; r < RT; ++r)
-#pragma unroll
-              for (int c = 0; c < CT; ++c) S[r][c] = fmaf(um[r], km[c], am * S[r][c]);
+              for (int i = 0; i < CP; ++i) S2[r][i] = ptx::fma2(um2, km[i], ptx::mul2(am2, S2[r][i]));
+            }
           }
           amp = 1.f;
         } else {
+          const uint64_t ia2 = ptx::f2(ia, ia);
 #pragma unroll
-          for (int r = 0; r < RT; ++r)
+          for (int r = 0; r < RT; ++r) {
+            const uint64_t nu2 = ptx::f2(-ur[r], -ur[r]);
 #pragma unroll
-            for (int c = 0; c < CT; ++c) S[r][c] = (S[r][c] - ur[r] * kk[c]) * ia;
+            for (int i = 0; i < CP; ++i) S2[r][i] = ptx::mul2(ptx::fma2(nu2, k2[i], S2[r][i]), ia2);
+          }
           amp *= ia;
         }
       }
-      const float ab = a * b;
+      {
+        const float ab = a * b;
+        const uint64_t nab2 = ptx::f2(-ab, -ab);
 #pragma unroll
-      for (int c = 0; c < CT; ++c) {
-        float acc = 0.f;
+        for (int i = 0; i < CP; ++i) {
+          uint64_t acc = 0ull;
 #pragma unroll
-        for (int r = 0; r < RT; ++r) acc = fmaf(S[r][c], y[r], acc);
-        pk[c] = fmaf(-ab, acc, pk[c]);
+          for (int r = 0; r < RT; ++r) acc = ptx::fma2(S2[r][i], ptx::f2(y[r], y[r]), acc);
+          pk[i] = ptx::fma2(nab2, acc, pk[i]);
+        }
       }
       // D_{t-1} without the previous token's output term
 #pragma unroll
       for (int r = 0; r < RT; ++r) {
         const float by = b * y[r];
+        const uint64_t nby2 = ptx::f2(-by, -by);
 #pragma unroll
-        for (int c = 0; c < CT; ++c) Dm[r][c] = a * fmaf(-by, kk[c], Dm[r][c]);
+        for (int i = 0; i < CP; ++i) D2[r][i] = ptx::mul2(a2, ptx::fma2(nby2, k2[i], D2[r][i]));
       }
       // column partials of the two row tiles of this warp, then to shared
 #pragma unroll
-      for (int c = 0; c < CT; ++c) {
-        pq[c] += __shfl_xor_sync(0xffffffffu, pq[c], 16);
-        pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], 16);
+      for (int i = 0; i < CP; ++i) {
+        pq[i] = ptx::add2(pq[i], __shfl_xor_sync(0xffffffffu, pq[i], 16));
+        pk[i] = ptx::add2(pk[i], __shfl_xor_sync(0xffffffffu, pk[i], 16));
       }
       if (lane < 16) {
 #pragma unroll
-        for (int c = 0; c < CT; c += 4) {
-          *reinterpret_cast<float4*>(&sm.part[j][warp][0][c0 + c]) = make_float4(pq[c], pq[c + 1], pq[c + 2], pq[c + 3]);
-          *reinterpret_cast<float4*>(&sm.part[j][warp][1][c0 + c]) = make_float4(pk[c], pk[c + 1], pk[c + 2], pk[c + 3]);
+        for (int i = 0; i < CP; i += 2) {
+          *reinterpret_cast<ulonglong2*>(&sm.part[j][warp][0][c0 + 2 * i]) = make_ulonglong2(pq[i], pq[i + 1]);
+          *reinterpret_cast<ulonglong2*>(&sm.part[j][warp][1][c0 + 2 * i]) = make_ulonglong2(pk[i], pk[i + 1]);
         }
       }
       float sy = 0.f;
@@ -703,7 +728,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
     }
   }
   // D = gradient of the initial state: the parent adds it to its own
-  if (par >= 0) tile_store(Dm, p.G + (static_cast<int64_t>(inst) * p.H + h) * D * D);
+  if (par >= 0) tile_store(D2, p.G + (static_cast<int64_t>(inst) * p.H + h) * D * D);
 }
 
 struct BwdScratch {
