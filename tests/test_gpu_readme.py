@@ -19,6 +19,7 @@ def test_readme_python_example_runs():
     torch.cuda.synchronize()
     F, R = env["F"], env["R"]
     assert env["o"].shape == (F, 16, 128) and env["o_raw"].shape == (R, 16, 128)
-    for name in ("o", "lse", "do", "dq", "dk", "dv", "o_p", "o_lo", "pq", "pk", "pv"):
+    for name in ("o", "lse", "do", "dq", "dk", "dv", "o_p", "o_lo", "pq", "pk", "pv", "go", "dy", "gdg", "gdb", "dx",
+                 "dcw"):
         assert torch.isfinite(env[name].float()).all(), name
     assert env["tok"].shape == (F,)
