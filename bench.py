@@ -54,8 +54,8 @@ LAUNCHES_PER_STEP = 8   # rope, fwd, scatter rows, scatter lse, dO sum, bwd prep
 # (first launch of each kernel; the summary is in profiles/), tagged with a
 # digest of the kernel and planner sources they were built from.  Once those
 # differ the figure no longer describes the kernel and is reported as null.
-TRAFFIC = {"digest": "29dafe4c75302e09c91a5e0f10cf7f24417bba68c3c0a3370f6a747d9b9c94be",
-           "fwd": 173525838080, "bwd_dkdv": 475601425920, "bwd_dq": 268955221248}
+TRAFFIC = {"digest": "100edcac35ca9338fcb582255699e5ceff033039501fb48da7ae28a266c0c8d8",
+           "fwd": 175401812480, "bwd_dkdv": 478771346944, "bwd_dq": 274274299136}
 
 
 # the sources that decide the recorded kernels' memory traffic: the attention
