@@ -287,7 +287,7 @@ void launch_conv_bwd(const int32_t* par, const int32_t* dep, const int32_t* sub,
 
 // ------------------------------------------------------------- delta rule
 constexpr int kBT = 256;          // threads
-constexpr int kRT = 8;            // tokens per staged round (one per warp in the epilogue)
+constexpr int kRT = 16;           // tokens per staged round
 constexpr int kCk = 32;           // checkpoint interval (tokens); a multiple of kRT
 constexpr float kAmpLimit = 64.f; // largest growth of the reversal's error before a replay
 
@@ -312,6 +312,8 @@ struct BwdSm {
   float k[kRT][D], q[kRT][D], v[kRT][D], dO[kRT][D], u[kRT][D], w[kRT][D], y[kRT][D];
   float part[kRT][8][2][D];   // per-warp column partials of dq~ and dk^
   float alpha[kRT], beta[kRT], ik[kRT], iq[kRT], vy[kRT], wy[kRT];
+  float dot[kRT + 1];   // do . o of the round's tokens and of the token before it (pass B)
+  float dgo[kRT];
   float dotp[kRT][8];
   float red[8];
 };
@@ -407,6 +409,10 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
       const int64_t f = start + j0 + t;
       sm.alpha[t] = __expf(__ldg(p.g + f * p.H + h));
       sm.beta[t] = __ldg(p.beta + f * p.H + h);
+    }
+    if (with_uw && t <= nt) {   // dot[i] = do . o of token j0 - 1 + i
+      const int jj = j0 - 1 + t;
+      sm.dot[t] = jj >= 0 ? p.dotv[(static_cast<int64_t>(off) + jj) * p.H + h] : 0.f;
     }
     __syncthreads();
     for (int j = warp; j < nt; j += kBT / 32) {
@@ -672,9 +678,8 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
       if (ct < RT) sm.y[j][r0 + ct] = sy;
     }
     __syncthreads();
-    // epilogue: warp j finishes token j of the round
-    if (warp < nt) {
-      const int j = warp;
+    // epilogue: warp w finishes tokens w, w + 8 of the round
+    for (int j = warp; j < nt; j += kBT / 32) {
       const int64_t f = start + j0 + j;
       float qd = 0.f, kd = 0.f, vy = 0.f, wy = 0.f;
       float gq[D / 32], gk[D / 32];
@@ -716,15 +721,18 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
       }
     }
     __syncthreads();
-    if (t == 0) {   // psi runs backwards through the round
+    if (t == 0) {   // psi runs backwards through the round, in shared memory
       for (int j = nt - 1; j >= 0; --j) {
-        const int jj = j0 + j;
-        const int64_t f = start + jj;
         const float dg = psi - sm.beta[j] * sm.vy[j];
-        p.dg[f * p.H + h] = dg;
-        p.dbeta[f * p.H + h] = sm.vy[j] - sm.alpha[j] * sm.wy[j];
-        if (jj > 0) psi = dg + p.dotv[(static_cast<int64_t>(off) + jj - 1) * p.H + h];
+        sm.dgo[j] = dg;
+        psi = dg + sm.dot[j];   // + do . o of token j0 + j - 1 (0 before the first)
       }
+    }
+    __syncthreads();
+    if (t < nt) {
+      const int64_t f = start + j0 + t;
+      p.dg[f * p.H + h] = sm.dgo[t];
+      p.dbeta[f * p.H + h] = sm.vy[t] - sm.alpha[t] * sm.wy[t];
     }
   }
   // D = gradient of the initial state: the parent adds it to its own
