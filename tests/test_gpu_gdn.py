@@ -327,3 +327,25 @@ def test_gdn_conv_bwd_full_size_sampled(ops):
     rest = torch.ones(F, dtype=torch.bool, device="cuda")
     rest[pt] = False
     assert not bool(dx[rest].any())
+
+
+@pytest.mark.parametrize("width", [1, 2, 3, 5, 8])
+def test_gdn_conv_widths(ops, width):
+    """Every compiled window width other than 4: the convolution and its
+    backward against the oracle on a ragged tree with forks (a fork within
+    W - 1 steps below a position sends its dx through the general walk)."""
+    w = SMALL["ragged_d64_gqa2"]()
+    plan, dp, ref = _plans(ops, w)
+    F, C = plan.info["n_fwd"], 3 * 2 * 64
+    x, wc, _, _ = wrng.gdn_inputs(w.seed_base + 90 + width, F, C, 2, width, "cuda")
+    dy = wrng.normal_bf16(w.seed_base + 95 + width, (F, C), "cuda")
+    y = ops.gdn_conv(dp, x, wc)
+    dx, dw = ops.gdn_conv_bwd(dp, x, wc, dy)
+    torch.cuda.synchronize()
+    yr = og.conv(ref, f64(x), f64(wc))
+    err = np.abs(f64(y) - yr)
+    record("W=%d gdn conv" % width, max_abs=float(err.max()))
+    assert np.all(err <= 2.0 ** -7 * np.abs(yr) + 1e-5)
+    rdx, rdw = og.conv_bwd(ref, f64(x), f64(wc), f64(dy))
+    assert_close(f64(dx), rdx, "W=%d gdn conv bwd dx" % width)
+    assert_close(f64(dw), rdw, "W=%d gdn conv bwd dw" % width)
