@@ -41,8 +41,9 @@
 // checkpoint instead.  D starts as the sum of the children's initial-state
 // gradients (ascending child order), plus nothing at a leaf.
 //
-// State layout: D x D tiles, 256 threads = 16 x 16 tiles of (D/16)^2; warp w
-// holds row tiles 2w, 2w+1, lanes 0-15 / 16-31, column tile = lane & 15.
+// State layout: D x D, 256 threads = 16 row tiles x 16 column tiles; warp w
+// holds row tiles 2w, 2w+1 (lanes 0-15 / 16-31), column tile = lane & 15,
+// whose columns are every 16th 16-byte chunk starting at chunk lane & 15.
 // Row contractions (S k, S q, D k) reduce over the 16 lanes of a half warp;
 // column contractions (S^T do, D^T u, S^T y) reduce over the two half warps
 // and then over the 8 warps through shared memory, once per round of kRT
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
   const int h = static_cast<int>(blockIdx.x) % p.H;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int ct = lane & 15, rt = 2 * warp + (lane >> 4);
-  const int r0 = rt * RT, c0 = ct * CT;
+  const int r0 = rt * RT;
   const int start = __ldg(p.seg_start + inst), len = __ldg(p.seg_len + inst);
   const int par = __ldg(p.seg_parent + inst);
   const int off = __ldg(p.seg_off + inst);
@@ -335,16 +336,20 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
   const int64_t HD = static_cast<int64_t>(p.H) * D;
   if (len <= 0) return;
 
-  // S and D as packed fp32 pairs along the columns: S2[r][i] = columns
-  // c0 + 2i, c0 + 2i + 1 of row r0 + r (two lanes per f32x2 instruction)
+  // S and D as packed fp32 pairs along the columns (two lanes per f32x2
+  // instruction): S2[r][i] = columns colp(i), colp(i) + 1 of row r0 + r.  A
+  // thread's columns are the 16-byte chunks ct, ct + 16, .. (4 columns
+  // each), so the 16 column tiles of a half warp read one contiguous run of
+  // a staged row and write one of the partial sums (no bank conflicts)
   constexpr int CP = CT / 2;
+  auto colp = [&](int i) { return 4 * (ct + 16 * (i >> 1)) + 2 * (i & 1); };
   uint64_t S2[RT][CP], D2[RT][CP];
   auto tile_load = [&](uint64_t (&M)[RT][CP], const float* base) {   // base: [D][D] row-major
 #pragma unroll
     for (int r = 0; r < RT; ++r)
 #pragma unroll
       for (int i = 0; i < CP; i += 2) {
-        const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(base + (r0 + r) * D + c0 + 2 * i);
+        const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(base + (r0 + r) * D + colp(i));
         M[r][i] = v.x;
         M[r][i + 1] = v.y;
       }
@@ -354,18 +359,18 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
     for (int r = 0; r < RT; ++r)
 #pragma unroll
       for (int i = 0; i < CP; i += 2)
-        *reinterpret_cast<ulonglong2*>(base + (r0 + r) * D + c0 + 2 * i) = make_ulonglong2(M[r][i], M[r][i + 1]);
+        *reinterpret_cast<ulonglong2*>(base + (r0 + r) * D + colp(i)) = make_ulonglong2(M[r][i], M[r][i + 1]);
   };
   auto pair_sum = [](uint64_t v) {
     float lo, hi;
     ptx::unf2(v, lo, hi);
     return lo + hi;
   };
-  // columns c0 .. c0 + CT - 1 of a staged row as pairs
+  // this thread's columns of a staged row as pairs
   auto row_pairs = [&](const float* rowp, uint64_t (&out)[CP]) {
 #pragma unroll
     for (int i = 0; i < CP; i += 2) {
-      const ulonglong2 v = ptx::lds128u(rowp + c0 + 2 * i);
+      const ulonglong2 v = ptx::lds128u(rowp + colp(i));
       out[i] = v.x;
       out[i + 1] = v.y;
     }
@@ -527,7 +532,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
       for (int r = 0; r < RT; ++r)
 #pragma unroll
         for (int i = 0; i < CP; i += 2) {
-          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(src + (r0 + r) * D + c0 + 2 * i);
+          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(src + (r0 + r) * D + colp(i));
           D2[r][i] = ptx::add2(D2[r][i], v.x);
           D2[r][i + 1] = ptx::add2(D2[r][i + 1], v.y);
         }
@@ -617,8 +622,8 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
             uint64_t km[CP];
 #pragma unroll
             for (int i = 0; i < CP; ++i)
-              km[i] = ptx::f2(__bfloat162float(p.k[f * p.ld_qk + h * D + c0 + 2 * i]) * ikm,
-                              __bfloat162float(p.k[f * p.ld_qk + h * D + c0 + 2 * i + 1]) * ikm);
+              km[i] = ptx::f2(__bfloat162float(p.k[f * p.ld_qk + h * D + colp(i)]) * ikm,
+                              __bfloat162float(p.k[f * p.ld_qk + h * D + colp(i) + 1]) * ikm);
 #pragma unroll
             for (int r = 0; r < RT; ++r) {
               const float um = p.U[tok * HD + h * D + r0 + r];
@@ -667,8 +672,8 @@ __global__ void __launch_bounds__(kBT, 1) gdn_delta_bwd_kernel(const GdnBwdParam
       if (lane < 16) {
 #pragma unroll
         for (int i = 0; i < CP; i += 2) {
-          *reinterpret_cast<ulonglong2*>(&sm.part[j][warp][0][c0 + 2 * i]) = make_ulonglong2(pq[i], pq[i + 1]);
-          *reinterpret_cast<ulonglong2*>(&sm.part[j][warp][1][c0 + 2 * i]) = make_ulonglong2(pk[i], pk[i + 1]);
+          *reinterpret_cast<ulonglong2*>(&sm.part[j][warp][0][colp(i)]) = make_ulonglong2(pq[i], pq[i + 1]);
+          *reinterpret_cast<ulonglong2*>(&sm.part[j][warp][1][colp(i)]) = make_ulonglong2(pk[i], pk[i + 1]);
         }
       }
       float sy = 0.f;
