@@ -347,3 +347,61 @@ def test_shape_checks_before_any_launch(lib, monkeypatch):
     # right shapes, host tensors: refused as such (there is no CPU path)
     raises(lambda: ops.tree_attn_fwd(dp, q, k, v), "must be a CUDA tensor")
     raises(lambda: bwd(), "must be a CUDA tensor")
+
+
+def test_gdn_shape_checks_before_any_launch(lib, monkeypatch):
+    """The GDN wrappers (forward and backward) check every tensor against
+    the plan and each other before calling the library."""
+    import types
+    import torch
+    from prefix_tree_packed_dfs_gb300 import binding as B
+    from prefix_tree_packed_dfs_gb300 import ops
+
+    class NoKernels:
+        """The real library, with its GDN entry points (not the size queries) replaced by a trap."""
+        def __getattr__(self, name):
+            if name.startswith("tpk_gdn_") and not name.endswith("_bytes"):
+                raise AssertionError("%s reached despite a bad argument" % name)
+            return getattr(lib, name)
+    monkeypatch.setattr(B, "load", lambda *a, **k: NoKernels())
+    w = workloads.get("tiny_fit")
+    plan = _cpp_plan(w.sequences, min_shared=w.min_shared, cap=w.row_capacity)
+    F = plan.info["n_fwd"]
+    dp = types.SimpleNamespace(plan=plan, n_fwd=F, image=torch.empty(256, dtype=torch.uint8))
+    H, d, W = 2, 64, 4
+    C = 3 * H * d
+    bf = dict(dtype=torch.bfloat16)
+    x, dy = torch.zeros(F, C, **bf), torch.zeros(F, C, **bf)
+    wc = torch.zeros(C, W)
+    y = torch.zeros(F, C, **bf)
+    q, k, v = (y[:, i * H * d:(i + 1) * H * d].unflatten(1, (H, d)) for i in range(3))
+    g, b = torch.zeros(F, H), torch.zeros(F, H)
+    do = torch.zeros(F, H, d, **bf)
+    state = torch.empty(int(lib.tpk_gdn_workspace_bytes(plan.handle, H, d, d)) + 256, dtype=torch.uint8)
+
+    def raises(fn, what, exc=ValueError):
+        with pytest.raises(exc, match=what):
+            fn()
+    # convolution backward
+    raises(lambda: ops.gdn_conv_bwd(dp, x[:-1], wc, dy[:-1]), "forwarded positions")
+    raises(lambda: ops.gdn_conv_bwd(dp, x, wc[:-1].contiguous(), dy), "w must have shape")
+    raises(lambda: ops.gdn_conv_bwd(dp, x, wc, dy[:, :8].contiguous()), "dy must have shape")
+    raises(lambda: ops.gdn_conv_bwd(dp, x, wc, dy, dx=dy[:-1]), "dx must have shape")
+    raises(lambda: ops.gdn_conv_bwd(dp, x, wc, dy, dw=wc[:, :1].contiguous()), "dw must have shape")
+    raises(lambda: ops.gdn_conv_bwd(dp, x, wc, dy, workspace=torch.empty(16, dtype=torch.uint8)),
+           "workspace has 16 bytes")
+    raises(lambda: ops.gdn_conv_bwd(dp, x, wc, dy), "must be a CUDA tensor")
+    # delta rule backward
+    bwd = lambda **kw: ops.gdn_delta_rule_bwd(dp, kw.get("q", q), k, v, kw.get("g", g), b, kw.get("do", do),
+                                              kw.get("state", state), dq=kw.get("dq"), dk=kw.get("dk"),
+                                              dv=kw.get("dv"), dg=kw.get("dg"), workspace=kw.get("ws"))
+    raises(lambda: bwd(q=q[:-1]), "forwarded positions")
+    raises(lambda: bwd(g=g[:, :1].contiguous()), "g must have shape")
+    raises(lambda: bwd(do=do[:-1]), "dout must have shape")
+    raises(lambda: bwd(dq=torch.zeros(F, H, d + 8, **bf)), "dq must have shape")
+    raises(lambda: bwd(dv=torch.zeros(F, H + 1, d, **bf)), "dv must have shape")
+    raises(lambda: bwd(dk=torch.zeros(F, H, d // 2, **bf)), "dk must have shape")
+    raises(lambda: bwd(dg=torch.zeros(F, H + 1)), "dg must have shape")
+    raises(lambda: bwd(state=torch.empty(16, dtype=torch.uint8)), "state has 16 bytes")
+    raises(lambda: bwd(ws=torch.empty(16, dtype=torch.uint8)), "workspace has 16 bytes")
+    raises(lambda: bwd(), "must be a CUDA tensor")
