@@ -349,3 +349,48 @@ def test_gdn_conv_widths(ops, width):
     rdx, rdw = og.conv_bwd(ref, f64(x), f64(wc), f64(dy))
     assert_close(f64(dx), rdx, "W=%d gdn conv bwd dx" % width)
     assert_close(f64(dw), rdw, "W=%d gdn conv bwd dw" % width)
+
+
+def _edge_tree():
+    """Sequences over one 80-token base, cut at 1, 2, 16, 31, 32, 33, 47 and
+    64 tokens (segment boundaries on either side of the kernels' 16-token
+    rounds and 32-token checkpoints), then tails of 1 to 40 tokens; four
+    sequences share the 32-token cut (a position with four children), and
+    two are one token long."""
+    rng = np.random.Generator(np.random.PCG64(4321))
+    base = rng.integers(0, 50, size=80)
+    seqs = [base[:1].copy(), base[:1].copy()]
+    for cut, tail in [(2, 1), (16, 5), (31, 33), (32, 1), (32, 16), (32, 40), (32, 2), (33, 31), (47, 17), (64, 3),
+                      (80, 0)]:
+        t = rng.integers(50, 100, size=tail)
+        seqs.append(np.concatenate([base[:cut], t]).astype(np.int32))
+    return [np.asarray(s, dtype=np.int32) for s in seqs]
+
+
+def test_gdn_edge_segments(ops):
+    """Forward and backward on the crafted tree (minimum shared run 1), with
+    a width-4 convolution: every boundary case of the level schedule and of
+    the backward's rounds and checkpoints against the oracle."""
+    seqs = _edge_tree()
+    plan = ops.Plan.from_sequences(seqs, row_capacity=4096, min_shared=1)
+    dp = plan.to_device()
+    ref = op.plan(seqs, min_shared=1, row_capacity=4096)
+    assert plan.info["n_fwd"] == ref["n_fwd"]
+    F, H, d = plan.info["n_fwd"], 2, 64
+    lens = np.asarray(ref["seg_len"])
+    assert lens.min() == 1 and plan.info["n_seg_levels"] >= 3
+    x, wc, g, b = wrng.gdn_inputs(777, F, 3 * H * d, H, W, "cuda")
+    dO = wrng.normal_bf16(778, (F, H, d), "cuda")
+    y = ops.gdn_conv(dp, x, wc)
+    o, dy, dg, db = _bwd_layer(ops, dp, y, g, b, H, d, dO)
+    dx, dw = ops.gdn_conv_bwd(dp, x, wc, dy)
+    torch.cuda.synchronize()
+    qn, kn, vn = (f64(t) for t in _split(y, H, d, d))
+    assert_close(f64(o), og.delta_rule(ref, qn, kn, vn, f64(g), f64(b)), "edge gdn delta rule")
+    grads = og.delta_rule_bwd(ref, qn, kn, vn, f64(g), f64(b), f64(dO))
+    dq, dk, dv = _split(dy, H, d, d)
+    for got, want, n in zip((dq, dk, dv, dg, db), grads, ("dq", "dk", "dv", "dg", "dbeta")):
+        assert_close(f64(got), want, "edge gdn bwd %s" % n)
+    rdx, rdw = og.conv_bwd(ref, f64(x), f64(wc), f64(dy))
+    assert_close(f64(dx), rdx, "edge gdn conv bwd dx")
+    assert_close(f64(dw), rdw, "edge gdn conv bwd dw")
