@@ -487,7 +487,8 @@ size_t tpk_gdn_workspace_bytes(const tpk_plan* plan, int32_t H, int32_t dk, int3
  *   o      [F, H, dv] bf16 (contiguous)
  *   (dk, dv) in {(64, 64), (128, 128)}; scale > 0 (usually 1/sqrt(dk))
  *   workspace: >= tpk_gdn_workspace_bytes bytes, 256-byte aligned; need not be
- *   cleared.
+ *   cleared.  It holds the final states of the chains that have children
+ *   afterwards: keep it unchanged for tpk_gdn_delta_rule_bwd (its `state`).
  * Pointers and strides must give 16-byte aligned rows (TPK_E_ARG). */
 int tpk_gdn_delta_rule(const tpk_plan* plan, const void* dev_image, const void* q, const void* k, const void* v,
                        int64_t ld_qk, int64_t ld_v, const float* g, const float* beta, void* o, int32_t H,
